@@ -1,0 +1,1054 @@
+// frame_kernel.cu -- one codec frame of the lockstep multi-codebook decode as
+// a single persistent kernel: one CTA per SM walks the frame's stage program
+// (Talker layers, codebook-0 head + projection, sampler, 15 Code-Predictor
+// steps) and the CTAs meet at a grid-wide barrier between dependent stages.
+//
+// The stage sequence follows "Qwen3-TTS Native v0.3.0", section "What
+// changed" (one batched call runs the talker and the 15-step code predictor
+// for every active session, each shared weight read once per frame) and
+// "De grens van snelheid en kosten verleggen voor Qwen3-TTS", section 3
+// (the Code Predictor's fixed 15 steps over a pre-allocated short cache).
+// The pages' engines replay ~1,600 kernels per frame as a CUDA graph; here the
+// whole frame is one launch, so the only per-stage cost is the barrier.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "qtts_internal.h"
+
+namespace qtts {
+
+// ---------------------------------------------------------------------------
+// helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf2f(uint32_t h16) { return __uint_as_float(h16 << 16); }
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// streaming read-only load of weights: never written while a frame runs
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+  uint2 v;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ int read_err(const int* e) { return *(const volatile int*)e; }
+__device__ __forceinline__ void set_err(int* e, int code) { atomicCAS(e, 0, code); }
+
+constexpr uint64_t kBarrierTimeoutNs = 2000000000ull;  // 2 s: a frame takes milliseconds
+
+// Grid-wide barrier with a bounded wait. Every CTA adds one to the counter and
+// waits for `target`; a wait that outlives the limit sets QTTS_DEV_TIMEOUT,
+// and any error word set elsewhere also ends the wait. Returns false to make
+// the CTA leave the frame.
+__device__ bool grid_sync(const Globals& g, unsigned target, volatile int* sflag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(g.barrier, 1u);
+    int ok = 1;
+    const uint64_t t0 = global_timer_ns();
+    unsigned spins = 0;
+    while (ld_acquire_gpu(g.barrier) < target) {
+      if (read_err(g.err)) {
+        ok = 0;
+        break;
+      }
+      if ((++spins & 63u) == 0u && global_timer_ns() - t0 > kBarrierTimeoutNs) {
+        set_err(g.err, QTTS_DEV_TIMEOUT);
+        ok = 0;
+        break;
+      }
+    }
+    __threadfence();
+    *sflag = ok;
+  }
+  __syncthreads();
+  return *sflag != 0;
+}
+
+// deterministic block sum (fixed combination order)
+__device__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kWarps; ++w) t += red[w];
+    red[kWarps] = t;
+  }
+  __syncthreads();
+  return red[kWarps];
+}
+
+// ---------------------------------------------------------------------------
+// sampler arithmetic: Philox4x32-10 and a binary32 log written for this
+// project so that any two implementations of the same steps agree bit for bit
+// ---------------------------------------------------------------------------
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of two 32x32
+// multiplies with a Weyl-sequence key schedule.
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
+    const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
+    const uint32_t n0 = hi1 ^ c[1] ^ k0;
+    const uint32_t n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// ln(x) for finite x > 0: x = m 2^k with m in (sqrt(1/2), sqrt(2)], then
+// ln m = 2 atanh(s), s = (m-1)/(m+1), atanh(s) = s (1 + s^2/3 + ... + s^10/11).
+// Each step is one correctly rounded binary32 operation (no contraction).
+__device__ float log_series_f32(float x) {
+  uint32_t u = __float_as_uint(x);
+  int k = 0;
+  if (((u >> 23) & 0xFFu) == 0u) {
+    x = __fmul_rn(x, 33554432.0f);  // 2^25, exact
+    u = __float_as_uint(x);
+    k = -25;
+  }
+  k += (int)((u >> 23) & 0xFFu) - 127;
+  uint32_t mb = (u & 0x007FFFFFu) | 0x3F800000u;
+  if (mb > 0x3FB504F3u) {
+    mb = (u & 0x007FFFFFu) | 0x3F000000u;
+    k += 1;
+  }
+  const float m = __uint_as_float(mb);
+  const float s = __fdiv_rn(__fsub_rn(m, 1.0f), __fadd_rn(m, 1.0f));
+  const float s2 = __fmul_rn(s, s);
+  float t = 0x1.745d18p-4f;                          // 1/11
+  t = __fadd_rn(__fmul_rn(t, s2), 0x1.c71c72p-4f);  // 1/9
+  t = __fadd_rn(__fmul_rn(t, s2), 0x1.24924ap-3f);  // 1/7
+  t = __fadd_rn(__fmul_rn(t, s2), 0x1.99999ap-3f);  // 1/5
+  t = __fadd_rn(__fmul_rn(t, s2), 0x1.555556p-2f);  // 1/3
+  t = __fadd_rn(__fmul_rn(t, s2), 1.0f);
+  const float lm = __fmul_rn(__fadd_rn(s, s), t);
+  return __fadd_rn(__fmul_rn(__int2float_rn(k), 0x1.62e430p-1f), lm);  // k ln2 + ln m
+}
+
+// Gumbel noise -ln(-ln u) for vocabulary id v of codebook j, u from word v&3
+// of Philox(key, (v>>2, j, frame_ctr, 0)): u = (top 23 bits + 1/2) 2^-23.
+__device__ __forceinline__ float gumbel(uint32_t key0, uint32_t key1, int j, uint32_t fctr, int v) {
+  uint32_t c[4] = {(uint32_t)v >> 2, (uint32_t)j, fctr, 0u};
+  philox4x32_10(c, key0, key1);
+  const uint32_t w = c[v & 3];
+  const float u = __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
+  const float l1 = log_series_f32(u);
+  const float l2 = log_series_f32(-l1);
+  return -l2;
+}
+
+// order-preserving map of a binary32 value to uint32 (-0 and +0 map together)
+__device__ __forceinline__ uint32_t order_key(float z) {
+  uint32_t u = __float_as_uint(z);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// (val, id) is better than (bv, bid): larger value, then smaller id
+__device__ __forceinline__ bool better(bool have, float val, int id, bool bhave, float bv, int bid) {
+  if (!have) return false;
+  if (!bhave) return true;
+  return val > bv || (val == bv && id < bid);
+}
+
+// Block-wide arg-best over (have, val, id); every thread gets the winner.
+__device__ int block_argbest(bool have, float val, int id, float* redv, int* redi, int* redh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, val, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, id, o);
+    const bool oh = __shfl_xor_sync(0xffffffffu, (int)have, o) != 0;
+    if (better(oh, ov, oi, have, val, id)) {
+      val = ov;
+      id = oi;
+      have = oh;
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    redv[warp] = val;
+    redi[warp] = id;
+    redh[warp] = have;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool bh = false;
+    float bv = 0.f;
+    int bi = 0;
+    for (int w = 0; w < kWarps; ++w)
+      if (better(redh[w] != 0, redv[w], redi[w], bh, bv, bi)) {
+        bh = redh[w] != 0;
+        bv = redv[w];
+        bi = redi[w];
+      }
+    redi[kWarps] = bi;
+  }
+  __syncthreads();
+  return redi[kWarps];
+}
+
+// ---------------------------------------------------------------------------
+// shared sampler core: one row of raw logits -> one code
+//   1. codebook 0: ids >= n_codes other than eos -> -inf; eos -> -inf unless
+//      allowed; repetition penalty on the seen set ("Qwen3-TTS PR 5", "Graph":
+//      group 0 sampler with repetition penalty; "Known gaps": seen tokens)
+//   2. greedy (T == 0 or top_k == 1): argmax, lowest id on ties
+//   3. z = l / T, keep the top_k ids by (z desc, id asc) via a radix select
+//   4. Gumbel-max over the kept ids, lowest id on ties
+// ---------------------------------------------------------------------------
+
+struct SampleSmem {
+  float lp[kMaxVocab];
+  uint32_t key[kMaxVocab];
+  int hist[256];
+  int scan[kThreads];
+  float redv[kWarps + 1];
+  int redi[kWarps + 1];
+  int redh[kWarps + 1];
+  uint32_t sel_prefix;
+  int sel_rem;
+};
+
+__device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, int j, const qtts_session& ss,
+                          uint32_t key0, uint32_t key1, uint32_t fctr, const uint32_t* seen, int eos_id,
+                          int n_codes) {
+  const int tid = threadIdx.x;
+  float T;
+  int k;
+  if (j == 0) {
+    T = ss.temperature;
+    k = ss.top_k;
+  } else {
+    T = ss.cp_temperature;
+    k = ss.cp_top_k;
+  }
+  for (int v = tid; v < V; v += kThreads) {
+    float l = row_cg ? __ldcg(row + v) : row[v];
+    if (j == 0) {
+      if (v >= n_codes && v != eos_id) l = -INFINITY;
+      if (v == eos_id && !ss.eos_allowed) l = -INFINITY;
+      if (seen && ((seen[v >> 5] >> (v & 31)) & 1u))
+        l = (l > 0.0f) ? __fdiv_rn(l, ss.rep_penalty) : __fmul_rn(l, ss.rep_penalty);
+    }
+    S.lp[v] = l;
+  }
+  __syncthreads();
+
+  // contiguous id block per thread, visited in ascending order
+  const int per = (V + kThreads - 1) / kThreads;
+  const int v0 = min(V, tid * per), v1 = min(V, v0 + per);
+
+  if (T == 0.0f || k == 1) {
+    bool have = false;
+    float bv = 0.f;
+    int bi = 0;
+    for (int v = v0; v < v1; ++v)
+      if (better(true, S.lp[v], v, have, bv, bi)) {
+        have = true;
+        bv = S.lp[v];
+        bi = v;
+      }
+    return block_argbest(have, bv, bi, S.redv, S.redi, S.redh);
+  }
+
+  if (k <= 0 || k > V) k = V;
+  for (int v = tid; v < V; v += kThreads) {
+    float z = __fdiv_rn(S.lp[v], T);
+    if (z == 0.0f) z = 0.0f;
+    S.lp[v] = z;
+    S.key[v] = order_key(z);
+  }
+  __syncthreads();
+
+  const bool take_all = (k == V);
+  uint32_t thr = 0u;
+  int rem = 0;
+  if (!take_all) {
+    // MSB-first radix select of the k-th largest key
+    uint32_t prefix = 0u, pmask = 0u;
+    rem = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (tid < 256) S.hist[tid] = 0;
+      __syncthreads();
+      for (int v = tid; v < V; v += kThreads) {
+        const uint32_t kk = S.key[v];
+        if ((kk & pmask) == prefix) atomicAdd(&S.hist[(kk >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      if (tid < 32) {
+        // lane L owns digits 255-8L .. 248-8L (descending)
+        int part = 0;
+        for (int i = 0; i < 8; ++i) part += S.hist[255 - 8 * tid - i];
+        int incl = part;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (tid >= o) incl += t;
+        }
+        const int excl = incl - part;
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
+        const int L = __ffs(hit) - 1;
+        if (tid == L) {
+          int cum = excl;
+          int dsel = 255 - 8 * L - 7;
+          for (int i = 0; i < 8; ++i) {
+            const int dd = 255 - 8 * L - i;
+            if (cum + S.hist[dd] >= rem) {
+              dsel = dd;
+              break;
+            }
+            cum += S.hist[dd];
+          }
+          S.sel_prefix = prefix | ((uint32_t)dsel << shift);
+          S.sel_rem = rem - cum;
+        }
+      }
+      __syncthreads();
+      prefix = S.sel_prefix;
+      rem = S.sel_rem;
+      pmask |= 255u << shift;
+      __syncthreads();
+    }
+    thr = prefix;  // k-th largest key; `rem` ties with it are kept, lowest ids first
+  }
+
+  // exclusive scan of per-thread tie counts gives each tie its rank by id
+  int ties = 0;
+  if (!take_all)
+    for (int v = v0; v < v1; ++v) ties += (S.key[v] == thr);
+  S.scan[tid] = ties;
+  __syncthreads();
+  for (int o = 1; o < kThreads; o <<= 1) {
+    const int t = (tid >= o) ? S.scan[tid - o] : 0;
+    __syncthreads();
+    S.scan[tid] += t;
+    __syncthreads();
+  }
+  int rank = S.scan[tid] - ties;
+
+  bool have = false;
+  float bv = 0.f;
+  int bi = 0;
+  for (int v = v0; v < v1; ++v) {
+    bool cand = take_all;
+    if (!take_all) {
+      const uint32_t kk = S.key[v];
+      if (kk > thr) {
+        cand = true;
+      } else if (kk == thr) {
+        cand = rank < rem;
+        ++rank;
+      }
+    }
+    if (cand) {
+      const float val = __fadd_rn(S.lp[v], gumbel(key0, key1, j, fctr, v));
+      if (better(true, val, v, have, bv, bi)) {
+        have = true;
+        bv = val;
+        bi = v;
+      }
+    }
+  }
+  return block_argbest(have, bv, bi, S.redv, S.redi, S.redh);
+}
+
+// ---------------------------------------------------------------------------
+// stage: begin -- validate every session (each CTA reaches the same verdict
+// from the same data, so no CTA waits on a barrier the others skipped), reset
+// the attention counters, load the Talker inputs
+// ---------------------------------------------------------------------------
+
+__device__ bool stage_begin(const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+  const int tid = threadIdx.x;
+  int bad = 0;
+  for (int b = tid; b < fa.B; b += kThreads) {
+    const qtts_session s = fa.sess[b];
+    const int kv = s.kv_len;
+    if (kv < 0 || kv + 1 > g.max_context || kv + 1 > fa.bt_stride * kPage) bad = QTTS_DEV_BAD_SESSION;
+    if (!(s.temperature >= 0.f) || !isfinite(s.temperature) || !(s.cp_temperature >= 0.f) ||
+        !isfinite(s.cp_temperature) || !(s.rep_penalty > 0.f) || !isfinite(s.rep_penalty))
+      bad = QTTS_DEV_BAD_SAMPLING;
+  }
+  for (int b = 0; b < fa.B; ++b) {
+    const int kv = fa.sess[b].kv_len;
+    if (kv < 0 || kv + 1 > fa.bt_stride * kPage) continue;  // reported above
+    const int np = kv / kPage + 1;
+    for (int p = tid; p < np; p += kThreads) {
+      const int page = fa.bt[(size_t)b * fa.bt_stride + p];
+      if (page < 0 || page >= g.pool_pages) bad = QTTS_DEV_BAD_PAGE;
+    }
+  }
+  if (fa.forced)
+    for (int i = tid; i < fa.B * kCodebooks; i += kThreads) {
+      const int c = fa.forced[i];
+      const int V = (i % kCodebooks) == 0 ? g.V0 : g.Vc;
+      if (c < 0 || c >= V) bad = QTTS_DEV_BAD_CODE;
+    }
+  if (bad && blockIdx.x == 0) set_err(g.err, bad);
+  if (__syncthreads_or(bad)) return false;
+
+  if (blockIdx.x == 0)
+    for (int i = tid; i < kMaxBatch * g.nkv; i += kThreads) g.attn_cnt[i] = 0;
+
+  float* red = (float*)smem;
+  const int b = blockIdx.x;
+  float ss = 0.f;
+  if (b < fa.B) {
+    for (int k = tid; k < g.H; k += kThreads) {
+      const float x = bf2f(fa.in_embeds[(size_t)b * g.H + k]);
+      g.x_t[(size_t)b * g.H + k] = x;
+      ss += x * x;
+    }
+  }
+  ss = block_sum(ss, red);
+  for (int r = tid; r < fa.B; r += kThreads) g.ssq_t[(size_t)blockIdx.x * kMaxRows + r] = (r == b) ? ss : 0.f;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// stage: GEMV with a fused prologue (RMSNorm) and epilogues
+//   Y[rows, N] = X[rows, K] W[N, K]^T, W streamed once for all rows.
+// Each CTA owns a contiguous range of row units; each warp walks its units,
+// lanes striding K in 8-element (16-byte bf16 / 8-byte int8) vectors.
+// ---------------------------------------------------------------------------
+
+struct GemvSmemTail {
+  float rfac[8];
+  float ssq_w[kWarps * kMaxRows];
+};
+
+template <typename WT>
+__device__ __forceinline__ void load_w8(const WT* base, float out[8]);
+
+template <>
+__device__ __forceinline__ void load_w8<uint16_t>(const uint16_t* p, float o[8]) {
+  const uint4 v = ld_stream16(p);
+  o[0] = bf_lo(v.x); o[1] = bf_hi(v.x); o[2] = bf_lo(v.y); o[3] = bf_hi(v.y);
+  o[4] = bf_lo(v.z); o[5] = bf_hi(v.z); o[6] = bf_lo(v.w); o[7] = bf_hi(v.w);
+}
+template <>
+__device__ __forceinline__ void load_w8<int8_t>(const int8_t* p, float o[8]) {
+  const uint2 v = ld_stream8(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = (float)(int)(int8_t)((v.x >> (8 * i)) & 0xFFu);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[4 + i] = (float)(int)(int8_t)((v.y >> (8 * i)) & 0xFFu);
+}
+
+struct RowMap {
+  int rps, in_rps, in_off;
+  __device__ int in_row(int r) const { return (r / rps) * in_rps + in_off + (r % rps); }
+};
+
+__device__ __forceinline__ int out_row_of(const Seg& sg, int rps, int r) {
+  return (r / rps) * sg.out_rps + sg.out_off + (r % rps);
+}
+
+__device__ __forceinline__ uint16_t* talker_kv_ptr(const Globals& g, const FrameArgs& fa, int layer, int b,
+                                                    int pos, int kv, int head) {
+  int page = fa.bt[(size_t)b * fa.bt_stride + pos / kPage];
+  if (page < 0 || page >= g.pool_pages) {  // validated in stage_begin; stay in bounds regardless
+    set_err(g.err, QTTS_DEV_BAD_PAGE);
+    page = 0;
+  }
+  return g.kv_pool +
+         (((((size_t)layer * g.pool_pages + page) * 2 + kv) * g.nkv + head) * kPage + pos % kPage) * g.d;
+}
+
+__device__ __forceinline__ uint16_t* cp_kv_ptr(const Globals& g, uint16_t* layer_base, int b, int pos, int kv,
+                                                int head) {
+  return layer_base + ((((size_t)b * 2 + kv) * kCodebooks + pos) * g.nkvc + head) * g.dc;
+}
+
+// Epilogue for one output unit (rows n0, n0+1 when U == 2) of stage row r.
+__device__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, int n0,
+                              float y0, float y1, int r, float& ssq_acc) {
+  const int b = r / d.rps, p = r % d.rps;
+  const int orow = out_row_of(sg, d.rps, r);
+  switch (sg.epi) {
+    case E_QKV_T:
+    case E_QKV_CP: {
+      const bool talker = sg.epi == E_QKV_T;
+      const int hd = talker ? g.d : g.dc;
+      const int nq = talker ? g.nq : g.nqc;
+      const int nkv = talker ? g.nkv : g.nkvc;
+      const int pos = talker ? fa.sess[b].kv_len : d.pos_base + p;
+      const int half = hd / 2;
+      if (n0 < (nq + nkv) * hd) {
+        // rows arrive as rotate-half pairs (i, i + hd/2) of one head
+        const bool is_q = n0 < nq * hd;
+        const int rel = is_q ? n0 : n0 - nq * hd;
+        const int head = rel / hd, i = (rel % hd) / 2;
+        const float c = talker ? g.rope_cos[(size_t)pos * half + i] : g.cp_rope_cos[pos * half + i];
+        const float s = talker ? g.rope_sin[(size_t)pos * half + i] : g.cp_rope_sin[pos * half + i];
+        const float o0 = y0 * c - y1 * s;
+        const float o1 = y1 * c + y0 * s;
+        if (is_q) {
+          float* q = sg.out + (size_t)orow * sg.out_stride + head * hd;
+          q[i] = o0;
+          q[i + half] = o1;
+        } else {
+          uint16_t* kp =
+              talker ? talker_kv_ptr(g, fa, d.layer, b, pos, 0, head) : cp_kv_ptr(g, d.cp_kv, b, pos, 0, head);
+          kp[i] = f2bf(o0);
+          kp[i + half] = f2bf(o1);
+        }
+      } else {
+        const int rel = n0 - (nq + nkv) * hd;
+        const int head = rel / hd, e = rel % hd;
+        uint16_t* vp =
+            talker ? talker_kv_ptr(g, fa, d.layer, b, pos, 1, head) : cp_kv_ptr(g, d.cp_kv, b, pos, 1, head);
+        vp[e] = f2bf(y0);
+        vp[e + 1] = f2bf(y1);
+      }
+      break;
+    }
+    case E_RESID: {
+      float* x = sg.out + (size_t)orow * sg.out_stride + n0;
+      const float v = __ldcg(x) + y0;
+      *x = v;
+      ssq_acc += v * v;
+      break;
+    }
+    case E_SWIGLU: {
+      const float silu = y0 / (1.0f + expf(-y0));
+      sg.out[(size_t)orow * sg.out_stride + n0 / 2] = silu * y1;
+      break;
+    }
+    case E_LOGITS: {
+      sg.out[(size_t)orow * sg.out_stride + n0] = y0;
+      if (fa.logits_out) fa.logits_out[((size_t)b * kCodebooks + d.codebook) * g.V0 + n0] = y0;
+      break;
+    }
+    case E_CPIN: {
+      float v = y0;
+      if (sg.bias) v += bf2f(sg.bias[n0]);
+      sg.out[(size_t)orow * sg.out_stride + n0] = v;
+      ssq_acc += v * v;
+      break;
+    }
+  }
+}
+
+template <typename WT, int U, int RT>
+__device__ void gemv_seg(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, const float* xs,
+                         int r0, int nr, float* ssq_w) {
+  const int K = d.K;
+  const int units = sg.N / U;
+  const int u0 = (int)((long long)units * blockIdx.x / gridDim.x);
+  const int u1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WT* W = (const WT*)sg.w;
+  float ssq_acc = 0.f;
+  for (int u = u0 + warp; u < u1; u += kWarps) {
+    const int n0 = u * U;
+    float acc[U][RT];
+#pragma unroll
+    for (int i = 0; i < U; ++i)
+#pragma unroll
+      for (int r = 0; r < RT; ++r) acc[i][r] = 0.f;
+#pragma unroll 2
+    for (int k = lane * 8; k < K; k += 256) {
+      float wv[U][8];
+#pragma unroll
+      for (int i = 0; i < U; ++i) load_w8<WT>(W + (size_t)(n0 + i) * K + k, wv[i]);
+#pragma unroll
+      for (int r = 0; r < RT; ++r) {
+        if (r < nr) {
+          const float4 a = *reinterpret_cast<const float4*>(xs + r * K + k);
+          const float4 c = *reinterpret_cast<const float4*>(xs + r * K + k + 4);
+#pragma unroll
+          for (int i = 0; i < U; ++i) {
+            float t = acc[i][r];
+            t = fmaf(wv[i][0], a.x, t);
+            t = fmaf(wv[i][1], a.y, t);
+            t = fmaf(wv[i][2], a.z, t);
+            t = fmaf(wv[i][3], a.w, t);
+            t = fmaf(wv[i][4], c.x, t);
+            t = fmaf(wv[i][5], c.y, t);
+            t = fmaf(wv[i][6], c.z, t);
+            t = fmaf(wv[i][7], c.w, t);
+            acc[i][r] = t;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i)
+#pragma unroll
+      for (int r = 0; r < RT; ++r) acc[i][r] = warp_sum(acc[i][r]);
+    if (sg.scale) {
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        const float sc = sg.scale[n0 + i];
+#pragma unroll
+        for (int r = 0; r < RT; ++r) acc[i][r] *= sc;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+      if (lane == r && r < nr)
+        gemv_epilogue(d, sg, g, fa, n0, acc[0][r], U == 2 ? acc[U - 1][r] : 0.f, r0 + r, ssq_acc);
+  }
+  if (lane < nr) ssq_w[warp * kMaxRows + r0 + lane] += ssq_acc;
+}
+
+template <typename WT, int U>
+__device__ void gemv_seg_rt(int RT, const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa,
+                            const float* xs, int r0, int nr, float* ssq_w) {
+  switch (RT) {
+    case 1: gemv_seg<WT, U, 1>(d, sg, g, fa, xs, r0, nr, ssq_w); break;
+    case 2: gemv_seg<WT, U, 2>(d, sg, g, fa, xs, r0, nr, ssq_w); break;
+    case 4: gemv_seg<WT, U, 4>(d, sg, g, fa, xs, r0, nr, ssq_w); break;
+    default: gemv_seg<WT, U, 8>(d, sg, g, fa, xs, r0, nr, ssq_w); break;
+  }
+}
+
+__device__ void stage_gemv(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+  const int tid = threadIdx.x;
+  const int rows = fa.B * d.rps;
+  const int K = d.K;
+  float* xs = (float*)smem;
+  GemvSmemTail* tail = (GemvSmemTail*)(smem + kSmemX);
+  for (int i = tid; i < kWarps * kMaxRows; i += kThreads) tail->ssq_w[i] = 0.f;
+
+  int RT = kSmemX / (K * 4);
+  RT = RT >= 8 ? 8 : RT >= 4 ? 4 : RT >= 2 ? 2 : 1;
+  while (RT > 1 && RT / 2 >= rows) RT /= 2;
+  const RowMap rm{d.rps, d.in_rps, d.in_off};
+
+  for (int r0 = 0; r0 < rows; r0 += RT) {
+    const int nr = min(RT, rows - r0);
+    __syncthreads();
+    if (d.xsrc == X_NORM) {
+      const int warp = tid >> 5, lane = tid & 31;
+      if (warp < nr) {
+        const int ir = rm.in_row(r0 + warp);
+        float s = 0.f;
+        for (int c = lane; c < g.G; c += 32) s += __ldcg(d.ssq + (size_t)c * kMaxRows + ir);
+        s = warp_sum(s);
+        if (lane == 0) tail->rfac[warp] = 1.0f / sqrtf(s / (float)K + g.eps);
+      }
+      __syncthreads();
+    }
+    for (int idx = tid * 4; idx < nr * K; idx += kThreads * 4) {
+      const int r = idx / K, k = idx % K;
+      const int ir = rm.in_row(r0 + r);
+      float4 v = __ldcg(reinterpret_cast<const float4*>(d.x + (size_t)ir * d.x_stride + k));
+      if (d.xsrc == X_NORM) {
+        const float f = tail->rfac[r];
+        const uint2 gw = *reinterpret_cast<const uint2*>(d.gain + k);
+        v.x = v.x * f * bf_lo(gw.x);
+        v.y = v.y * f * bf_hi(gw.x);
+        v.z = v.z * f * bf_lo(gw.y);
+        v.w = v.w * f * bf_hi(gw.y);
+      }
+      *reinterpret_cast<float4*>(xs + r * K + k) = v;
+    }
+    __syncthreads();
+    for (int s = 0; s < d.nseg; ++s) {
+      const Seg& sg = d.seg[s];
+      if (sg.scale) {
+        if (sg.unit == 2) gemv_seg_rt<int8_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail->ssq_w);
+        else gemv_seg_rt<int8_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail->ssq_w);
+      } else {
+        if (sg.unit == 2) gemv_seg_rt<uint16_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail->ssq_w);
+        else gemv_seg_rt<uint16_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail->ssq_w);
+      }
+    }
+  }
+  __syncthreads();
+  for (int s = 0; s < d.nseg; ++s) {
+    const Seg& sg = d.seg[s];
+    if (!sg.ssq_out) continue;
+    for (int r = tid; r < rows; r += kThreads) {
+      float t = 0.f;
+      for (int w = 0; w < kWarps; ++w) t += tail->ssq_w[w * kMaxRows + r];
+      sg.ssq_out[(size_t)blockIdx.x * kMaxRows + out_row_of(sg, d.rps, r)] = t;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// attention: one warp per (row, kv head[, split]); lanes own positions for
+// the scores and head dimensions for the value sum; online softmax
+// ---------------------------------------------------------------------------
+
+template <int HD, int GRP>
+struct AttnAcc {
+  float o[GRP][HD / 32];
+  float m[GRP], l[GRP];
+};
+
+template <int HD, int GRP, typename KPtr, typename VPtr>
+__device__ void attn_warp(const float* qs, int p0, int p1, float scale, KPtr kptr, VPtr vptr,
+                          AttnAcc<HD, GRP>& A) {
+  const int lane = threadIdx.x & 31;
+  constexpr int E = HD / 32;
+#pragma unroll
+  for (int j = 0; j < GRP; ++j) {
+    A.m[j] = -INFINITY;
+    A.l[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) A.o[j][e] = 0.f;
+  }
+  for (int base = p0; base < p1; base += 32) {
+    const int p = base + lane;
+    const bool valid = p < p1;
+    float sc[GRP];
+#pragma unroll
+    for (int j = 0; j < GRP; ++j) sc[j] = 0.f;
+    if (valid) {
+      const uint16_t* kp = kptr(p);
+#pragma unroll 4
+      for (int t = 0; t < HD; t += 8) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(kp + t);
+        const float k8[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
+                             bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
+#pragma unroll
+        for (int j = 0; j < GRP; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sc[j] = fmaf(qs[j * HD + t + e], k8[e], sc[j]);
+      }
+    }
+    float pj[GRP];
+#pragma unroll
+    for (int j = 0; j < GRP; ++j) {
+      const float s = valid ? sc[j] * scale : -INFINITY;
+      const float mnew = fmaxf(A.m[j], warp_max(s));
+      const float corr = expf(A.m[j] - mnew);
+      pj[j] = valid ? expf(s - mnew) : 0.f;
+      A.l[j] = A.l[j] * corr + warp_sum(pj[j]);
+#pragma unroll
+      for (int e = 0; e < E; ++e) A.o[j][e] *= corr;
+      A.m[j] = mnew;
+    }
+    const int nvalid = min(32, p1 - base);
+    for (int i = 0; i < nvalid; ++i) {
+      const uint16_t* vp = vptr(base + i) + lane * E;
+      float v[E];
+      if constexpr (E == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(vp);
+        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = bf2f(vp[e]);
+      }
+#pragma unroll
+      for (int j = 0; j < GRP; ++j) {
+        const float pij = __shfl_sync(0xffffffffu, pj[j], i);
+#pragma unroll
+        for (int e = 0; e < E; ++e) A.o[j][e] = fmaf(pij, v[e], A.o[j][e]);
+      }
+    }
+  }
+}
+
+template <int HD, int GRP>
+__device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int E = HD / 32;
+  const int nkv = g.nkv;
+  const int qstride = d.q_stride;
+  // split plan: identical on every CTA (same inputs, same arithmetic)
+  const int len = lane < fa.B ? fa.sess[lane].kv_len + 1 : 0;
+  int total = len;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  const int target = g.G * kWarps;
+  int chunk = (total * nkv + target - 1) / target;
+  chunk = ((chunk + 31) / 32) * 32;
+  if (chunk < kMinChunk) chunk = kMinChunk;
+  const int nsp = (len + chunk - 1) / chunk;
+  int incl = nsp * nkv;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int n_items = __shfl_sync(0xffffffffu, incl, 31);
+  float* qs = (float*)smem + warp * GRP * HD;
+  const float scale = rsqrtf((float)HD);
+  const int layer = d.layer;
+
+  for (int item = blockIdx.x * kWarps + warp; item < n_items; item += g.G * kWarps) {
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > item);
+    const int b = __ffs(hit) - 1;
+    const int before = __shfl_sync(0xffffffffu, incl - nsp * nkv, b);
+    const int nsp_b = __shfl_sync(0xffffffffu, nsp, b);
+    const int len_b = __shfl_sync(0xffffffffu, len, b);
+    const int rem = item - before;
+    const int kvh = rem / nsp_b, sp = rem % nsp_b;
+    const int p0 = sp * chunk, p1 = min(p0 + chunk, len_b);
+    const float* qsrc = d.q + (size_t)b * qstride + kvh * GRP * HD;
+    for (int e = lane; e < GRP * HD; e += 32) qs[e] = __ldcg(qsrc + e);
+    __syncwarp();
+    AttnAcc<HD, GRP> A;
+    attn_warp<HD, GRP>(
+        qs, p0, p1, scale, [&](int p) { return (const uint16_t*)talker_kv_ptr(g, fa, layer, b, p, 0, kvh); },
+        [&](int p) { return (const uint16_t*)talker_kv_ptr(g, fa, layer, b, p, 1, kvh); }, A);
+    float* out = d.attn_out + (size_t)b * qstride + kvh * GRP * HD;
+    if (nsp_b == 1) {
+#pragma unroll
+      for (int j = 0; j < GRP; ++j)
+#pragma unroll
+        for (int e = 0; e < E; ++e) out[j * HD + lane * E + e] = A.o[j][e] / A.l[j];
+    } else {
+      // partial (m, l, o) per query head; the last split to finish combines
+      float* part = g.attn_part + ((((size_t)b * nkv + kvh) * kMaxSplits + sp) * GRP) * (HD + 2);
+#pragma unroll
+      for (int j = 0; j < GRP; ++j) {
+        float* pj = part + j * (HD + 2);
+        if (lane == 0) {
+          pj[0] = A.m[j];
+          pj[1] = A.l[j];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) pj[2 + lane * E + e] = A.o[j][e];
+      }
+      __threadfence();
+      __syncwarp();
+      int old = 0;
+      if (lane == 0) old = atomicAdd(&g.attn_cnt[b * nkv + kvh], 1);
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if (old == nsp_b - 1) {
+        __threadfence();
+        const float* base = g.attn_part + ((((size_t)b * nkv + kvh) * kMaxSplits) * GRP) * (HD + 2);
+#pragma unroll
+        for (int j = 0; j < GRP; ++j) {
+          float M = -INFINITY;
+          for (int s = 0; s < nsp_b; ++s) M = fmaxf(M, __ldcg(base + ((size_t)s * GRP + j) * (HD + 2)));
+          float L = 0.f;
+          float o[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[e] = 0.f;
+          for (int s = 0; s < nsp_b; ++s) {
+            const float* ps = base + ((size_t)s * GRP + j) * (HD + 2);
+            const float w = expf(__ldcg(ps) - M);
+            L += w * __ldcg(ps + 1);
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] += w * __ldcg(ps + 2 + lane * E + e);
+          }
+#pragma unroll
+          for (int e = 0; e < E; ++e) out[j * HD + lane * E + e] = o[e] / L;
+        }
+        if (lane == 0) g.attn_cnt[b * nkv + kvh] = 0;  // ready for the next layer
+      }
+    }
+    __syncwarp();
+  }
+}
+
+template <int HD, int GRP>
+__device__ void stage_attn_cp(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int E = HD / 32;
+  const int nkv = g.nkvc;
+  const int qstride = d.q_stride;
+  const int rows = fa.B * d.rps;
+  float* qs = (float*)smem + warp * GRP * HD;
+  const float scale = rsqrtf((float)HD);
+  for (int item = blockIdx.x * kWarps + warp; item < rows * nkv; item += g.G * kWarps) {
+    const int r = item / nkv, kvh = item % nkv;
+    const int b = r / d.rps, p = r % d.rps;
+    const int pos = d.pos_base + p;
+    const float* qsrc = d.q + (size_t)r * qstride + kvh * GRP * HD;
+    for (int e = lane; e < GRP * HD; e += 32) qs[e] = __ldcg(qsrc + e);
+    __syncwarp();
+    AttnAcc<HD, GRP> A;
+    attn_warp<HD, GRP>(
+        qs, 0, pos + 1, scale, [&](int t) { return (const uint16_t*)cp_kv_ptr(g, d.cp_kv, b, t, 0, kvh); },
+        [&](int t) { return (const uint16_t*)cp_kv_ptr(g, d.cp_kv, b, t, 1, kvh); }, A);
+    float* out = d.attn_out + (size_t)r * qstride + kvh * GRP * HD;
+#pragma unroll
+    for (int j = 0; j < GRP; ++j)
+#pragma unroll
+      for (int e = 0; e < E; ++e) out[j * HD + lane * E + e] = A.o[j][e] / A.l[j];
+    __syncwarp();
+  }
+}
+
+template <bool TALKER>
+__device__ void stage_attn(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+  const int hd = TALKER ? g.d : g.dc;
+  const int grp = TALKER ? g.nq / g.nkv : g.nqc / g.nkvc;
+#define QTTS_ATTN_CASE(H_, G_)                             \
+  if (hd == H_ && grp == G_) {                             \
+    if (TALKER) stage_attn_talker<H_, G_>(d, g, fa, smem); \
+    else stage_attn_cp<H_, G_>(d, g, fa, smem);            \
+    return;                                                \
+  }
+  QTTS_ATTN_CASE(128, 2)
+  QTTS_ATTN_CASE(64, 2)
+  QTTS_ATTN_CASE(128, 1)
+  QTTS_ATTN_CASE(64, 1)
+  QTTS_ATTN_CASE(128, 4)
+  QTTS_ATTN_CASE(64, 4)
+#undef QTTS_ATTN_CASE
+}
+
+// ---------------------------------------------------------------------------
+// stage: sampler for codebook j (one CTA per session), then the next
+// Code-Predictor input: the projected embedding row T_j[c] of the committed
+// code, with its sum of squares for the next stage's RMSNorm
+// ---------------------------------------------------------------------------
+
+__device__ void stage_sample(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+  const int b = blockIdx.x;
+  if (b >= fa.B) return;
+  SampleSmem& S = *reinterpret_cast<SampleSmem*>(smem);
+  const int j = d.codebook;
+  const qtts_session ss = fa.sess[b];
+  const qtts_rng rs = fa.rng[b];
+  const uint32_t* seen = (j == 0 && fa.seen) ? fa.seen + (size_t)b * g.seen_words : nullptr;
+  const int code = sample_row(S, g.logits + (size_t)b * g.V0, true, d.V, j, ss, rs.key0, rs.key1, rs.frame_ctr,
+                              seen, g.eos_id, g.n_codes);
+  const int committed = fa.forced ? fa.forced[(size_t)b * kCodebooks + j] : code;
+  if (threadIdx.x == 0) {
+    fa.codes_out[(size_t)b * kCodebooks + j] = code;
+    g.committed[(size_t)b * kCodebooks + j] = committed;
+    if (j == 0) {
+      if (fa.seen) fa.seen[(size_t)b * g.seen_words + (committed >> 5)] |= 1u << (committed & 31);
+      fa.eos_out[b] = (uint8_t)(code == g.eos_id);
+      fa.sess[b].kv_len = ss.kv_len + 1;
+    }
+    if (j == kCodebooks - 1) fa.rng[b].frame_ctr = rs.frame_ctr + 1u;
+  }
+  if (d.table) {
+    const int row = b * d.next_rps + d.next_off;
+    const float* src = d.table + (size_t)committed * g.Hc;
+    float* dst = d.x_next + (size_t)row * g.Hc;
+    float s = 0.f;
+    for (int k = threadIdx.x; k < g.Hc; k += kThreads) {
+      const float v = src[k];
+      dst[k] = v;
+      s += v * v;
+    }
+    s = block_sum(s, S.redv);
+    for (int c = threadIdx.x; c < g.G; c += kThreads) d.ssq_next[(size_t)c * kMaxRows + row] = (c == 0) ? s : 0.f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the persistent frame kernel
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads, 1)
+    frame_kernel(const StageDesc* __restrict__ prog, int s0, int s1, Globals g, FrameArgs fa) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int sflag;
+  if (read_err(g.err)) return;  // a device error is sticky until qtts_frame_status clears it
+  unsigned bar = 0;
+  for (int s = s0; s < s1; ++s) {
+    const StageDesc& d = prog[s];
+    switch (d.type) {
+      case ST_BEGIN:
+        if (!stage_begin(g, fa, smem)) return;
+        break;
+      case ST_GEMV: stage_gemv(d, g, fa, smem); break;
+      case ST_ATTN_T: stage_attn<true>(d, g, fa, smem); break;
+      case ST_ATTN_CP: stage_attn<false>(d, g, fa, smem); break;
+      case ST_SAMPLE: stage_sample(d, g, fa, smem); break;
+      default: break;
+    }
+    if (s + 1 < s1) {
+      bar += gridDim.x;
+      if (!grid_sync(g, bar, &sflag)) return;
+    }
+  }
+}
+
+// Sampling of caller-supplied logits [B][V] for codebook j (one CTA per
+// session): the same sampler the frame uses, without the next-input gather.
+__global__ void __launch_bounds__(kThreads, 1)
+    sample_kernel(const float* __restrict__ logits, int V, int j, Globals g, FrameArgs fa) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int b = blockIdx.x;
+  SampleSmem& S = *reinterpret_cast<SampleSmem*>(smem);
+  const qtts_session ss = fa.sess[b];
+  const qtts_rng rs = fa.rng[b];
+  const uint32_t* seen = (j == 0 && fa.seen) ? fa.seen + (size_t)b * g.seen_words : nullptr;
+  const int code = sample_row(S, logits + (size_t)b * V, false, V, j, ss, rs.key0, rs.key1, rs.frame_ctr, seen,
+                              g.eos_id, g.n_codes);
+  if (threadIdx.x == 0) fa.codes_out[b] = code;
+}
+
+cudaError_t frame_kernel_setup() {
+  cudaError_t e = cudaFuncSetAttribute(frame_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SampleSmem));
+}
+
+cudaError_t frame_kernel_occupancy(int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, frame_kernel, kThreads, kSmemBytes);
+}
+
+cudaError_t launch_frame(const StageDesc* prog, int n_stages, const Globals& g, const FrameArgs& fa, bool stepwise,
+                         cudaStream_t stream) {
+  if (stepwise) {
+    for (int s = 0; s < n_stages; ++s) {
+      frame_kernel<<<g.G, kThreads, kSmemBytes, stream>>>(prog, s, s + 1, g, fa);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  cudaError_t e = cudaMemsetAsync(g.barrier, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  int s0 = 0, s1 = n_stages;
+  Globals gg = g;
+  FrameArgs ff = fa;
+  void* args[] = {(void*)&prog, (void*)&s0, (void*)&s1, (void*)&gg, (void*)&ff};
+  return cudaLaunchCooperativeKernel((const void*)frame_kernel, dim3(g.G), dim3(kThreads), args, kSmemBytes, stream);
+}
+
+cudaError_t launch_sample(const float* logits, int V, int j, const Globals& g, const FrameArgs& fa,
+                          cudaStream_t stream) {
+  sample_kernel<<<fa.B, kThreads, sizeof(SampleSmem), stream>>>(logits, V, j, g, fa);
+  return cudaGetLastError();
+}
+
+}  // namespace qtts

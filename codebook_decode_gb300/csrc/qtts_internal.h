@@ -1,0 +1,138 @@
+// Internal declarations shared by the library's CUDA translation units.
+// Nothing here is part of the C ABI (include/qtts.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qtts.h"
+
+namespace qtts {
+
+constexpr int kThreads = 512;            // one persistent CTA per SM
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxBatch = 32;
+constexpr int kMaxRows = 2 * kMaxBatch;  // Code-Predictor step 1 runs two positions per session
+constexpr int kCodebooks = 16;
+constexpr int kPage = 16;
+constexpr int kMaxSplits = 64;           // split-K pieces per (session, kv head) in Talker attention
+constexpr int kMinChunk = 32;            // positions per split, at least one warp-tile
+constexpr int kMaxContext = kMaxSplits * kMinChunk;
+constexpr int kSmemX = 128 * 1024;       // GEMV activation tile (fp32 rows)
+constexpr int kSmemBytes = kSmemX + 16 * 1024;
+constexpr int kMaxVocab = 4096;
+
+enum StageType { ST_BEGIN = 0, ST_GEMV = 1, ST_ATTN_T = 2, ST_ATTN_CP = 3, ST_SAMPLE = 4 };
+enum XSrc { X_NORM = 0, X_PLAIN = 1 };
+enum Epi { E_QKV_T = 0, E_QKV_CP = 1, E_RESID = 2, E_SWIGLU = 3, E_LOGITS = 4, E_CPIN = 5 };
+
+// One weight segment of a GEMV stage: rows [0, N) of W, split over the grid
+// in units of `unit` rows, each finished by epilogue `epi`.
+struct Seg {
+  const void* w;          // bf16 [N][K] or int8 [N][K]
+  const float* scale;     // int8 per-row scale; nullptr for bf16
+  int N;
+  int unit;               // 2: rows come in (RoPE pair | gate,up | v pair) pairs
+  int epi;
+  float* out;             // destination rows (see Epi)
+  int out_stride;         // floats per destination row
+  int out_rps, out_off;   // destination row of (session b, position p) = b*out_rps + out_off + p
+  float* ssq_out;         // E_RESID / E_CPIN: per-CTA sum-of-squares partials [G][kMaxRows]
+  const uint16_t* bias;   // E_CPIN: optional bf16 bias [N]
+};
+
+struct StageDesc {
+  int type;
+  int rps;                // rows (positions) per session this stage works on
+  int pos_base;           // Code-Predictor position of row p of a session: pos_base + p
+  int layer;
+  int codebook;           // head / sample stages
+  // GEMV input X [rows][K]
+  int K;
+  int xsrc;
+  int in_rps, in_off;     // input row of (b, p) = b*in_rps + in_off + p
+  int x_stride;           // floats per input row
+  const float* x;
+  const float* ssq;       // X_NORM: partials [G][kMaxRows] of the input rows
+  const uint16_t* gain;   // X_NORM gain [K]
+  int nseg;
+  Seg seg[2];
+  // attention: q [rows][q_stride] in, attn_out [rows][q_stride] out
+  const float* q;
+  float* attn_out;
+  int q_stride;
+  uint16_t* cp_kv;        // Code-Predictor cache of this layer [kMaxBatch][2][16][nkv][d]
+  // sampler
+  int V;
+  const float* table;     // projected embedding table T_j [V_j][Hc] fp32 (nullptr for j = 15)
+  float* x_next;
+  float* ssq_next;
+  int next_rps, next_off;
+};
+
+// Model-constant device pointers and sizes, passed by value to the kernel.
+struct Globals {
+  int H, nq, nkv, d, F, V0;
+  int Hc, nqc, nkvc, dc, Fc, Vc;
+  int eos_id, n_codes, seen_words, max_context;
+  float eps;
+  int G;                  // persistent grid size (SM count)
+  uint16_t* kv_pool;      // [layer][page][2][nkv][16][d]
+  int pool_pages;
+  const float* rope_cos;  // [max_context][d/2]
+  const float* rope_sin;
+  const float* cp_rope_cos;  // [16][dc/2]
+  const float* cp_rope_sin;
+  float* x_t;             // Talker residual [kMaxBatch][H]
+  float* x_c;             // Code-Predictor residual [kMaxRows][Hc]
+  float* ssq_t;           // [G][kMaxRows]
+  float* ssq_c;
+  float* q;               // [kMaxRows][max(nq*d, nqc*dc)]
+  float* attn;            // same shape
+  float* h;               // [kMaxRows][max(F, Fc)]
+  float* logits;          // [kMaxBatch][V0]
+  float* attn_part;       // [kMaxBatch][nkv][kMaxSplits][grp][d + 2]
+  int* attn_cnt;          // [kMaxBatch][nkv]
+  int* committed;         // [kMaxBatch][16] codes fed forward (forced or sampled)
+  unsigned* barrier;      // grid barrier counter (zeroed before each persistent launch)
+  int* err;               // device error word (QTTS_DEV_*)
+};
+
+struct FrameArgs {
+  int B;
+  qtts_session* sess;
+  const int32_t* bt;
+  int bt_stride;
+  const uint16_t* in_embeds;
+  qtts_rng* rng;
+  uint32_t* seen;
+  const int32_t* forced;
+  int32_t* codes_out;
+  uint8_t* eos_out;
+  float* logits_out;
+};
+
+// frame_kernel.cu
+cudaError_t launch_frame(const StageDesc* prog, int n_stages, const Globals& g, const FrameArgs& fa,
+                         bool stepwise, cudaStream_t stream);
+cudaError_t frame_kernel_setup();
+cudaError_t frame_kernel_occupancy(int* blocks_per_sm);
+cudaError_t launch_sample(const float* logits, int V, int j, const Globals& g, const FrameArgs& fa,
+                          cudaStream_t stream);
+
+// util_kernels.cu
+cudaError_t launch_gather_rows(uint16_t* dst, const uint16_t* src, const int32_t* map, int n_rows, int K,
+                               cudaStream_t s);
+cudaError_t launch_quantize_rows(const uint16_t* w, int N, int K, int8_t* q, float* scale, cudaStream_t s);
+cudaError_t launch_project_table(const uint16_t* E, int rows, int H, const uint16_t* P, const int8_t* P8,
+                                 const float* P8s, const uint16_t* bias, int Hc, float* T, cudaStream_t s);
+cudaError_t launch_kv_scatter(uint16_t* pool, int pool_pages, int nkv, int d, int layer, int n_tok,
+                              const int32_t* pages, uint16_t* k, uint16_t* v, int to_pool, cudaStream_t s);
+struct EmbedTables {
+  const uint16_t* e[kCodebooks];
+  int rows[kCodebooks];
+};
+cudaError_t launch_feedback(int B, int H, const int32_t* codes, const uint16_t* text, EmbedTables tables,
+                            uint16_t* out, cudaStream_t s);
+
+}  // namespace qtts
