@@ -1,0 +1,344 @@
+"""Codec frames/s of the lockstep multi-codebook frame decode on GB300.
+
+One step = one frame for all B sessions of the workload (the whole hot path:
+Talker step, codebook-0 head and sampler, projection, 15 Code-Predictor steps
+with heads and samplers) followed by the free-running feedback embedding of
+the next Talker input. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload full_b1]
+  python bench.py --impl reference ...   # the CPU oracle on this host's cores
+
+Multi-GPU: the sessions are independent, so N ranks run N replicas (one model
+and B sessions each, no collective on the data path); value = all frames / the
+slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from codebook_decode_gb300 import configs, synth  # noqa: E402
+
+METRIC = "codec frames/s (sessions x frames) per GB300 at B=1/8/32; % HBM roofline"
+UNIT = "frames/s"
+
+
+def workload_desc(wl):
+    d = wl.dims
+    return (f"{wl.name}: Talker {d.n_layers}L h{d.hidden} {d.n_q_heads}q/{d.n_kv_heads}kv d{d.head_dim} "
+            f"ffn{d.ffn} V0 {d.vocab0}; proj {d.hidden}->{d.cp_hidden}; CP {d.cp_layers}L h{d.cp_hidden} "
+            f"ffn{d.cp_ffn} 15x{d.cp_vocab}; B={wl.batch}; prefix {wl.prefix}; offsets {wl.offset}; "
+            f"T {wl.temperature} top-k {wl.top_k} rep {wl.rep_penalty}; "
+            f"{'INT8' if wl.int8 else 'BF16'} weights; shuffled paged KV")
+
+
+def measured_peak_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kv_bytes_per_frame(d, kv_lens):
+    """Algorithmic cache bytes of one frame: Talker K/V read over positions
+    0..kv_len (new token included) and written at kv_len; Code-Predictor K/V
+    read over positions 0..p at each of its 16 positions and written once."""
+    t_tok = d.n_layers * 2 * d.n_kv_heads * d.head_dim * 2
+    c_tok = d.cp_layers * 2 * d.cp_n_kv_heads * d.cp_head_dim * 2
+    B = len(kv_lens)
+    read = sum(int(n) + 1 for n in kv_lens) * t_tok + B * sum(p + 1 for p in range(16)) * c_tok
+    write = B * (t_tok + 16 * c_tok)
+    return read + write
+
+
+class Clocks:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    def __init__(self, index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--id={index}", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+               "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+               "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "50"]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def run_gpu(wl, steps, warmup, local, weights):
+    import torch
+
+    from codebook_decode_gb300 import qtts
+    from codebook_decode_gb300.engine import Engine, to_dev_u16
+
+    d = wl.dims
+    sess = synth.make_sessions(wl)
+    cap = min(2048, int(sess.kv_len0.max()) + steps + warmup + 4)
+    limit = cap - int(sess.kv_len0.max()) - 2  # frames before the contexts are rewound
+    pool = wl.batch * ((cap + 15) // 16) + 8
+    eng = Engine(d, weights, max_batch=max(wl.batch, 1), max_context=cap, pool_pages=pool, device=local, int8=wl.int8)
+    eng.setup_sessions(sess, cap, shuffle=wl.shuffle_pages)
+    dev = eng.dev
+    stream = torch.cuda.current_stream()
+    sess0 = eng.sess.clone()
+    emb = to_dev_u16(sess.in_embeds(0), dev)
+    text = to_dev_u16(sess.text_embeds(0), dev)
+    nxt = torch.empty_like(emb)
+    weight_bytes = qtts.qtts_frame_weight_bytes(eng.m)
+    B = wl.batch
+
+    def step(i, inp):
+        eng.step(inp, None, want_logits=False, stream=stream)
+        qtts.qtts_feedback_embed(eng.m, B, eng.codes, text, nxt, stream)
+        return nxt
+
+    cur = emb
+    done = 0
+    for i in range(warmup):
+        cur = step(i, cur).clone()
+        done += 1
+    torch.cuda.synchronize()
+    rc, derr = qtts.qtts_frame_status(eng.m, raise_on_error=False)
+    assert rc == 0 and derr == 0, (rc, derr)
+    # average context over the timed frames, for the cache bytes
+    kv_start = eng.sess[:, 0].cpu().numpy().astype(np.int64)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    kv_bytes = 0
+    clocks = Clocks(local)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    kv_now = kv_start.copy()
+    for i in range(steps):
+        if done >= limit:  # keep every context inside the cache: rewind to the prefix
+            eng.sess.copy_(sess0)
+            kv_now = sess.kv_len0.astype(np.int64).copy()
+            done = 0
+        starts[i].record(stream)
+        eng.step(cur, None, want_logits=False, stream=stream)
+        ends[i].record(stream)
+        qtts.qtts_feedback_embed(eng.m, B, eng.codes, text, nxt, stream)
+        cur, nxt = nxt, cur
+        kv_bytes += kv_bytes_per_frame(d, kv_now)
+        kv_now += 1
+        done += 1
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    rc, derr = qtts.qtts_frame_status(eng.m, raise_on_error=False)
+    assert rc == 0 and derr == 0, (rc, derr)
+    total_ms = t0.elapsed_time(t1)
+    frame_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    avg_frame_s = statistics.mean(frame_ms) / 1e3
+    bytes_per_frame = weight_bytes + kv_bytes / steps + B * 15 * d.cp_hidden * 4
+    res = dict(total_ms=total_ms, frame_ms=statistics.mean(frame_ms), weight_bytes=weight_bytes,
+               bytes_per_frame=bytes_per_frame, achieved_gbs=bytes_per_frame / avg_frame_s / 1e9, clocks=clk)
+
+    # end to end through the host-buffer entry point: inputs copied in, codes
+    # and advanced state copied back, every frame
+    sess_h = torch.from_numpy(sess.session_array()).pin_memory().numpy()
+    bt_h = torch.from_numpy(eng.bt_host).pin_memory().numpy()
+    emb_h = torch.from_numpy(sess.in_embeds(0).view(np.int16)).pin_memory().numpy().view(np.uint16)
+    rng_h = torch.from_numpy(sess.rng_state().view(np.int32)).pin_memory().numpy()
+    seen_h = torch.from_numpy(sess.seen_bitmap().view(np.int32)).pin_memory().numpy()
+    codes_h = torch.zeros(B, 16, dtype=torch.int32).pin_memory().numpy()
+    eos_h = torch.zeros(B, dtype=torch.uint8).pin_memory().numpy()
+    sess_init = sess_h.copy()
+
+    def host_step():
+        qtts.qtts_frame_step_host(eng.m, B, sess_h, bt_h, eng.bt_stride, emb_h, rng_h, seen_h, None, codes_h, eos_h,
+                                  None, stream)
+
+    for _ in range(warmup):
+        host_step()
+    sess_h[:] = sess_init
+    e2e_steps = steps
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    n_done = 0
+    for _ in range(e2e_steps):
+        if n_done >= limit:
+            sess_h[:] = sess_init
+            n_done = 0
+        host_step()
+        n_done += 1
+    e2e_s = time.perf_counter() - t
+    h2d = sess_h.nbytes + B * eng.bt_stride * 4 + emb_h.nbytes + rng_h.nbytes + seen_h.nbytes
+    d2h = codes_h.nbytes + eos_h.nbytes + sess_h.nbytes + rng_h.nbytes + seen_h.nbytes
+    res["e2e"] = dict(value=B * e2e_steps / e2e_s, h2d=h2d, d2h=d2h)
+    eng.release_pages()
+    eng.close()
+    return res
+
+
+def oracle_sample(wl, weights, frames, threads=None):
+    """The CPU oracle on a bounded sample of the workload: `frames` teacher-forced
+    frames of the first min(B, 2) sessions. Returns (frames/s, frames, sessions)."""
+    from oracle import orc
+
+    d = wl.dims
+    sess = synth.make_sessions(wl)
+    Bs = min(wl.batch, 2)
+    O = orc.Oracle(d, weights, use_int8=wl.int8)
+    cap = int(sess.kv_len0[:Bs].max()) + frames + 2
+    rows = sess.session_array()[:Bs].copy()
+    kv = [orc.kv_cache_from_prefix(sess.prefix_kv(b), cap) for b in range(Bs)]
+    rng = sess.rng_state()[:Bs].copy()
+    seen = sess.seen_bitmap()[:Bs].copy()
+    O.frame_step(rows, kv, cap, sess.in_embeds(0)[:Bs], rng, seen, want_logits=False)  # warm-up
+    t = time.perf_counter()
+    for f in range(frames):
+        O.frame_step(rows, kv, cap, sess.in_embeds(f)[:Bs], rng, seen, want_logits=False)
+    dt = time.perf_counter() - t
+    return Bs * frames / dt, frames, Bs
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full_b1", choices=sorted(configs.WORKLOADS))
+    ap.add_argument("--no-sweep", action="store_true", help="skip the B=8/B=32/INT8 side measurements")
+    ap.add_argument("--oracle-frames", type=int, default=6)
+    args = ap.parse_args()
+    wl = configs.WORKLOADS[args.workload]
+    ws, rank, local = (1, 0, 0)
+    if args.impl == "ours" or args.gpus > 1:
+        ws, rank, local = dist_setup()
+    cores = os.cpu_count()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = synth.make_weights(wl.dims, 1000 + wl.seed)
+        t = time.perf_counter()
+        for _ in range(args.warmup):
+            oracle_sample(wl, w, 1)
+        fps, nfr, bs = oracle_sample(wl, w, args.steps)
+        ms = 1e3 * bs / fps
+        line = {"metric": METRIC, "value": fps, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": workload_desc(wl), "sessions_per_step": bs},
+                "cpu_baseline": {"value": fps, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                 "sample": f"{nfr} teacher-forced frames x {bs} sessions of {wl.name}"},
+                "e2e": {"value": fps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": time.perf_counter() - t}
+        print(json.dumps(line))
+        return
+
+    import torch
+    w = synth.make_weights(wl.dims, 1000 + wl.seed)
+    barrier(ws)
+    r = run_gpu(wl, args.steps, args.warmup, local, w)
+    total_s = max_over_ranks(r["total_ms"] / 1e3, ws)
+    value = ws * wl.batch * args.steps / total_s
+    peak, peak_kind = measured_peak_gbs()
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8" if wl.int8 else "bf16",
+            "data": "synthetic: seeded N(0,0.02) random-init weights and N(0,1) prefix KV, free-running sampling",
+            "config": {"workload": workload_desc(wl), "global_batch": ws * wl.batch,
+                       "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2: every frame streams the full weight set (GBs) through HBM"},
+            "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": r["achieved_gbs"] / peak, "traffic": None,
+                         "peak_kind": peak_kind, "kernel": "qtts::frame_kernel",
+                         "bytes_per_launch": r["bytes_per_frame"], "launch_ms": r["frame_ms"]},
+            "e2e": {"value": ws * r["e2e"]["value"], "unit": UNIT, "h2d_bytes_per_step": r["e2e"]["h2d"],
+                    "d2h_bytes_per_step": r["e2e"]["d2h"]},
+            "gpu_launches": 2 * args.steps,
+            "clocks": r["clocks"]}
+    if rank == 0:
+        fps, nfr, bs = oracle_sample(wl, w, args.oracle_frames)
+        line["cpu_baseline"] = {"value": fps, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{nfr} teacher-forced frames x {bs} session(s) of {wl.name}"}
+        if not args.no_sweep and ws == 1:
+            sweep = {}
+            for name in ("full_b8", "full_b32", "int8_b1", "int8_b32"):
+                o = configs.WORKLOADS[name]
+                rr = run_gpu(o, min(args.steps, 50), 3, local, w)  # same random-init weights
+                sweep[name] = {"frames_per_s": o.batch * min(args.steps, 50) / (rr["total_ms"] / 1e3),
+                               "frame_ms": rr["frame_ms"], "achieved_gbs": rr["achieved_gbs"],
+                               "frac": rr["achieved_gbs"] / peak, "bytes_per_frame": rr["bytes_per_frame"]}
+            line["sweep"] = sweep
+        print(json.dumps(line))
+    barrier(ws)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -14,7 +14,9 @@ arithmetic):
     N(0, 0.02) code embeddings plus text.
   * Teacher-forced codes: uniform in [0, n_codes).
 """
+import os
 import zlib
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -22,11 +24,16 @@ from .configs import Dims, PAGE_SIZE
 
 
 def bf16_bits(a):
-    """float32 array -> uint16 bf16 bit patterns, round to nearest even."""
+    """float32 array -> uint16 bf16 bit patterns, round to nearest even
+    (finite inputs)."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    u = a.view(np.uint32)
+    t = u >> np.uint32(16)
+    t &= np.uint32(1)
+    t += np.uint32(0x7FFF)
+    t += u
+    t >>= np.uint32(16)
+    return t.astype(np.uint16)
 
 
 def bf16_to_f32(h):
@@ -82,9 +89,15 @@ def make_tensor(seed, name, shape, kind, std=0.02):
     return bf16_bits(a)
 
 
-def make_weights(d: Dims, seed: int, std=0.02):
-    """dict name -> uint16 bf16 array, N(0, std) weights, 1 + N(0, std) gains."""
-    return {n: make_tensor(seed, n, s, k, std) for (n, s, k) in tensor_specs(d)}
+def make_weights(d: Dims, seed: int, std=0.02, threads=None):
+    """dict name -> uint16 bf16 array, N(0, std) weights, 1 + N(0, std) gains.
+    Each tensor has its own stream, so drawing them on several threads gives
+    the same values as drawing them one after another."""
+    specs = tensor_specs(d)
+    threads = threads or min(16, os.cpu_count() or 1)
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        arrs = list(ex.map(lambda t: make_tensor(seed, t[0], t[1], t[2], std), specs))
+    return {t[0]: a for t, a in zip(specs, arrs)}
 
 
 class Sessions:
