@@ -956,3 +956,21 @@ int qtts_frame_weight_bytes(const qtts_model* m, int64_t* bytes) {
 }
 
 }  // extern "C"
+
+// Accessors for translation units that do not see qtts_model's definition.
+namespace qtts {
+
+int model_kv_layout(qtts_model* m, KvLayout* out) {
+  if (!m || !out) return QTTS_E_INVALID;
+  out->device = m->device;
+  out->pool = m->kv_pool;
+  out->pool_pages = m->cfg.kv_pool_pages;
+  out->n_layers = m->cfg.n_layers;
+  out->nkv = m->cfg.n_kv_heads;
+  out->d = m->cfg.head_dim;
+  return QTTS_OK;
+}
+
+int model_fail(qtts_model* m, int code, const char* msg) { return fail(m, code, "%s", msg); }
+
+}  // namespace qtts

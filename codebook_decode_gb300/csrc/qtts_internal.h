@@ -135,4 +135,13 @@ struct EmbedTables {
 cudaError_t launch_feedback(int B, int H, const int32_t* codes, const uint16_t* text, EmbedTables tables,
                             uint16_t* out, cudaStream_t s);
 
+// qtts_api.cu: model internals for other translation units
+struct KvLayout {
+  int device;
+  uint16_t* pool;
+  int pool_pages, n_layers, nkv, d;
+};
+int model_kv_layout(qtts_model* m, KvLayout* out);
+int model_fail(qtts_model* m, int code, const char* msg);
+
 }  // namespace qtts

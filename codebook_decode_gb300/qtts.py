@@ -77,6 +77,7 @@ SIGNATURES = [
     ("qtts_kv_pool_free_count", C.c_int, [_P]),
     ("qtts_kv_write", C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P]),
     ("qtts_kv_read", C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P]),
+    ("qtts_kv_write_noalloc", C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P, _P]),
     ("qtts_frame_step", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
     ("qtts_frame_step_host", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
     ("qtts_frame_status", C.c_int, [_P, C.POINTER(C.c_int)]),
@@ -186,6 +187,13 @@ def qtts_kv_write(m, layer, n_tok, pages_host, k, v):
 
 def qtts_kv_read(m, layer, n_tok, pages_host, k_host, v_host):
     return _check(m, load_library().qtts_kv_read(m, layer, n_tok, ptr(pages_host), ptr(k_host), ptr(v_host)))
+
+
+def qtts_kv_write_noalloc(m, layer, n_tok, pages_host, k, v, stream=None):
+    """qtts_kv_write through the library's static staging array: no device
+    allocation, queued on `stream`."""
+    return _check(m, load_library().qtts_kv_write_noalloc(m, layer, n_tok, ptr(pages_host), ptr(k), ptr(v),
+                                                          _stream(stream)))
 
 
 def qtts_frame_step(m, B, sessions, block_tables, bt_stride, in_embeds, rng, seen, forced_codes, codes_out,

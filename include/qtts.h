@@ -179,6 +179,25 @@ int qtts_kv_write(qtts_model* m, int layer, int n_tok, const int32_t* pages_host
 int qtts_kv_read(qtts_model* m, int layer, int n_tok, const int32_t* pages_host, uint16_t* k_host,
                  uint16_t* v_host);
 
+/* qtts_kv_write for callers that must not allocate device memory. The pages
+ * have no counterpart: this is a deployment variant, not part of the method.
+ * qtts_kv_write stages K/V through buffers it cudaMallocs and cudaFrees on
+ * every call, and cudaFree waits for the whole device; a serving loop that
+ * writes a new session's prompt KV while other sessions' frames run, or code
+ * living under a memory pool it does not own, cannot do that. This entry point
+ * allocates nothing: it stages through one static device array of 4 MiB
+ * (K then V; at most 1024 pages per call), which every GPU that loads the
+ * library holds until the process exits. Larger writes are rejected with
+ * QTTS_E_INVALID: split them. Same arguments and cache result as
+ * qtts_kv_write, plus `stream`: the copies and the scatter are queued on it and
+ * the call returns without waiting; pinned host inputs must stay untouched
+ * until the stream has run the copies. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture. All calls share the one array, so calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race. */
+int qtts_kv_write_noalloc(qtts_model* m, int layer, int n_tok, const int32_t* pages_host, const uint16_t* k,
+                          const uint16_t* v, void* stream);
+
 /* One codec frame for B sessions, asynchronous on `stream` (a cudaStream_t;
  * NULL = default stream). All array pointers are device memory owned by the
  * caller, read/written in stream order:
