@@ -131,7 +131,35 @@ def max_over_ranks(x, ws):
 # our arm
 # --------------------------------------------------------------------------
 
-def run_gpu(wl, steps, warmup, local, weights):
+def stage_names(d):
+    """Kind of every stage of the frame program, in order."""
+    layer = ["qkv", "attn", "o", "gateup", "down"]
+    names = ["begin"] + [f"talker.{n}" for _ in range(d.n_layers) for n in layer] + ["head0+proj", "sample0"]
+    for _ in range(1, 16):
+        names += [f"cp.{n}" for _ in range(d.cp_layers) for n in layer] + ["cp.head", "cp.sample"]
+    return names
+
+
+def trace_summary(d, stamps):
+    """Per stage kind: mean body time on CTA 0 and mean wait from its end to
+    the next stage's start (the barrier), in microseconds."""
+    names = stage_names(d)
+    n = len(names)
+    t = stamps[: 2 * n].reshape(n, 2).astype(np.int64)
+    out = {}
+    for i, nm in enumerate(names):
+        body = (t[i, 1] - t[i, 0]) / 1e3
+        gap = (t[i + 1, 0] - t[i, 1]) / 1e3 if i + 1 < n else 0.0
+        o = out.setdefault(nm, [0, 0.0, 0.0])
+        o[0] += 1
+        o[1] += body
+        o[2] += gap
+    total = (t[-1, 1] - t[0, 0]) / 1e3
+    return {"frame_us": total, "stages": {k: {"n": v[0], "body_us": v[1] / v[0], "barrier_us": v[2] / v[0],
+                                                "total_us": v[1] + v[2]} for k, v in out.items()}}
+
+
+def run_gpu(wl, steps, warmup, local, weights, prefetch=None, trace=False):
     import torch
 
     from codebook_decode_gb300 import qtts
@@ -144,6 +172,8 @@ def run_gpu(wl, steps, warmup, local, weights):
     pool = wl.batch * ((cap + 15) // 16) + 8
     eng = Engine(d, weights, max_batch=max(wl.batch, 1), max_context=cap, pool_pages=pool, device=local, int8=wl.int8)
     eng.setup_sessions(sess, cap, shuffle=wl.shuffle_pages)
+    if prefetch is not None:
+        qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_PREFETCH, prefetch)
     dev = eng.dev
     stream = torch.cuda.current_stream()
     sess0 = eng.sess.clone()
@@ -235,6 +265,14 @@ def run_gpu(wl, steps, warmup, local, weights):
     h2d = sess_h.nbytes + B * eng.bt_stride * 4 + emb_h.nbytes + rng_h.nbytes + seen_h.nbytes
     d2h = codes_h.nbytes + eos_h.nbytes + sess_h.nbytes + rng_h.nbytes + seen_h.nbytes
     res["e2e"] = dict(value=B * e2e_steps / e2e_s, h2d=h2d, d2h=d2h)
+    if trace:
+        qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_TRACE, 1)
+        eng.sess.copy_(sess0)
+        for _ in range(2):
+            eng.step(emb, None, want_logits=False, stream=stream)
+        stamps = np.zeros(4 * len(stage_names(d)), dtype=np.uint64)
+        qtts.qtts_frame_trace(eng.m, stamps)
+        res["trace"] = trace_summary(d, stamps)
     eng.release_pages()
     eng.close()
     return res
@@ -271,6 +309,8 @@ def main():
     ap.add_argument("--workload", default="full_b1", choices=sorted(configs.WORKLOADS))
     ap.add_argument("--no-sweep", action="store_true", help="skip the B=8/B=32/INT8 side measurements")
     ap.add_argument("--oracle-frames", type=int, default=6)
+    ap.add_argument("--prefetch", type=int, default=None, help="L2 prefetch distance in stages (library default 1)")
+    ap.add_argument("--trace", action="store_true", help="print a per-stage time breakdown to stderr")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
     ws, rank, local = (1, 0, 0)
@@ -301,7 +341,9 @@ def main():
     import torch
     w = synth.make_weights(wl.dims, 1000 + wl.seed)
     barrier(ws)
-    r = run_gpu(wl, args.steps, args.warmup, local, w)
+    r = run_gpu(wl, args.steps, args.warmup, local, w, prefetch=args.prefetch, trace=args.trace)
+    if args.trace:
+        print(json.dumps(r["trace"]), file=sys.stderr)
     total_s = max_over_ranks(r["total_ms"] / 1e3, ws)
     value = ws * wl.batch * args.steps / total_s
     peak, peak_kind = measured_peak_gbs()
@@ -328,7 +370,7 @@ def main():
             sweep = {}
             for name in ("full_b8", "full_b32", "int8_b1", "int8_b32"):
                 o = configs.WORKLOADS[name]
-                rr = run_gpu(o, min(args.steps, 50), 3, local, w)  # same random-init weights
+                rr = run_gpu(o, min(args.steps, 50), 3, local, w, prefetch=args.prefetch)  # same weights
                 sweep[name] = {"frames_per_s": o.batch * min(args.steps, 50) / (rr["total_ms"] / 1e3),
                                "frame_ms": rr["frame_ms"], "achieved_gbs": rr["achieved_gbs"],
                                "frac": rr["achieved_gbs"] / peak, "bytes_per_frame": rr["bytes_per_frame"]}

@@ -66,30 +66,35 @@ __device__ __forceinline__ void set_err(int* e, int code) { atomicCAS(e, 0, code
 
 constexpr uint64_t kBarrierTimeoutNs = 2000000000ull;  // 2 s: a frame takes milliseconds
 
-// Grid-wide barrier with a bounded wait. Every CTA adds one to the counter and
-// waits for `target`; a wait that outlives the limit sets QTTS_DEV_TIMEOUT,
-// and any error word set elsewhere also ends the wait. Returns false to make
-// the CTA leave the frame.
+__device__ __forceinline__ void red_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier with a bounded wait. After the CTA's bar.sync, thread 0
+// adds one to the counter with release semantics (publishing the whole CTA's
+// writes) and polls it with acquire loads until it reaches `target`. A wait
+// that outlives the limit sets QTTS_DEV_TIMEOUT, and an error word set
+// elsewhere also ends the wait. Returns false to make the CTA leave the frame.
 __device__ bool grid_sync(const Globals& g, unsigned target, volatile int* sflag) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(g.barrier, 1u);
+    red_release_gpu(g.barrier, 1u);
     int ok = 1;
-    const uint64_t t0 = global_timer_ns();
-    unsigned spins = 0;
-    while (ld_acquire_gpu(g.barrier) < target) {
-      if (read_err(g.err)) {
-        ok = 0;
-        break;
-      }
-      if ((++spins & 63u) == 0u && global_timer_ns() - t0 > kBarrierTimeoutNs) {
-        set_err(g.err, QTTS_DEV_TIMEOUT);
-        ok = 0;
-        break;
+    if (ld_acquire_gpu(g.barrier) < target) {
+      const uint64_t t0 = global_timer_ns();
+      unsigned spins = 0;
+      while (ld_acquire_gpu(g.barrier) < target) {
+        if (read_err(g.err)) {
+          ok = 0;
+          break;
+        }
+        if ((++spins & 63u) == 0u && global_timer_ns() - t0 > kBarrierTimeoutNs) {
+          set_err(g.err, QTTS_DEV_TIMEOUT);
+          ok = 0;
+          break;
+        }
       }
     }
-    __threadfence();
     *sflag = ok;
   }
   __syncthreads();
@@ -455,10 +460,20 @@ __device__ bool stage_begin(const Globals& g, const FrameArgs& fa, unsigned char
 // lanes striding K in 8-element (16-byte bf16 / 8-byte int8) vectors.
 // ---------------------------------------------------------------------------
 
+// Phase-1 work item: one row unit and a 1024-wide slice of K, so that a lane
+// has all of its (up to 4 per row) 16-byte weight loads in flight at once.
+constexpr int kKChunk = 1024;
+constexpr int kSub = kKChunk / 256;
+constexpr int kPartFloats = 2048;
+constexpr int kSqFloats = 512;
+
 struct GemvSmemTail {
   float rfac[8];
-  float ssq_w[kWarps * kMaxRows];
+  float ssq_row[kMaxRows];   // this CTA's sum of squares per stage row
+  float part[kPartFloats];   // phase-1 partial dot products [task][U][RT]
+  float sq[kSqFloats];       // phase-2 squares [unit][RT]
 };
+static_assert(sizeof(GemvSmemTail) <= kSmemBytes - kSmemX, "GEMV shared-memory tail");
 
 template <typename WT>
 __device__ __forceinline__ void load_w8(const WT* base, float out[8]);
@@ -498,9 +513,10 @@ __device__ __forceinline__ uint16_t* talker_kv_ptr(const Globals& g, const Frame
          (((((size_t)layer * g.pool_pages + page) * 2 + kv) * g.nkv + head) * kPage + pos % kPage) * g.d;
 }
 
+// Code-Predictor cache of one layer: [session][K|V][kv head][16 positions][d]
 __device__ __forceinline__ uint16_t* cp_kv_ptr(const Globals& g, uint16_t* layer_base, int b, int pos, int kv,
                                                 int head) {
-  return layer_base + ((((size_t)b * 2 + kv) * kCodebooks + pos) * g.nkvc + head) * g.dc;
+  return layer_base + ((((size_t)b * 2 + kv) * g.nkvc + head) * kCodebooks + pos) * g.dc;
 }
 
 // Epilogue for one output unit (rows n0, n0+1 when U == 2) of stage row r.
@@ -573,45 +589,85 @@ __device__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& 
   }
 }
 
+template <typename WT>
+struct Raw8 {
+  using T = uint4;  // 8 bf16
+  static __device__ __forceinline__ T load(const WT* p) { return ld_stream16(p); }
+  static __device__ __forceinline__ void unpack(const T& v, float o[8]) {
+    o[0] = bf_lo(v.x); o[1] = bf_hi(v.x); o[2] = bf_lo(v.y); o[3] = bf_hi(v.y);
+    o[4] = bf_lo(v.z); o[5] = bf_hi(v.z); o[6] = bf_lo(v.w); o[7] = bf_hi(v.w);
+  }
+};
+template <>
+struct Raw8<int8_t> {
+  using T = uint2;  // 8 int8
+  static __device__ __forceinline__ T load(const int8_t* p) { return ld_stream8(p); }
+  static __device__ __forceinline__ void unpack(const T& v, float o[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = (float)(int)(int8_t)((v.x >> (8 * i)) & 0xFFu);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[4 + i] = (float)(int)(int8_t)((v.y >> (8 * i)) & 0xFFu);
+  }
+};
+
+// This CTA's share of rows [u0*U, u1*U) of one segment for stage rows
+// [r0, r0 + nr): phase 1 spreads (unit, K-slice) tasks over all warps and
+// leaves one partial per task in shared memory; phase 2 gives each (unit, row)
+// to one thread, which sums the partials in K order and runs the epilogue.
 template <typename WT, int U, int RT>
 __device__ void gemv_seg(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, const float* xs,
-                         int r0, int nr, float* ssq_w) {
+                         int r0, int nr, GemvSmemTail* tail) {
+  using R = Raw8<WT>;
   const int K = d.K;
   const int units = sg.N / U;
   const int u0 = (int)((long long)units * blockIdx.x / gridDim.x);
   const int u1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x);
+  const int nu = u1 - u0;
+  const int nkc = (K + kKChunk - 1) / kKChunk;
+  const int ntask = nu * nkc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WT* W = (const WT*)sg.w;
-  float ssq_acc = 0.f;
-  for (int u = u0 + warp; u < u1; u += kWarps) {
-    const int n0 = u * U;
+  for (int t = warp; t < ntask; t += kWarps) {
+    const int ul = t / nkc, kc = t - ul * nkc;
+    const int n0 = (u0 + ul) * U;
+    const int kb = kc * kKChunk + lane * 8;
+    typename R::T raw[kSub][U];
+#pragma unroll
+    for (int sb = 0; sb < kSub; ++sb) {
+      const int k = kb + sb * 256;
+#pragma unroll
+      for (int i = 0; i < U; ++i) raw[sb][i] = (k < K) ? R::load(W + (size_t)(n0 + i) * K + k) : typename R::T{};
+    }
     float acc[U][RT];
 #pragma unroll
     for (int i = 0; i < U; ++i)
 #pragma unroll
       for (int r = 0; r < RT; ++r) acc[i][r] = 0.f;
-#pragma unroll 2
-    for (int k = lane * 8; k < K; k += 256) {
-      float wv[U][8];
 #pragma unroll
-      for (int i = 0; i < U; ++i) load_w8<WT>(W + (size_t)(n0 + i) * K + k, wv[i]);
+    for (int sb = 0; sb < kSub; ++sb) {
+      const int k = kb + sb * 256;
+      if (k < K) {
+        float wv[U][8];
 #pragma unroll
-      for (int r = 0; r < RT; ++r) {
-        if (r < nr) {
-          const float4 a = *reinterpret_cast<const float4*>(xs + r * K + k);
-          const float4 c = *reinterpret_cast<const float4*>(xs + r * K + k + 4);
+        for (int i = 0; i < U; ++i) R::unpack(raw[sb][i], wv[i]);
 #pragma unroll
-          for (int i = 0; i < U; ++i) {
-            float t = acc[i][r];
-            t = fmaf(wv[i][0], a.x, t);
-            t = fmaf(wv[i][1], a.y, t);
-            t = fmaf(wv[i][2], a.z, t);
-            t = fmaf(wv[i][3], a.w, t);
-            t = fmaf(wv[i][4], c.x, t);
-            t = fmaf(wv[i][5], c.y, t);
-            t = fmaf(wv[i][6], c.z, t);
-            t = fmaf(wv[i][7], c.w, t);
-            acc[i][r] = t;
+        for (int r = 0; r < RT; ++r) {
+          if (r < nr) {
+            const float4 a = *reinterpret_cast<const float4*>(xs + r * K + k);
+            const float4 c = *reinterpret_cast<const float4*>(xs + r * K + k + 4);
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+              float v = acc[i][r];
+              v = fmaf(wv[i][0], a.x, v);
+              v = fmaf(wv[i][1], a.y, v);
+              v = fmaf(wv[i][2], a.z, v);
+              v = fmaf(wv[i][3], a.w, v);
+              v = fmaf(wv[i][4], c.x, v);
+              v = fmaf(wv[i][5], c.y, v);
+              v = fmaf(wv[i][6], c.z, v);
+              v = fmaf(wv[i][7], c.w, v);
+              acc[i][r] = v;
+            }
           }
         }
       }
@@ -619,96 +675,145 @@ __device__ void gemv_seg(const StageDesc& d, const Seg& sg, const Globals& g, co
 #pragma unroll
     for (int i = 0; i < U; ++i)
 #pragma unroll
-      for (int r = 0; r < RT; ++r) acc[i][r] = warp_sum(acc[i][r]);
-    if (sg.scale) {
-#pragma unroll
-      for (int i = 0; i < U; ++i) {
-        const float sc = sg.scale[n0 + i];
-#pragma unroll
-        for (int r = 0; r < RT; ++r) acc[i][r] *= sc;
+      for (int r = 0; r < RT; ++r) {
+        const float v = warp_sum(acc[i][r]);
+        if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
       }
-    }
-#pragma unroll
-    for (int r = 0; r < RT; ++r)
-      if (lane == r && r < nr)
-        gemv_epilogue(d, sg, g, fa, n0, acc[0][r], U == 2 ? acc[U - 1][r] : 0.f, r0 + r, ssq_acc);
   }
-  if (lane < nr) ssq_w[warp * kMaxRows + r0 + lane] += ssq_acc;
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nu * nr; idx += kThreads) {
+    const int ul = idx / nr, r = idx - ul * nr;
+    const int n0 = (u0 + ul) * U;
+    float y[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      float acc = 0.f;
+      for (int kc = 0; kc < nkc; ++kc) acc += tail->part[((ul * nkc + kc) * U + i) * RT + r];
+      y[i] = sg.scale ? acc * sg.scale[n0 + i] : acc;
+    }
+    float sqv = 0.f;
+    gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + r, sqv);
+    tail->sq[ul * RT + r] = sqv;
+  }
+  __syncthreads();
+  if (sg.ssq_out)
+    for (int r = threadIdx.x; r < nr; r += kThreads) {
+      float acc = 0.f;
+      for (int ul = 0; ul < nu; ++ul) acc += tail->sq[ul * RT + r];
+      tail->ssq_row[r0 + r] += acc;
+    }
+  __syncthreads();
 }
 
 template <typename WT, int U>
 __device__ void gemv_seg_rt(int RT, const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa,
-                            const float* xs, int r0, int nr, float* ssq_w) {
+                            const float* xs, int r0, int nr, GemvSmemTail* tail) {
   switch (RT) {
-    case 1: gemv_seg<WT, U, 1>(d, sg, g, fa, xs, r0, nr, ssq_w); break;
-    case 2: gemv_seg<WT, U, 2>(d, sg, g, fa, xs, r0, nr, ssq_w); break;
-    case 4: gemv_seg<WT, U, 4>(d, sg, g, fa, xs, r0, nr, ssq_w); break;
-    default: gemv_seg<WT, U, 8>(d, sg, g, fa, xs, r0, nr, ssq_w); break;
+    case 1: gemv_seg<WT, U, 1>(d, sg, g, fa, xs, r0, nr, tail); break;
+    case 2: gemv_seg<WT, U, 2>(d, sg, g, fa, xs, r0, nr, tail); break;
+    case 4: gemv_seg<WT, U, 4>(d, sg, g, fa, xs, r0, nr, tail); break;
+    default: gemv_seg<WT, U, 8>(d, sg, g, fa, xs, r0, nr, tail); break;
   }
 }
 
 __device__ void stage_gemv(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rows = fa.B * d.rps;
   const int K = d.K;
+  const bool norm = d.xsrc == X_NORM;
   float* xs = (float*)smem;
   GemvSmemTail* tail = (GemvSmemTail*)(smem + kSmemX);
-  for (int i = tid; i < kWarps * kMaxRows; i += kThreads) tail->ssq_w[i] = 0.f;
+  for (int i = tid; i < kMaxRows; i += kThreads) tail->ssq_row[i] = 0.f;
 
-  int RT = kSmemX / (K * 4);
+  // activation rows per tile; a norm stage keeps one more row's worth for the gains
+  int RT = kSmemX / (K * 4) - (norm ? 1 : 0);
   RT = RT >= 8 ? 8 : RT >= 4 ? 4 : RT >= 2 ? 2 : 1;
   while (RT > 1 && RT / 2 >= rows) RT /= 2;
+  float* gs = xs + RT * K;
   const RowMap rm{d.rps, d.in_rps, d.in_off};
 
   for (int r0 = 0; r0 < rows; r0 += RT) {
     const int nr = min(RT, rows - r0);
     __syncthreads();
-    if (d.xsrc == X_NORM) {
-      const int warp = tid >> 5, lane = tid & 31;
-      if (warp < nr) {
-        const int ir = rm.in_row(r0 + warp);
-        float s = 0.f;
-        for (int c = lane; c < g.G; c += 32) s += __ldcg(d.ssq + (size_t)c * kMaxRows + ir);
-        s = warp_sum(s);
-        if (lane == 0) tail->rfac[warp] = 1.0f / sqrtf(s / (float)K + g.eps);
-      }
-      __syncthreads();
+    // issue the sum-of-squares loads, the activation loads and the gain loads
+    // together: one L2 round trip for the whole prologue
+    float ssq_part = 0.f;
+    if (norm && warp < nr) {
+      const int ir = rm.in_row(r0 + warp);
+      for (int c = lane; c < g.G; c += 32) ssq_part += __ldcg(d.ssq + (size_t)c * kMaxRows + ir);
     }
     for (int idx = tid * 4; idx < nr * K; idx += kThreads * 4) {
-      const int r = idx / K, k = idx % K;
+      const int r = idx / K, k = idx - r * K;
       const int ir = rm.in_row(r0 + r);
-      float4 v = __ldcg(reinterpret_cast<const float4*>(d.x + (size_t)ir * d.x_stride + k));
-      if (d.xsrc == X_NORM) {
-        const float f = tail->rfac[r];
-        const uint2 gw = *reinterpret_cast<const uint2*>(d.gain + k);
-        v.x = v.x * f * bf_lo(gw.x);
-        v.y = v.y * f * bf_hi(gw.x);
-        v.z = v.z * f * bf_lo(gw.y);
-        v.w = v.w * f * bf_hi(gw.y);
+      *reinterpret_cast<float4*>(xs + r * K + k) =
+          __ldcg(reinterpret_cast<const float4*>(d.x + (size_t)ir * d.x_stride + k));
+    }
+    if (norm) {
+      if (r0 == 0)
+        for (int k = tid * 4; k < K; k += kThreads * 4) {
+          const uint2 gw = *reinterpret_cast<const uint2*>(d.gain + k);
+          *reinterpret_cast<float4*>(gs + k) = make_float4(bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y));
+        }
+      if (warp < nr) {
+        const float sum = warp_sum(ssq_part);
+        if (lane == 0) tail->rfac[warp] = 1.0f / sqrtf(sum / (float)K + g.eps);
       }
-      *reinterpret_cast<float4*>(xs + r * K + k) = v;
+      __syncthreads();
+      for (int idx = tid * 4; idx < nr * K; idx += kThreads * 4) {
+        const int r = idx / K, k = idx - r * K;
+        const float f = tail->rfac[r];
+        float4 v = *reinterpret_cast<float4*>(xs + r * K + k);
+        const float4 gg = *reinterpret_cast<const float4*>(gs + k);
+        v.x = v.x * f * gg.x;
+        v.y = v.y * f * gg.y;
+        v.z = v.z * f * gg.z;
+        v.w = v.w * f * gg.w;
+        *reinterpret_cast<float4*>(xs + r * K + k) = v;
+      }
     }
     __syncthreads();
     for (int s = 0; s < d.nseg; ++s) {
       const Seg& sg = d.seg[s];
       if (sg.scale) {
-        if (sg.unit == 2) gemv_seg_rt<int8_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail->ssq_w);
-        else gemv_seg_rt<int8_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail->ssq_w);
+        if (sg.unit == 2) gemv_seg_rt<int8_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail);
+        else gemv_seg_rt<int8_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail);
       } else {
-        if (sg.unit == 2) gemv_seg_rt<uint16_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail->ssq_w);
-        else gemv_seg_rt<uint16_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail->ssq_w);
+        if (sg.unit == 2) gemv_seg_rt<uint16_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail);
+        else gemv_seg_rt<uint16_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail);
       }
     }
   }
-  __syncthreads();
   for (int s = 0; s < d.nseg; ++s) {
     const Seg& sg = d.seg[s];
     if (!sg.ssq_out) continue;
-    for (int r = tid; r < rows; r += kThreads) {
-      float t = 0.f;
-      for (int w = 0; w < kWarps; ++w) t += tail->ssq_w[w * kMaxRows + r];
-      sg.ssq_out[(size_t)blockIdx.x * kMaxRows + out_row_of(sg, d.rps, r)] = t;
-    }
+    for (int r = tid; r < rows; r += kThreads)
+      sg.ssq_out[(size_t)blockIdx.x * kMaxRows + out_row_of(sg, d.rps, r)] = tail->ssq_row[r];
+  }
+}
+
+// L2 prefetch of this CTA's weight rows of a GEMV stage (a hint: the bytes
+// stream from HBM while the grid waits at the barrier before that stage)
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+  uint64_t a = (uint64_t)__cvta_generic_to_global(p);
+  uint64_t s = (a + 15) & ~15ull;
+  const uint64_t e = (a + bytes) & ~15ull;
+  while (s < e) {
+    const uint32_t n = (uint32_t)((e - s) < 65536ull ? (e - s) : 65536ull);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s), "r"(n) : "memory");
+    s += n;
+  }
+}
+
+__device__ void prefetch_stage(const StageDesc& d) {
+  if (d.type != ST_GEMV) return;
+  for (int s = 0; s < d.nseg; ++s) {
+    const Seg& sg = d.seg[s];
+    const int U = sg.unit;
+    const int units = sg.N / U;
+    const int u0 = (int)((long long)units * blockIdx.x / gridDim.x);
+    const int u1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x);
+    const size_t es = sg.scale ? 1 : 2;
+    prefetch_l2((const char*)sg.w + (size_t)u0 * U * d.K * es, (size_t)(u1 - u0) * U * d.K * es);
   }
 }
 
@@ -717,74 +822,162 @@ __device__ void stage_gemv(const StageDesc& d, const Globals& g, const FrameArgs
 // the scores and head dimensions for the value sum; online softmax
 // ---------------------------------------------------------------------------
 
+// ---- TMA bulk copies into shared memory, tracked by an mbarrier ----
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar`, at most kBarrierTimeoutNs.
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > kBarrierTimeoutNs) {
+      set_err(err, QTTS_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// attention: one warp per (row, kv head[, split]); the split's 16-position
+// tiles of K and V (one head of one page: 2 x 4 KB contiguous) arrive in
+// shared memory by TMA bulk copy; online softmax over the tiles
+// ---------------------------------------------------------------------------
+
+constexpr int kAttnMaxHD = 128;
+constexpr int kAttnMaxGrp = 2;
+
+struct AttnTile {
+  uint16_t k[kPage * kAttnMaxHD];
+  uint16_t v[kPage * kAttnMaxHD];
+  float q[kAttnMaxGrp * kAttnMaxHD];
+  uint64_t bar;
+  uint64_t pad;
+};
+static_assert(kWarps * sizeof(AttnTile) <= kSmemBytes, "attention tiles");
+
 template <int HD, int GRP>
 struct AttnAcc {
   float o[GRP][HD / 32];
   float m[GRP], l[GRP];
 };
 
-template <int HD, int GRP, typename KPtr, typename VPtr>
-__device__ void attn_warp(const float* qs, int p0, int p1, float scale, KPtr kptr, VPtr vptr,
-                          AttnAcc<HD, GRP>& A) {
-  const int lane = threadIdx.x & 31;
-  constexpr int E = HD / 32;
+template <int HD, int GRP>
+__device__ __forceinline__ void attn_init(AttnAcc<HD, GRP>& A) {
 #pragma unroll
   for (int j = 0; j < GRP; ++j) {
     A.m[j] = -INFINITY;
     A.l[j] = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) A.o[j][e] = 0.f;
+    for (int e = 0; e < HD / 32; ++e) A.o[j][e] = 0.f;
   }
-  for (int base = p0; base < p1; base += 32) {
-    const int p = base + lane;
-    const bool valid = p < p1;
-    float sc[GRP];
+}
+
+// Fold positions 0..nvalid-1 of the tile into A. Scores: lane i & 15 takes
+// position i, lane halves split the head dims (each lane starts at a
+// different 16-byte column so the row reads do not collide in the banks).
+// Values: lanes take E = HD/32 consecutive dims.
+template <int HD, int GRP>
+__device__ void attn_tile(const AttnTile& T, int nvalid, float scale, AttnAcc<HD, GRP>& A) {
+  const int lane = threadIdx.x & 31;
+  constexpr int E = HD / 32;
+  constexpr int HH = HD / 2;
+  const int i = lane & 15, half = lane >> 4;
+  const bool valid = i < nvalid;
+  float sc[GRP];
 #pragma unroll
-    for (int j = 0; j < GRP; ++j) sc[j] = 0.f;
-    if (valid) {
-      const uint16_t* kp = kptr(p);
+  for (int j = 0; j < GRP; ++j) sc[j] = 0.f;
+  const uint16_t* krow = T.k + i * HD + half * HH;
 #pragma unroll 4
-      for (int t = 0; t < HD; t += 8) {
-        const uint4 kv = *reinterpret_cast<const uint4*>(kp + t);
-        const float k8[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
-                             bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
-#pragma unroll
-        for (int j = 0; j < GRP; ++j)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) sc[j] = fmaf(qs[j * HD + t + e], k8[e], sc[j]);
-      }
-    }
-    float pj[GRP];
+  for (int tt = 0; tt < HH; tt += 8) {
+    const int t = (tt + i * 8) & (HH - 1);
+    const uint4 kv = *reinterpret_cast<const uint4*>(krow + t);
+    const float k8[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
+                         bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
 #pragma unroll
     for (int j = 0; j < GRP; ++j) {
-      const float s = valid ? sc[j] * scale : -INFINITY;
-      const float mnew = fmaxf(A.m[j], warp_max(s));
-      const float corr = expf(A.m[j] - mnew);
-      pj[j] = valid ? expf(s - mnew) : 0.f;
-      A.l[j] = A.l[j] * corr + warp_sum(pj[j]);
+      const float* q = T.q + j * HD + half * HH + t;
 #pragma unroll
-      for (int e = 0; e < E; ++e) A.o[j][e] *= corr;
-      A.m[j] = mnew;
-    }
-    const int nvalid = min(32, p1 - base);
-    for (int i = 0; i < nvalid; ++i) {
-      const uint16_t* vp = vptr(base + i) + lane * E;
-      float v[E];
-      if constexpr (E == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(vp);
-        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[e] = bf2f(vp[e]);
-      }
-#pragma unroll
-      for (int j = 0; j < GRP; ++j) {
-        const float pij = __shfl_sync(0xffffffffu, pj[j], i);
-#pragma unroll
-        for (int e = 0; e < E; ++e) A.o[j][e] = fmaf(pij, v[e], A.o[j][e]);
-      }
+      for (int e = 0; e < 8; ++e) sc[j] = fmaf(q[e], k8[e], sc[j]);
     }
   }
+  float pj[GRP];
+#pragma unroll
+  for (int j = 0; j < GRP; ++j) {
+    sc[j] += __shfl_xor_sync(0xffffffffu, sc[j], 16);
+    const float s = valid ? sc[j] * scale : -INFINITY;
+    const float mnew = fmaxf(A.m[j], warp_max(s));
+    const float corr = expf(A.m[j] - mnew);
+    pj[j] = valid ? expf(s - mnew) : 0.f;
+    A.l[j] = A.l[j] * corr + warp_sum(half == 0 ? pj[j] : 0.f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) A.o[j][e] *= corr;
+    A.m[j] = mnew;
+  }
+  for (int p = 0; p < nvalid; ++p) {
+    float v[E];
+    const uint16_t* vr = T.v + p * HD + lane * E;
+    if constexpr (E == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(vr);
+      v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(vr);
+      v[0] = bf_lo(w);
+      v[1] = bf_hi(w);
+    }
+#pragma unroll
+    for (int j = 0; j < GRP; ++j) {
+      const float pp = __shfl_sync(0xffffffffu, pj[j], p);
+#pragma unroll
+      for (int e = 0; e < E; ++e) A.o[j][e] = fmaf(pp, v[e], A.o[j][e]);
+    }
+  }
+}
+
+// One 16-position tile by bulk copy (K then V of one head), then fold it in.
+template <int HD, int GRP>
+__device__ bool attn_fetch_fold(AttnTile& T, const uint16_t* ksrc, const uint16_t* vsrc, int nvalid, float scale,
+                                uint32_t& parity, int* err, AttnAcc<HD, GRP>& A) {
+  const int lane = threadIdx.x & 31;
+  constexpr uint32_t bytes = kPage * HD * sizeof(uint16_t);
+  __syncwarp();
+  if (lane == 0) {
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&T.bar, 2 * bytes);
+    bulk_load(T.k, ksrc, bytes, &T.bar);
+    bulk_load(T.v, vsrc, bytes, &T.bar);
+  }
+  const bool ok = mbar_wait(&T.bar, parity, err);
+  parity ^= 1u;
+  if (ok) attn_tile<HD, GRP>(T, nvalid, scale, A);
+  return ok;
 }
 
 template <int HD, int GRP>
@@ -793,14 +986,19 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
   constexpr int E = HD / 32;
   const int nkv = g.nkv;
   const int qstride = d.q_stride;
-  // split plan: identical on every CTA (same inputs, same arithmetic)
+  AttnTile& T = reinterpret_cast<AttnTile*>(smem)[warp];
+  if (lane == 0) mbar_init(&T.bar);
+  __syncwarp();
+  uint32_t parity = 0;
+  // split plan, identical on every CTA (same inputs, same arithmetic): about
+  // one page-aligned split per warp of the grid
   const int len = lane < fa.B ? fa.sess[lane].kv_len + 1 : 0;
   int total = len;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
   const int target = g.G * kWarps;
   int chunk = (total * nkv + target - 1) / target;
-  chunk = ((chunk + 31) / 32) * 32;
+  chunk = ((chunk + kPage - 1) / kPage) * kPage;
   if (chunk < kMinChunk) chunk = kMinChunk;
   const int nsp = (len + chunk - 1) / chunk;
   int incl = nsp * nkv;
@@ -810,11 +1008,11 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
     if (lane >= o) incl += t;
   }
   const int n_items = __shfl_sync(0xffffffffu, incl, 31);
-  float* qs = (float*)smem + warp * GRP * HD;
   const float scale = rsqrtf((float)HD);
   const int layer = d.layer;
 
-  for (int item = blockIdx.x * kWarps + warp; item < n_items; item += g.G * kWarps) {
+  // item i goes to CTA i % G, so the splits spread over the SMs first
+  for (int item = warp * g.G + blockIdx.x; item < n_items; item += g.G * kWarps) {
     const unsigned hit = __ballot_sync(0xffffffffu, incl > item);
     const int b = __ffs(hit) - 1;
     const int before = __shfl_sync(0xffffffffu, incl - nsp * nkv, b);
@@ -824,12 +1022,15 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
     const int kvh = rem / nsp_b, sp = rem % nsp_b;
     const int p0 = sp * chunk, p1 = min(p0 + chunk, len_b);
     const float* qsrc = d.q + (size_t)b * qstride + kvh * GRP * HD;
-    for (int e = lane; e < GRP * HD; e += 32) qs[e] = __ldcg(qsrc + e);
     __syncwarp();
+    for (int e = lane; e < GRP * HD; e += 32) T.q[e] = __ldcg(qsrc + e);
     AttnAcc<HD, GRP> A;
-    attn_warp<HD, GRP>(
-        qs, p0, p1, scale, [&](int p) { return (const uint16_t*)talker_kv_ptr(g, fa, layer, b, p, 0, kvh); },
-        [&](int p) { return (const uint16_t*)talker_kv_ptr(g, fa, layer, b, p, 1, kvh); }, A);
+    attn_init(A);
+    bool ok = true;
+    for (int pt = p0; pt < p1 && ok; pt += kPage)
+      ok = attn_fetch_fold<HD, GRP>(T, talker_kv_ptr(g, fa, layer, b, pt, 0, kvh), talker_kv_ptr(g, fa, layer, b, pt, 1, kvh),
+                                    min(kPage, p1 - pt), scale, parity, g.err, A);
+    if (!ok) break;
     float* out = d.attn_out + (size_t)b * qstride + kvh * GRP * HD;
     if (nsp_b == 1) {
 #pragma unroll
@@ -859,18 +1060,37 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
         const float* base = g.attn_part + ((((size_t)b * nkv + kvh) * kMaxSplits) * GRP) * (HD + 2);
 #pragma unroll
         for (int j = 0; j < GRP; ++j) {
+          // lanes own splits for the max and the denominator
           float M = -INFINITY;
-          for (int s = 0; s < nsp_b; ++s) M = fmaxf(M, __ldcg(base + ((size_t)s * GRP + j) * (HD + 2)));
+          for (int s2 = lane; s2 < nsp_b; s2 += 32) M = fmaxf(M, __ldcg(base + ((size_t)s2 * GRP + j) * (HD + 2)));
+          M = warp_max(M);
           float L = 0.f;
+          for (int s2 = lane; s2 < nsp_b; s2 += 32) {
+            const float* ps = base + ((size_t)s2 * GRP + j) * (HD + 2);
+            L += expf(__ldcg(ps) - M) * __ldcg(ps + 1);
+          }
+          L = warp_sum(L);
+          // lanes own head dimensions for the weighted sum, 2 splits per batch
           float o[E];
 #pragma unroll
           for (int e = 0; e < E; ++e) o[e] = 0.f;
-          for (int s = 0; s < nsp_b; ++s) {
-            const float* ps = base + ((size_t)s * GRP + j) * (HD + 2);
-            const float w = expf(__ldcg(ps) - M);
-            L += w * __ldcg(ps + 1);
+          for (int s0 = 0; s0 < nsp_b; s0 += 2) {
+            float mv[2], ov[2][E];
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[e] += w * __ldcg(ps + 2 + lane * E + e);
+            for (int u = 0; u < 2; ++u)
+              if (s0 + u < nsp_b) {
+                const float* ps = base + ((size_t)(s0 + u) * GRP + j) * (HD + 2);
+                mv[u] = __ldcg(ps);
+#pragma unroll
+                for (int e = 0; e < E; ++e) ov[u][e] = __ldcg(ps + 2 + lane * E + e);
+              }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              if (s0 + u < nsp_b) {
+                const float w = expf(mv[u] - M);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[e] = fmaf(w, ov[u][e], o[e]);
+              }
           }
 #pragma unroll
           for (int e = 0; e < E; ++e) out[j * HD + lane * E + e] = o[e] / L;
@@ -878,8 +1098,9 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
         if (lane == 0) g.attn_cnt[b * nkv + kvh] = 0;  // ready for the next layer
       }
     }
-    __syncwarp();
   }
+  __syncwarp();
+  if (lane == 0) mbar_inval(&T.bar);
 }
 
 template <int HD, int GRP>
@@ -889,26 +1110,31 @@ __device__ void stage_attn_cp(const StageDesc& d, const Globals& g, const FrameA
   const int nkv = g.nkvc;
   const int qstride = d.q_stride;
   const int rows = fa.B * d.rps;
-  float* qs = (float*)smem + warp * GRP * HD;
+  AttnTile& T = reinterpret_cast<AttnTile*>(smem)[warp];
+  if (lane == 0) mbar_init(&T.bar);
+  __syncwarp();
+  uint32_t parity = 0;
   const float scale = rsqrtf((float)HD);
-  for (int item = blockIdx.x * kWarps + warp; item < rows * nkv; item += g.G * kWarps) {
+  for (int item = warp * g.G + blockIdx.x; item < rows * nkv; item += g.G * kWarps) {
     const int r = item / nkv, kvh = item % nkv;
     const int b = r / d.rps, p = r % d.rps;
     const int pos = d.pos_base + p;
     const float* qsrc = d.q + (size_t)r * qstride + kvh * GRP * HD;
-    for (int e = lane; e < GRP * HD; e += 32) qs[e] = __ldcg(qsrc + e);
     __syncwarp();
+    for (int e = lane; e < GRP * HD; e += 32) T.q[e] = __ldcg(qsrc + e);
     AttnAcc<HD, GRP> A;
-    attn_warp<HD, GRP>(
-        qs, 0, pos + 1, scale, [&](int t) { return (const uint16_t*)cp_kv_ptr(g, d.cp_kv, b, t, 0, kvh); },
-        [&](int t) { return (const uint16_t*)cp_kv_ptr(g, d.cp_kv, b, t, 1, kvh); }, A);
+    attn_init(A);
+    if (!attn_fetch_fold<HD, GRP>(T, cp_kv_ptr(g, d.cp_kv, b, 0, 0, kvh), cp_kv_ptr(g, d.cp_kv, b, 0, 1, kvh), pos + 1,
+                                  scale, parity, g.err, A))
+      break;
     float* out = d.attn_out + (size_t)r * qstride + kvh * GRP * HD;
 #pragma unroll
     for (int j = 0; j < GRP; ++j)
 #pragma unroll
       for (int e = 0; e < E; ++e) out[j * HD + lane * E + e] = A.o[j][e] / A.l[j];
-    __syncwarp();
   }
+  __syncwarp();
+  if (lane == 0) mbar_inval(&T.bar);
 }
 
 template <bool TALKER>
@@ -925,8 +1151,6 @@ __device__ void stage_attn(const StageDesc& d, const Globals& g, const FrameArgs
   QTTS_ATTN_CASE(64, 2)
   QTTS_ATTN_CASE(128, 1)
   QTTS_ATTN_CASE(64, 1)
-  QTTS_ATTN_CASE(128, 4)
-  QTTS_ATTN_CASE(64, 4)
 #undef QTTS_ATTN_CASE
 }
 
@@ -976,14 +1200,25 @@ __device__ void stage_sample(const StageDesc& d, const Globals& g, const FrameAr
 // the persistent frame kernel
 // ---------------------------------------------------------------------------
 
+__device__ __forceinline__ void trace_mark(const Globals& g, int s, int which) {
+  if (g.trace && threadIdx.x == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1)) {
+    const int slot = blockIdx.x == 0 ? 0 : 1;
+    g.trace[((size_t)slot * g.n_stages + s) * 2 + which] = global_timer_ns();
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     frame_kernel(const StageDesc* __restrict__ prog, int s0, int s1, Globals g, FrameArgs fa) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int sflag;
   if (read_err(g.err)) return;  // a device error is sticky until qtts_frame_status clears it
+  if (g.prefetch > 1 && threadIdx.x == kThreads - 1)
+    for (int s = s0 + 1; s < min(s1, s0 + g.prefetch); ++s) prefetch_stage(prog[s]);
   unsigned bar = 0;
   for (int s = s0; s < s1; ++s) {
     const StageDesc& d = prog[s];
+    trace_mark(g, s, 0);
+    if (g.prefetch > 0 && threadIdx.x == kThreads - 1 && s + g.prefetch < s1) prefetch_stage(prog[s + g.prefetch]);
     switch (d.type) {
       case ST_BEGIN:
         if (!stage_begin(g, fa, smem)) return;
@@ -994,6 +1229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       case ST_SAMPLE: stage_sample(d, g, fa, smem); break;
       default: break;
     }
+    trace_mark(g, s, 1);
     if (s + 1 < s1) {
       bar += gridDim.x;
       if (!grid_sync(g, bar, &sflag)) return;

@@ -69,6 +69,7 @@ struct qtts_model {
   std::vector<uint8_t> page_used;
 
   uint16_t* cp_kv = nullptr;
+  unsigned long long* trace_buf = nullptr;
   Globals g{};
   StageDesc* prog_dev[2] = {nullptr, nullptr};
   int n_stages = 0;
@@ -157,7 +158,7 @@ bool cfg_ok(const qtts_config& c, std::string& why) {
     if (hd != 64 && hd != 128) return why = "head dims must be 64 or 128", false;
   if (c.n_q_heads % c.n_kv_heads || c.cp_n_q_heads % c.cp_n_kv_heads) return why = "q heads % kv heads != 0", false;
   for (int gg : {c.n_q_heads / c.n_kv_heads, c.cp_n_q_heads / c.cp_n_kv_heads})
-    if (gg != 1 && gg != 2 && gg != 4) return why = "GQA group must be 1, 2 or 4", false;
+    if (gg != 1 && gg != 2) return why = "GQA group must be 1 or 2", false;
   if (c.n_kv_heads > 32 || c.cp_n_kv_heads > 32) return why = "at most 32 kv heads", false;
   // every GEMM K must be a multiple of 8 (vector loads) and one activation
   // row of it must fit the GEMV's shared-memory tile
@@ -301,12 +302,33 @@ std::vector<StageDesc> build_program(qtts_model* m, bool i8) {
   return P;
 }
 
+// The GEMV keeps one partial per (row unit, 1024-wide K slice, row) of this
+// CTA's share in shared memory; check every segment's share fits.
+int check_gemv_tiles(qtts_model* m, const std::vector<StageDesc>& P) {
+  for (const StageDesc& d : P) {
+    if (d.type != ST_GEMV) continue;
+    for (int s = 0; s < d.nseg; ++s) {
+      const Seg& sg = d.seg[s];
+      const int units = sg.N / sg.unit;
+      const int upc = (units + m->G - 1) / m->G;
+      const int nkc = (d.K + 1023) / 1024;
+      if ((long long)upc * nkc * sg.unit * 8 > 2048 || upc * 8 > 512)
+        return fail(m, QTTS_E_INVALID, "a %d x %d GEMV share does not fit the %d-SM grid's shared memory", sg.N,
+                    d.K, m->G);
+    }
+  }
+  return QTTS_OK;
+}
+
 int upload_program(qtts_model* m, bool i8) {
   std::vector<StageDesc> P = build_program(m, i8);
+  int rc;
+  if ((rc = check_gemv_tiles(m, P))) return rc;
   StageDesc*& dst = m->prog_dev[i8 ? 1 : 0];
   if (!dst) AL(m, dst, P.size());
   CK(m, cudaMemcpy(dst, P.data(), P.size() * sizeof(StageDesc), cudaMemcpyHostToDevice));
   m->n_stages = (int)P.size();
+  m->g.n_stages = m->n_stages;
   return QTTS_OK;
 }
 
@@ -492,6 +514,7 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
   g.Hc = c.cp_hidden; g.nqc = c.cp_n_q_heads; g.nkvc = c.cp_n_kv_heads; g.dc = c.cp_head_dim; g.Fc = c.cp_ffn;
   g.Vc = c.cp_vocab; g.eos_id = c.eos_id; g.n_codes = c.n_codes; g.seen_words = seen_words(c);
   g.max_context = c.max_context; g.eps = c.rms_eps; g.G = sms; g.pool_pages = c.kv_pool_pages;
+  g.prefetch = 0;
 
   const size_t kv_elems = (size_t)c.n_layers * c.kv_pool_pages * 2 * c.n_kv_heads * kPage * c.head_dim;
   if ((rc = dalloc(m, &m->kv_pool, kv_elems))) return bail(rc);
@@ -937,7 +960,31 @@ int qtts_set_option(qtts_model* m, int option, int value) {
     m->stepwise = value != 0;
     return QTTS_OK;
   }
+  if (option == QTTS_OPT_PREFETCH) {
+    if (value < 0 || value > 4) return fail(m, QTTS_E_INVALID, "prefetch distance must be 0..4");
+    m->g.prefetch = value;
+    return QTTS_OK;
+  }
+  if (option == QTTS_OPT_TRACE) {
+    if (!m->loaded) return fail(m, QTTS_E_STATE, "load weights first");
+    if (value && !m->trace_buf) {
+      cudaSetDevice(m->device);
+      AL(m, m->trace_buf, (size_t)4 * m->n_stages);
+    }
+    m->g.trace = value ? m->trace_buf : nullptr;
+    return QTTS_OK;
+  }
   return fail(m, QTTS_E_INVALID, "unknown option %d", option);
+}
+
+int qtts_frame_trace(qtts_model* m, uint64_t* host, int capacity) {
+  if (!m || !host || capacity < 0) return fail(m, QTTS_E_INVALID, "bad argument");
+  if (!m->trace_buf) return fail(m, QTTS_E_STATE, "tracing was never enabled");
+  cudaSetDevice(m->device);
+  CK(m, cudaStreamSynchronize(m->last_stream));
+  const int n = std::min(capacity, 4 * m->n_stages);
+  CK(m, cudaMemcpy(host, m->trace_buf, (size_t)n * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+  return n;
 }
 
 int qtts_frame_weight_bytes(const qtts_model* m, int64_t* bytes) {

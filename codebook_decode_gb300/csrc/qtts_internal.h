@@ -15,11 +15,11 @@ constexpr int kMaxBatch = 32;
 constexpr int kMaxRows = 2 * kMaxBatch;  // Code-Predictor step 1 runs two positions per session
 constexpr int kCodebooks = 16;
 constexpr int kPage = 16;
-constexpr int kMaxSplits = 64;           // split-K pieces per (session, kv head) in Talker attention
-constexpr int kMinChunk = 32;            // positions per split, at least one warp-tile
+constexpr int kMaxSplits = 128;          // split-K pieces per (session, kv head) in Talker attention
+constexpr int kMinChunk = 16;            // positions per split: at least one KV page
 constexpr int kMaxContext = kMaxSplits * kMinChunk;
 constexpr int kSmemX = 128 * 1024;       // GEMV activation tile (fp32 rows)
-constexpr int kSmemBytes = kSmemX + 16 * 1024;
+constexpr int kSmemBytes = kSmemX + 32 * 1024;
 constexpr int kMaxVocab = 4096;
 
 enum StageType { ST_BEGIN = 0, ST_GEMV = 1, ST_ATTN_T = 2, ST_ATTN_CP = 3, ST_SAMPLE = 4 };
@@ -61,7 +61,7 @@ struct StageDesc {
   const float* q;
   float* attn_out;
   int q_stride;
-  uint16_t* cp_kv;        // Code-Predictor cache of this layer [kMaxBatch][2][16][nkv][d]
+  uint16_t* cp_kv;        // Code-Predictor cache of this layer [kMaxBatch][2][nkv][16][d]
   // sampler
   int V;
   const float* table;     // projected embedding table T_j [V_j][Hc] fp32 (nullptr for j = 15)
@@ -96,6 +96,9 @@ struct Globals {
   int* committed;         // [kMaxBatch][16] codes fed forward (forced or sampled)
   unsigned* barrier;      // grid barrier counter (zeroed before each persistent launch)
   int* err;               // device error word (QTTS_DEV_*)
+  int prefetch;           // stages ahead whose weight slices are prefetched into L2 (0 = off)
+  int n_stages;
+  unsigned long long* trace;  // optional [2 CTAs][n_stages][start, end] %globaltimer stamps
 };
 
 struct FrameArgs {

@@ -26,6 +26,8 @@ QTTS_E_TIMEOUT = -11
 (QTTS_DEV_OK, QTTS_DEV_BAD_SESSION, QTTS_DEV_BAD_PAGE, QTTS_DEV_BAD_SAMPLING, QTTS_DEV_BAD_CODE,
  QTTS_DEV_TIMEOUT) = range(6)
 QTTS_OPT_STEPWISE = 1
+QTTS_OPT_PREFETCH = 2
+QTTS_OPT_TRACE = 3
 
 
 class QttsError(RuntimeError):
@@ -85,6 +87,7 @@ SIGNATURES = [
     ("qtts_sample", C.c_int, [_P, C.c_int, C.c_int, _P, C.c_int, _P, _P, _P, _P, _P]),
     ("qtts_set_option", C.c_int, [_P, C.c_int, C.c_int]),
     ("qtts_frame_weight_bytes", C.c_int, [_P, C.POINTER(C.c_int64)]),
+    ("qtts_frame_trace", C.c_int, [_P, _P, C.c_int]),
 ]
 
 
@@ -237,3 +240,11 @@ def qtts_frame_weight_bytes(m):
     v = C.c_int64(0)
     _check(m, load_library().qtts_frame_weight_bytes(m, C.byref(v)))
     return v.value
+
+
+def qtts_frame_trace(m, host_u64):
+    """Fill a uint64 numpy array with the last traced frame's stage stamps."""
+    n = load_library().qtts_frame_trace(m, ptr(host_u64), len(host_u64))
+    if n < 0:
+        _check(m, n)
+    return n

@@ -251,10 +251,24 @@ int qtts_feedback_embed(qtts_model* m, int B, const int32_t* codes, const uint16
 int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, const qtts_session* sessions,
                 const qtts_rng* rng, const uint32_t* seen, int32_t* codes_out, void* stream);
 
-/* Execution options. QTTS_OPT_STEPWISE = 1 runs the frame as one launch per
- * stage instead of one persistent launch (debugging aid; same results). */
+/* Execution options (same results whatever their values):
+ *   QTTS_OPT_STEPWISE  1: one launch per stage instead of one persistent
+ *                      launch per frame (debugging aid). Default 0.
+ *   QTTS_OPT_PREFETCH  stages ahead (0..4) whose weight rows each CTA asks
+ *                      the L2 to fetch while the grid waits at a barrier.
+ *                      Default 0.
+ *   QTTS_OPT_TRACE     1: record %globaltimer stamps at the start and end of
+ *                      every stage on the first and last CTA (qtts_frame_trace). */
 #define QTTS_OPT_STEPWISE 1
+#define QTTS_OPT_PREFETCH 2
+#define QTTS_OPT_TRACE 3
 int qtts_set_option(qtts_model* m, int option, int value);
+
+/* Stage timestamps of the last frame run with QTTS_OPT_TRACE on: 4 values per
+ * stage, [CTA 0 start, CTA 0 end] for every stage, then the same for the last
+ * CTA (nanoseconds, %globaltimer). Synchronises the model's last stream.
+ * Returns the number of values written (<= capacity) or a negative error. */
+int qtts_frame_trace(qtts_model* m, uint64_t* host, int capacity);
 
 /* Bytes of weights one frame streams (the roofline's numerator, without KV):
  * every GEMM weight once per pass that uses it, in the current precision. */
