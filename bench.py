@@ -141,25 +141,37 @@ def stage_names(d):
 
 
 def trace_summary(d, stamps):
-    """Per stage kind: mean body time on CTA 0 and mean wait from its end to
-    the next stage's start (the barrier), in microseconds."""
+    """Per stage kind, in microseconds on CTA 0: the stage body (start to end),
+    the wait from its end to the next stage's start (the grid barrier) and,
+    for GEMV stages, the prologue / weight pass / epilogue split."""
     names = stage_names(d)
     n = len(names)
-    t = stamps[: 2 * n].reshape(n, 2).astype(np.int64)
+    t = stamps[: 8 * n].reshape(n, 8).astype(np.int64)
     out = {}
     for i, nm in enumerate(names):
-        body = (t[i, 1] - t[i, 0]) / 1e3
-        gap = (t[i + 1, 0] - t[i, 1]) / 1e3 if i + 1 < n else 0.0
-        o = out.setdefault(nm, [0, 0.0, 0.0])
-        o[0] += 1
-        o[1] += body
-        o[2] += gap
-    total = (t[-1, 1] - t[0, 0]) / 1e3
-    return {"frame_us": total, "stages": {k: {"n": v[0], "body_us": v[1] / v[0], "barrier_us": v[2] / v[0],
-                                                "total_us": v[1] + v[2]} for k, v in out.items()}}
+        o = out.setdefault(nm, dict(n=0, body=0.0, barrier=0.0, pro=0.0, w=0.0, epi=0.0))
+        o["n"] += 1
+        o["body"] += (t[i, 7] - t[i, 0]) / 1e3
+        o["barrier"] += (t[i + 1, 0] - t[i, 7]) / 1e3 if i + 1 < n else 0.0
+        if t[i, 1] >= t[i, 0] and t[i, 3] <= t[i, 7] and t[i, 1] <= t[i, 2] <= t[i, 3]:
+            o["pro"] += (t[i, 1] - t[i, 0]) / 1e3
+            o["w"] += (t[i, 2] - t[i, 1]) / 1e3
+            o["epi"] += (t[i, 3] - t[i, 2]) / 1e3
+    total = (t[-1, 7] - t[0, 0]) / 1e3
+    ring = stamps[16 * n: 16 * n + 8192].reshape(4096, 2).astype(np.int64)
+    used = int((ring[:, 1] > 0).sum())
+    rq = ring[:used]
+    lead = (t[:, 0].min(), rq)
+    return {"frame_us": total, "ring": {"uses": used, "issue_us": ((rq[:, 0] - t[0, 0]) / 1e3).tolist(),
+                                          "ready_us": ((rq[:, 1] - t[0, 0]) / 1e3).tolist(),
+                                          "stage_start_us": ((t[:, 0] - t[0, 0]) / 1e3).tolist()},
+            "stages": {k: {"n": v["n"], "body_us": v["body"] / v["n"], "barrier_us": v["barrier"] / v["n"],
+                           "prologue_us": v["pro"] / v["n"], "weights_us": v["w"] / v["n"],
+                           "epilogue_us": v["epi"] / v["n"], "total_us": v["body"] + v["barrier"]}
+                       for k, v in out.items()}}
 
 
-def run_gpu(wl, steps, warmup, local, weights, prefetch=None, trace=False):
+def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None):
     import torch
 
     from codebook_decode_gb300 import qtts
@@ -172,8 +184,8 @@ def run_gpu(wl, steps, warmup, local, weights, prefetch=None, trace=False):
     pool = wl.batch * ((cap + 15) // 16) + 8
     eng = Engine(d, weights, max_batch=max(wl.batch, 1), max_context=cap, pool_pages=pool, device=local, int8=wl.int8)
     eng.setup_sessions(sess, cap, shuffle=wl.shuffle_pages)
-    if prefetch is not None:
-        qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_PREFETCH, prefetch)
+    if ring_slots is not None:
+        qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_RING_SLOTS, ring_slots)
     dev = eng.dev
     stream = torch.cuda.current_stream()
     sess0 = eng.sess.clone()
@@ -270,7 +282,7 @@ def run_gpu(wl, steps, warmup, local, weights, prefetch=None, trace=False):
         eng.sess.copy_(sess0)
         for _ in range(2):
             eng.step(emb, None, want_logits=False, stream=stream)
-        stamps = np.zeros(4 * len(stage_names(d)), dtype=np.uint64)
+        stamps = np.zeros(16 * len(stage_names(d)) + 2 * 4096, dtype=np.uint64)
         qtts.qtts_frame_trace(eng.m, stamps)
         res["trace"] = trace_summary(d, stamps)
     eng.release_pages()
@@ -309,8 +321,8 @@ def main():
     ap.add_argument("--workload", default="full_b1", choices=sorted(configs.WORKLOADS))
     ap.add_argument("--no-sweep", action="store_true", help="skip the B=8/B=32/INT8 side measurements")
     ap.add_argument("--oracle-frames", type=int, default=6)
-    ap.add_argument("--prefetch", type=int, default=None, help="L2 prefetch distance in stages (library default 1)")
     ap.add_argument("--trace", action="store_true", help="print a per-stage time breakdown to stderr")
+    ap.add_argument("--ring-slots", type=int, default=None, help="weight-ring depth per SM (library default 8)")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
     ws, rank, local = (1, 0, 0)
@@ -341,7 +353,7 @@ def main():
     import torch
     w = synth.make_weights(wl.dims, 1000 + wl.seed)
     barrier(ws)
-    r = run_gpu(wl, args.steps, args.warmup, local, w, prefetch=args.prefetch, trace=args.trace)
+    r = run_gpu(wl, args.steps, args.warmup, local, w, trace=args.trace, ring_slots=args.ring_slots)
     if args.trace:
         print(json.dumps(r["trace"]), file=sys.stderr)
     total_s = max_over_ranks(r["total_ms"] / 1e3, ws)
@@ -370,7 +382,7 @@ def main():
             sweep = {}
             for name in ("full_b8", "full_b32", "int8_b1", "int8_b32"):
                 o = configs.WORKLOADS[name]
-                rr = run_gpu(o, min(args.steps, 50), 3, local, w, prefetch=args.prefetch)  # same weights
+                rr = run_gpu(o, min(args.steps, 50), 3, local, w, ring_slots=args.ring_slots)  # same weights
                 sweep[name] = {"frames_per_s": o.batch * min(args.steps, 50) / (rr["total_ms"] / 1e3),
                                "frame_ms": rr["frame_ms"], "achieved_gbs": rr["achieved_gbs"],
                                "frac": rr["achieved_gbs"] / peak, "bytes_per_frame": rr["bytes_per_frame"]}

@@ -9,13 +9,23 @@
 // "De grens van snelheid en kosten verleggen voor Qwen3-TTS", section 3
 // (the Code Predictor's fixed 15 steps over a pre-allocated short cache).
 // The pages' engines replay ~1,600 kernels per frame as a CUDA graph; here the
-// whole frame is one launch, so the only per-stage cost is the barrier.
+// whole frame is one launch.
+//
+// Inside a CTA, warps 0..14 compute and warp 15 is a producer: it walks the
+// same stage program and streams this CTA's share of every upcoming weight
+// matrix into a ring of shared-memory slots with TMA bulk copies, running
+// ahead across stage boundaries and grid barriers (weights do not depend on
+// activations), so HBM keeps streaming while the grid synchronises.
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include "qtts_internal.h"
 
 namespace qtts {
+
+constexpr int kCWarps = kWarps - 1;          // compute warps
+constexpr int kCThreads = kCWarps * 32;
+constexpr int kProducerWarp = kCWarps;
 
 // ---------------------------------------------------------------------------
 // helpers
@@ -51,6 +61,18 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// barrier of the compute warps only (the producer warp never joins it)
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory"); }
+__device__ __forceinline__ int cbar_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.s32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(pred), "n"(kCThreads)
+      : "memory");
+  return r;
+}
+
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -70,13 +92,14 @@ __device__ __forceinline__ void red_release_gpu(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Grid-wide barrier with a bounded wait. After the CTA's bar.sync, thread 0
-// adds one to the counter with release semantics (publishing the whole CTA's
-// writes) and polls it with acquire loads until it reaches `target`. A wait
-// that outlives the limit sets QTTS_DEV_TIMEOUT, and an error word set
-// elsewhere also ends the wait. Returns false to make the CTA leave the frame.
+// Grid-wide barrier of the compute warps, with a bounded wait. After the
+// compute warps' bar.sync, thread 0 adds one to the counter with release
+// semantics (publishing the whole CTA's writes) and polls it with acquire
+// loads until it reaches `target`. A wait that outlives the limit sets
+// QTTS_DEV_TIMEOUT, and an error word set elsewhere also ends the wait.
+// Returns false to make the CTA leave the frame.
 __device__ bool grid_sync(const Globals& g, unsigned target, volatile int* sflag) {
-  __syncthreads();
+  cbar();
   if (threadIdx.x == 0) {
     red_release_gpu(g.barrier, 1u);
     int ok = 1;
@@ -97,24 +120,104 @@ __device__ bool grid_sync(const Globals& g, unsigned target, volatile int* sflag
     }
     *sflag = ok;
   }
-  __syncthreads();
+  cbar();
   return *sflag != 0;
 }
 
-// deterministic block sum (fixed combination order)
+// deterministic sum over the compute threads (fixed combination order)
 __device__ float block_sum(float v, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_sum(v);
-  __syncthreads();
+  cbar();
   if (lane == 0) red[warp] = v;
-  __syncthreads();
+  cbar();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < kWarps; ++w) t += red[w];
-    red[kWarps] = t;
+    for (int w = 0; w < kCWarps; ++w) t += red[w];
+    red[kCWarps] = t;
   }
-  __syncthreads();
-  return red[kWarps];
+  cbar();
+  return red[kCWarps];
+}
+
+// Stage trace: with tracing on, thread 0 of the first and the last CTA
+// stamps %globaltimer at up to 8 points of every stage (0 start, 1 after the
+// GEMV prologue, 2 after its phase 1, 3 after its phase 2, 7 end).
+constexpr int kTraceMarks = 8;
+constexpr int kTraceRing = 4096;  // ring uses traced per frame: issue and ready times on CTA 0
+__shared__ int g_trace_stage;
+__device__ __forceinline__ void trace_ring(const Globals& g, uint32_t q, int which) {
+  if (g.trace && blockIdx.x == 0 && q < (uint32_t)kTraceRing)
+    g.trace[(size_t)2 * g.n_stages * kTraceMarks + (size_t)q * 2 + which] = global_timer_ns();
+}
+__device__ __forceinline__ void trace_mark(const Globals& g, int which) {
+  if (g.trace && threadIdx.x == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1)) {
+    const int slot = blockIdx.x == 0 ? 0 : 1;
+    g.trace[((size_t)slot * g.n_stages + g_trace_stage) * kTraceMarks + which] = global_timer_ns();
+  }
+}
+
+// ---- mbarriers and TMA bulk copies into shared memory ----
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+// L2 policy for data read once per frame (weights, KV): evict it first, so
+// it streams through L2 without displacing the small data every stage reuses
+// (activations, gains, RoPE tables, block tables, stage descriptors)
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// generic-proxy global writes (KV appends) become visible to later bulk copies
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar` to complete, at most kBarrierTimeoutNs; an
+// error word set elsewhere ends the wait too.
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  unsigned spins = 0;
+  while (!mbar_test(bar, parity)) {
+    if ((++spins & 15u) == 0u) {
+      if (read_err(err)) return false;
+      if (global_timer_ns() - t0 > kBarrierTimeoutNs) {
+        set_err(err, QTTS_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -198,7 +301,7 @@ __device__ __forceinline__ bool better(bool have, float val, int id, bool bhave,
   return val > bv || (val == bv && id < bid);
 }
 
-// Block-wide arg-best over (have, val, id); every thread gets the winner.
+// Arg-best over the compute threads (have, val, id); every thread gets the winner.
 __device__ int block_argbest(bool have, float val, int id, float* redv, int* redi, int* redh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -212,27 +315,44 @@ __device__ int block_argbest(bool have, float val, int id, float* redv, int* red
       have = oh;
     }
   }
-  __syncthreads();
+  cbar();
   if (lane == 0) {
     redv[warp] = val;
     redi[warp] = id;
     redh[warp] = have;
   }
-  __syncthreads();
+  cbar();
   if (threadIdx.x == 0) {
     bool bh = false;
     float bv = 0.f;
     int bi = 0;
-    for (int w = 0; w < kWarps; ++w)
+    for (int w = 0; w < kCWarps; ++w)
       if (better(redh[w] != 0, redv[w], redi[w], bh, bv, bi)) {
         bh = redh[w] != 0;
         bv = redv[w];
         bi = redi[w];
       }
-    redi[kWarps] = bi;
+    redi[kCWarps] = bi;
   }
-  __syncthreads();
-  return redi[kWarps];
+  cbar();
+  return redi[kCWarps];
+}
+
+// Exclusive prefix sum of one int per compute thread (thread order).
+__device__ int block_excl_scan(int v, int* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  cbar();
+  if (lane == 31) wsum[warp] = incl;
+  cbar();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += wsum[w];
+  return base + incl - v;
 }
 
 // ---------------------------------------------------------------------------
@@ -249,7 +369,7 @@ struct SampleSmem {
   float lp[kMaxVocab];
   uint32_t key[kMaxVocab];
   int hist[256];
-  int scan[kThreads];
+  int wsum[kWarps];
   float redv[kWarps + 1];
   int redi[kWarps + 1];
   int redh[kWarps + 1];
@@ -260,7 +380,7 @@ struct SampleSmem {
 __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, int j, const qtts_session& ss,
                           uint32_t key0, uint32_t key1, uint32_t fctr, const uint32_t* seen, int eos_id,
                           int n_codes) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   float T;
   int k;
   if (j == 0) {
@@ -270,7 +390,7 @@ __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, i
     T = ss.cp_temperature;
     k = ss.cp_top_k;
   }
-  for (int v = tid; v < V; v += kThreads) {
+  for (int v = tid; v < V; v += kCThreads) {
     float l = row_cg ? __ldcg(row + v) : row[v];
     if (j == 0) {
       if (v >= n_codes && v != eos_id) l = -INFINITY;
@@ -280,10 +400,10 @@ __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, i
     }
     S.lp[v] = l;
   }
-  __syncthreads();
+  cbar();
 
   // contiguous id block per thread, visited in ascending order
-  const int per = (V + kThreads - 1) / kThreads;
+  const int per = (V + kCThreads - 1) / kCThreads;
   const int v0 = min(V, tid * per), v1 = min(V, v0 + per);
 
   if (T == 0.0f || k == 1) {
@@ -300,29 +420,37 @@ __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, i
   }
 
   if (k <= 0 || k > V) k = V;
-  for (int v = tid; v < V; v += kThreads) {
+  for (int v = tid; v < V; v += kCThreads) {
     float z = __fdiv_rn(S.lp[v], T);
     if (z == 0.0f) z = 0.0f;
     S.lp[v] = z;
     S.key[v] = order_key(z);
   }
-  __syncthreads();
+  cbar();
 
   const bool take_all = (k == V);
   uint32_t thr = 0u;
   int rem = 0;
   if (!take_all) {
-    // MSB-first radix select of the k-th largest key
+    // MSB-first radix select of the k-th largest key, 8 bits per pass; a warp
+    // adds equal digits together so hot bins see one atomic per warp
     uint32_t prefix = 0u, pmask = 0u;
     rem = k;
     for (int shift = 24; shift >= 0; shift -= 8) {
       if (tid < 256) S.hist[tid] = 0;
-      __syncthreads();
-      for (int v = tid; v < V; v += kThreads) {
-        const uint32_t kk = S.key[v];
-        if ((kk & pmask) == prefix) atomicAdd(&S.hist[(kk >> shift) & 255u], 1);
+      cbar();
+      for (int v0w = tid - lane; v0w < V; v0w += kCThreads) {
+        const int v = v0w + lane;
+        const uint32_t kk = v < V ? S.key[v] : 0u;
+        const bool in = v < V && (kk & pmask) == prefix;
+        const unsigned act = __ballot_sync(0xffffffffu, in);
+        if (in) {
+          const uint32_t dig = (kk >> shift) & 255u;
+          const unsigned same = __match_any_sync(act, dig);
+          if ((__ffs(same) - 1) == lane) atomicAdd(&S.hist[dig], __popc(same));
+        }
       }
-      __syncthreads();
+      cbar();
       if (tid < 32) {
         // lane L owns digits 255-8L .. 248-8L (descending)
         int part = 0;
@@ -351,11 +479,10 @@ __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, i
           S.sel_rem = rem - cum;
         }
       }
-      __syncthreads();
+      cbar();
       prefix = S.sel_prefix;
       rem = S.sel_rem;
       pmask |= 255u << shift;
-      __syncthreads();
     }
     thr = prefix;  // k-th largest key; `rem` ties with it are kept, lowest ids first
   }
@@ -364,15 +491,7 @@ __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, i
   int ties = 0;
   if (!take_all)
     for (int v = v0; v < v1; ++v) ties += (S.key[v] == thr);
-  S.scan[tid] = ties;
-  __syncthreads();
-  for (int o = 1; o < kThreads; o <<= 1) {
-    const int t = (tid >= o) ? S.scan[tid - o] : 0;
-    __syncthreads();
-    S.scan[tid] += t;
-    __syncthreads();
-  }
-  int rank = S.scan[tid] - ties;
+  int rank = block_excl_scan(ties, S.wsum);
 
   bool have = false;
   float bv = 0.f;
@@ -409,7 +528,7 @@ __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, i
 __device__ bool stage_begin(const Globals& g, const FrameArgs& fa, unsigned char* smem) {
   const int tid = threadIdx.x;
   int bad = 0;
-  for (int b = tid; b < fa.B; b += kThreads) {
+  for (int b = tid; b < fa.B; b += kCThreads) {
     const qtts_session s = fa.sess[b];
     const int kv = s.kv_len;
     if (kv < 0 || kv + 1 > g.max_context || kv + 1 > fa.bt_stride * kPage) bad = QTTS_DEV_BAD_SESSION;
@@ -421,77 +540,140 @@ __device__ bool stage_begin(const Globals& g, const FrameArgs& fa, unsigned char
     const int kv = fa.sess[b].kv_len;
     if (kv < 0 || kv + 1 > fa.bt_stride * kPage) continue;  // reported above
     const int np = kv / kPage + 1;
-    for (int p = tid; p < np; p += kThreads) {
+    for (int p = tid; p < np; p += kCThreads) {
       const int page = fa.bt[(size_t)b * fa.bt_stride + p];
       if (page < 0 || page >= g.pool_pages) bad = QTTS_DEV_BAD_PAGE;
     }
   }
   if (fa.forced)
-    for (int i = tid; i < fa.B * kCodebooks; i += kThreads) {
+    for (int i = tid; i < fa.B * kCodebooks; i += kCThreads) {
       const int c = fa.forced[i];
       const int V = (i % kCodebooks) == 0 ? g.V0 : g.Vc;
       if (c < 0 || c >= V) bad = QTTS_DEV_BAD_CODE;
     }
   if (bad && blockIdx.x == 0) set_err(g.err, bad);
-  if (__syncthreads_or(bad)) return false;
+  if (cbar_or(bad)) return false;
 
   if (blockIdx.x == 0)
-    for (int i = tid; i < kMaxBatch * g.nkv; i += kThreads) g.attn_cnt[i] = 0;
+    for (int i = tid; i < kMaxBatch * g.nkv; i += kCThreads) g.attn_cnt[i] = 0;
 
   float* red = (float*)smem;
   const int b = blockIdx.x;
   float ss = 0.f;
   if (b < fa.B) {
-    for (int k = tid; k < g.H; k += kThreads) {
+    for (int k = tid; k < g.H; k += kCThreads) {
       const float x = bf2f(fa.in_embeds[(size_t)b * g.H + k]);
       g.x_t[(size_t)b * g.H + k] = x;
       ss += x * x;
     }
   }
   ss = block_sum(ss, red);
-  for (int r = tid; r < fa.B; r += kThreads) g.ssq_t[(size_t)blockIdx.x * kMaxRows + r] = (r == b) ? ss : 0.f;
+  for (int r = tid; r < fa.B; r += kCThreads) g.ssq_t[(size_t)blockIdx.x * kMaxRows + r] = (r == b) ? ss : 0.f;
   return true;
 }
 
 // ---------------------------------------------------------------------------
 // stage: GEMV with a fused prologue (RMSNorm) and epilogues
 //   Y[rows, N] = X[rows, K] W[N, K]^T, W streamed once for all rows.
-// Each CTA owns a contiguous range of row units; each warp walks its units,
-// lanes striding K in 8-element (16-byte bf16 / 8-byte int8) vectors.
+// A segment's rows are split over the grid in contiguous row units; this
+// CTA's share is cut into tasks of one unit x a 1024-wide slice of K.
+// Ring path (rows small enough that the whole activation tile stays in
+// shared memory): the producer warp has already copied each task's weights
+// into a ring slot. Direct path (larger batches): lanes load the weights
+// themselves, once per tile of activation rows.
 // ---------------------------------------------------------------------------
 
-// Phase-1 work item: one row unit and a 1024-wide slice of K, so that a lane
-// has all of its (up to 4 per row) 16-byte weight loads in flight at once.
 constexpr int kKChunk = 1024;
-constexpr int kSub = kKChunk / 256;
-constexpr int kPartFloats = 2048;
+constexpr int kSub = kKChunk / 256;   // 16-byte vectors per lane per row per task
+constexpr int kPartFloats = 1536;
 constexpr int kSqFloats = 512;
+constexpr int kRingSlots = 8;
+constexpr int kSlotBytes = 16384;     // whole weight rows, one bulk copy per slot
+static_assert(kWorkBytes + kTailBytes + kRingSlots * kSlotBytes <= kSmemBytes, "shared-memory plan");
 
 struct GemvSmemTail {
   float rfac[8];
   float ssq_row[kMaxRows];   // this CTA's sum of squares per stage row
   float part[kPartFloats];   // phase-1 partial dot products [task][U][RT]
   float sq[kSqFloats];       // phase-2 squares [unit][RT]
+  float resid[kSqFloats];    // E_RESID operands x[row][unit] [unit][RT], loaded in the prologue
 };
-static_assert(sizeof(GemvSmemTail) <= kSmemBytes - kSmemX, "GEMV shared-memory tail");
+static_assert(sizeof(GemvSmemTail) <= kTailBytes, "GEMV shared-memory tail");
 
-template <typename WT>
-__device__ __forceinline__ void load_w8(const WT* base, float out[8]);
+// full[x]: the slot's bytes have landed (producer arms it, the bulk copy
+// completes it); empty[x]: its consumer is done with it; seq[x]: which use of
+// the slot (sequence index / slots in use) the producer has armed last. A
+// consumer waits for seq[x] to show its use before its parity wait on
+// full[x], so that wait is never for a phase two steps ahead of the barrier
+// (several warps consume slots independently).
+struct Ring {
+  uint64_t full[kRingSlots];
+  uint64_t empty[kRingSlots];
+  uint32_t seq[kRingSlots];
+  uint32_t done[kRingSlots];  // tasks of the slot's current use finished so far
+};
 
-template <>
-__device__ __forceinline__ void load_w8<uint16_t>(const uint16_t* p, float o[8]) {
-  const uint4 v = ld_stream16(p);
-  o[0] = bf_lo(v.x); o[1] = bf_hi(v.x); o[2] = bf_lo(v.y); o[3] = bf_hi(v.y);
-  o[4] = bf_lo(v.z); o[5] = bf_hi(v.z); o[6] = bf_lo(v.w); o[7] = bf_hi(v.w);
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) { return *(const volatile uint32_t*)p; }
+
+// Wait until ring slot `slot` holds use `use` and its bytes have landed.
+__device__ bool ring_wait_full(Ring* ring, int slot, uint32_t use, int* err) {
+  if (ld_volatile_u32(&ring->seq[slot]) != use) {
+    const uint64_t t0 = global_timer_ns();
+    unsigned spins = 0;
+    while (ld_volatile_u32(&ring->seq[slot]) != use) {
+      if ((++spins & 15u) == 0u) {
+        if (read_err(err)) return false;
+        if (global_timer_ns() - t0 > kBarrierTimeoutNs) {
+          set_err(err, QTTS_DEV_TIMEOUT);
+          return false;
+        }
+      }
+    }
+  }
+  return mbar_wait(&ring->full[slot], use & 1u, err);
 }
-template <>
-__device__ __forceinline__ void load_w8<int8_t>(const int8_t* p, float o[8]) {
-  const uint2 v = ld_stream8(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = (float)(int)(int8_t)((v.x >> (8 * i)) & 0xFFu);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) o[4 + i] = (float)(int)(int8_t)((v.y >> (8 * i)) & 0xFFu);
+
+// Copy a stage descriptor from global to shared memory (one warp).
+__device__ __forceinline__ void fetch_desc(const StageDesc* src, StageDesc* dst) {
+  constexpr int n = sizeof(StageDesc) / 16;
+  static_assert(sizeof(StageDesc) % 16 == 0 && n <= 32, "descriptor copy");
+  const int lane = threadIdx.x & 31;
+  if (lane < n) reinterpret_cast<int4*>(dst)[lane] = __ldg(reinterpret_cast<const int4*>(src) + lane);
 }
+
+__device__ __forceinline__ unsigned char* ring_slot(unsigned char* smem, int slot) {
+  return smem + kWorkBytes + kTailBytes + slot * kSlotBytes;
+}
+
+// Activation rows per tile of a GEMV stage; 0 when the stage takes the
+// direct path. The producer and the compute warps evaluate the same rule.
+__device__ __forceinline__ int ring_rt(const StageDesc& d, int B) {
+  const int rows = B * d.rps;
+  int RT = 1;
+  while (RT < rows) RT *= 2;
+  if (RT > 8) return 0;
+  const int need = (RT + (d.xsrc == X_NORM ? 1 : 0)) * d.K * 4;
+  if (need > kWorkBytes) return 0;
+  for (int s = 0; s < d.nseg; ++s)  // a row unit must fit one slot
+    if (d.seg[s].unit * d.K * (d.seg[s].scale ? 1 : 2) > kSlotBytes) return 0;
+  return RT;
+}
+
+// This CTA's share of one segment: units [u0, u0 + nu), each cut into nkc
+// K-slices (the tasks); on the ring path, slots of `upslot` whole units.
+struct SegShare {
+  int u0, nu, nkc, upslot, nslot;
+  __device__ SegShare(const Seg& sg, int K) {
+    const unsigned units = (unsigned)(sg.N / sg.unit);  // units * gridDim.x < 2^32
+    u0 = (int)(units * blockIdx.x / gridDim.x);
+    nu = (int)(units * (blockIdx.x + 1) / gridDim.x) - u0;
+    nkc = (K + kKChunk - 1) / kKChunk;
+    const int unit_bytes = sg.unit * K * (sg.scale ? 1 : 2);
+    upslot = kSlotBytes / unit_bytes;
+    if (upslot < 1) upslot = 1;
+    nslot = (nu + upslot - 1) / upslot;
+  }
+};
 
 struct RowMap {
   int rps, in_rps, in_off;
@@ -521,7 +703,7 @@ __device__ __forceinline__ uint16_t* cp_kv_ptr(const Globals& g, uint16_t* layer
 
 // Epilogue for one output unit (rows n0, n0+1 when U == 2) of stage row r.
 __device__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, int n0,
-                              float y0, float y1, int r, float& ssq_acc) {
+                              float y0, float y1, int r, float resid, float& ssq_acc) {
   const int b = r / d.rps, p = r % d.rps;
   const int orow = out_row_of(sg, d.rps, r);
   switch (sg.epi) {
@@ -562,9 +744,9 @@ __device__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& 
       }
       break;
     }
-    case E_RESID: {
+    case E_RESID: {  // `resid`: x[orow][n0], loaded in the prologue
       float* x = sg.out + (size_t)orow * sg.out_stride + n0;
-      const float v = __ldcg(x) + y0;
+      const float v = resid + y0;
       *x = v;
       ssq_acc += v * v;
       break;
@@ -593,6 +775,7 @@ template <typename WT>
 struct Raw8 {
   using T = uint4;  // 8 bf16
   static __device__ __forceinline__ T load(const WT* p) { return ld_stream16(p); }
+  static __device__ __forceinline__ T lds(const WT* p) { return *reinterpret_cast<const uint4*>(p); }
   static __device__ __forceinline__ void unpack(const T& v, float o[8]) {
     o[0] = bf_lo(v.x); o[1] = bf_hi(v.x); o[2] = bf_lo(v.y); o[3] = bf_hi(v.y);
     o[4] = bf_lo(v.z); o[5] = bf_hi(v.z); o[6] = bf_lo(v.w); o[7] = bf_hi(v.w);
@@ -602,6 +785,7 @@ template <>
 struct Raw8<int8_t> {
   using T = uint2;  // 8 int8
   static __device__ __forceinline__ T load(const int8_t* p) { return ld_stream8(p); }
+  static __device__ __forceinline__ T lds(const int8_t* p) { return *reinterpret_cast<const uint2*>(p); }
   static __device__ __forceinline__ void unpack(const T& v, float o[8]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = (float)(int)(int8_t)((v.x >> (8 * i)) & 0xFFu);
@@ -610,147 +794,224 @@ struct Raw8<int8_t> {
   }
 };
 
-// This CTA's share of rows [u0*U, u1*U) of one segment for stage rows
-// [r0, r0 + nr): phase 1 spreads (unit, K-slice) tasks over all warps and
-// leaves one partial per task in shared memory; phase 2 gives each (unit, row)
-// to one thread, which sums the partials in K order and runs the epilogue.
+// One task's partial dot products: U rows x up to 1024 of K against nr
+// activation rows, from registers already holding the weight vectors.
 template <typename WT, int U, int RT>
-__device__ void gemv_seg(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, const float* xs,
-                         int r0, int nr, GemvSmemTail* tail) {
-  using R = Raw8<WT>;
-  const int K = d.K;
-  const int units = sg.N / U;
-  const int u0 = (int)((long long)units * blockIdx.x / gridDim.x);
-  const int u1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x);
-  const int nu = u1 - u0;
-  const int nkc = (K + kKChunk - 1) / kKChunk;
-  const int ntask = nu * nkc;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WT* W = (const WT*)sg.w;
-  for (int t = warp; t < ntask; t += kWarps) {
-    const int ul = t / nkc, kc = t - ul * nkc;
-    const int n0 = (u0 + ul) * U;
-    const int kb = kc * kKChunk + lane * 8;
-    typename R::T raw[kSub][U];
+__device__ __forceinline__ void task_fma(const typename Raw8<WT>::T (&raw)[kSub][U], const float* xs, int K, int kb,
+                                         int nr, float (&acc)[U][RT]) {
 #pragma unroll
-    for (int sb = 0; sb < kSub; ++sb) {
-      const int k = kb + sb * 256;
+  for (int i = 0; i < U; ++i)
 #pragma unroll
-      for (int i = 0; i < U; ++i) raw[sb][i] = (k < K) ? R::load(W + (size_t)(n0 + i) * K + k) : typename R::T{};
-    }
-    float acc[U][RT];
+    for (int r = 0; r < RT; ++r) acc[i][r] = 0.f;
 #pragma unroll
-    for (int i = 0; i < U; ++i)
+  for (int sb = 0; sb < kSub; ++sb) {
+    const int k = kb + sb * 256;
+    if (k < K) {
+      float wv[U][8];
 #pragma unroll
-      for (int r = 0; r < RT; ++r) acc[i][r] = 0.f;
+      for (int i = 0; i < U; ++i) Raw8<WT>::unpack(raw[sb][i], wv[i]);
 #pragma unroll
-    for (int sb = 0; sb < kSub; ++sb) {
-      const int k = kb + sb * 256;
-      if (k < K) {
-        float wv[U][8];
+      for (int r = 0; r < RT; ++r) {
+        if (r < nr) {
+          const float4 a = *reinterpret_cast<const float4*>(xs + r * K + k);
+          const float4 c = *reinterpret_cast<const float4*>(xs + r * K + k + 4);
 #pragma unroll
-        for (int i = 0; i < U; ++i) R::unpack(raw[sb][i], wv[i]);
-#pragma unroll
-        for (int r = 0; r < RT; ++r) {
-          if (r < nr) {
-            const float4 a = *reinterpret_cast<const float4*>(xs + r * K + k);
-            const float4 c = *reinterpret_cast<const float4*>(xs + r * K + k + 4);
-#pragma unroll
-            for (int i = 0; i < U; ++i) {
-              float v = acc[i][r];
-              v = fmaf(wv[i][0], a.x, v);
-              v = fmaf(wv[i][1], a.y, v);
-              v = fmaf(wv[i][2], a.z, v);
-              v = fmaf(wv[i][3], a.w, v);
-              v = fmaf(wv[i][4], c.x, v);
-              v = fmaf(wv[i][5], c.y, v);
-              v = fmaf(wv[i][6], c.z, v);
-              v = fmaf(wv[i][7], c.w, v);
-              acc[i][r] = v;
-            }
+          for (int i = 0; i < U; ++i) {
+            float v = acc[i][r];
+            v = fmaf(wv[i][0], a.x, v);
+            v = fmaf(wv[i][1], a.y, v);
+            v = fmaf(wv[i][2], a.z, v);
+            v = fmaf(wv[i][3], a.w, v);
+            v = fmaf(wv[i][4], c.x, v);
+            v = fmaf(wv[i][5], c.y, v);
+            v = fmaf(wv[i][6], c.z, v);
+            v = fmaf(wv[i][7], c.w, v);
+            acc[i][r] = v;
           }
         }
       }
     }
-#pragma unroll
-    for (int i = 0; i < U; ++i)
-#pragma unroll
-      for (int r = 0; r < RT; ++r) {
-        const float v = warp_sum(acc[i][r]);
-        if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
-      }
   }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < nu * nr; idx += kThreads) {
+}
+
+// This CTA's share of one segment for stage rows [r0, r0 + nr): phase 1
+// spreads (unit, K-slice) tasks over the compute warps and leaves one partial
+// per task in shared memory; phase 2 gives each (unit, row) to one thread,
+// which sums the partials in K order and runs the epilogue. With `ring`,
+// task t's weights are in the ring slot of sequence index q + t.
+template <typename WT, int U, int RT>
+__device__ void gemv_seg(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, const float* xs,
+                         int r0, int nr, GemvSmemTail* tail, unsigned char* smem, Ring* ring, uint32_t q,
+                         const StageDesc* next, StageDesc* next_s) {
+  using R = Raw8<WT>;
+  const int K = d.K;
+  const SegShare sh(sg, K);
+  const int ntask = sh.nu * sh.nkc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WT* W = (const WT*)sg.w;
+  if (ring) {
+    // tasks go round-robin over the warps; the warp that finishes a slot's
+    // last task frees the slot
+    for (int t = warp; t < ntask; t += kCWarps) {
+      const int ul = t / sh.nkc, kc = t - ul * sh.nkc;
+      const int sl = ul / sh.upslot;
+      const int ua = sl * sh.upslot;
+      const int slot_tasks = (min(sh.nu, ua + sh.upslot) - ua) * sh.nkc;
+      const uint32_t qq = q + (uint32_t)sl;
+      const uint32_t nsl = (uint32_t)g.ring_slots;
+      const int slot = (int)(qq % nsl);
+      // a failed wait (time limit or an error elsewhere) leaves zeros and the
+      // warp carries on to every barrier; the frame is abandoned at the next
+      // grid barrier
+      const bool got = ring_wait_full(ring, slot, qq / nsl, g.err);
+      if (lane == 0 && kc == 0 && ul == ua) trace_ring(g, qq, 1);
+      const WT* rowp = (const WT*)ring_slot(smem, slot) + (size_t)(ul - ua) * U * K;
+      const int kb = kc * kKChunk + lane * 8;
+      typename R::T raw[kSub][U];
+#pragma unroll
+      for (int sb = 0; sb < kSub; ++sb)
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+          raw[sb][i] = (got && kb + sb * 256 < K) ? R::lds(rowp + (size_t)i * K + kb + sb * 256) : typename R::T{};
+      float acc[U][RT];
+      task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
+      __syncwarp();
+      if (lane == 0 && got) {
+        if (atomicAdd(&ring->done[slot], 1u) + 1u == (uint32_t)slot_tasks) {
+          ring->done[slot] = 0u;
+          mbar_arrive(&ring->empty[slot]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < U; ++i)
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+          const float v = warp_sum(acc[i][r]);
+          if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
+        }
+    }
+  } else {
+    for (int t = warp; t < ntask; t += kCWarps) {
+      const int ul = t / sh.nkc, kc = t - ul * sh.nkc;
+      const int n0 = (sh.u0 + ul) * U;
+      const int kb = kc * kKChunk + lane * 8;
+      typename R::T raw[kSub][U];
+#pragma unroll
+      for (int sb = 0; sb < kSub; ++sb) {
+        const int k = kb + sb * 256;
+#pragma unroll
+        for (int i = 0; i < U; ++i) raw[sb][i] = (k < K) ? R::load(W + (size_t)(n0 + i) * K + k) : typename R::T{};
+      }
+      float acc[U][RT];
+      task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
+#pragma unroll
+      for (int i = 0; i < U; ++i)
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+          const float v = warp_sum(acc[i][r]);
+          if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
+        }
+    }
+  }
+  cbar();
+  trace_mark(g, 2);
+  if (next && (threadIdx.x >> 5) == kCWarps - 1) fetch_desc(next, next_s);
+  for (int idx = threadIdx.x; idx < sh.nu * nr; idx += kCThreads) {
     const int ul = idx / nr, r = idx - ul * nr;
-    const int n0 = (u0 + ul) * U;
+    const int n0 = (sh.u0 + ul) * U;
     float y[U];
 #pragma unroll
     for (int i = 0; i < U; ++i) {
       float acc = 0.f;
-      for (int kc = 0; kc < nkc; ++kc) acc += tail->part[((ul * nkc + kc) * U + i) * RT + r];
+      for (int kc = 0; kc < sh.nkc; ++kc) acc += tail->part[((ul * sh.nkc + kc) * U + i) * RT + r];
       y[i] = sg.scale ? acc * sg.scale[n0 + i] : acc;
     }
     float sqv = 0.f;
-    gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + r, sqv);
+    gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + r, tail->resid[ul * RT + r], sqv);
     tail->sq[ul * RT + r] = sqv;
   }
-  __syncthreads();
+  cbar();
+  trace_mark(g, 3);
   if (sg.ssq_out)
-    for (int r = threadIdx.x; r < nr; r += kThreads) {
+    for (int r = threadIdx.x; r < nr; r += kCThreads) {
       float acc = 0.f;
-      for (int ul = 0; ul < nu; ++ul) acc += tail->sq[ul * RT + r];
+      for (int ul = 0; ul < sh.nu; ++ul) acc += tail->sq[ul * RT + r];
       tail->ssq_row[r0 + r] += acc;
     }
-  __syncthreads();
+  cbar();
 }
 
 template <typename WT, int U>
 __device__ void gemv_seg_rt(int RT, const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa,
-                            const float* xs, int r0, int nr, GemvSmemTail* tail) {
+                            const float* xs, int r0, int nr, GemvSmemTail* tail, unsigned char* smem, Ring* ring,
+                            uint32_t q, const StageDesc* next, StageDesc* next_s) {
   switch (RT) {
-    case 1: gemv_seg<WT, U, 1>(d, sg, g, fa, xs, r0, nr, tail); break;
-    case 2: gemv_seg<WT, U, 2>(d, sg, g, fa, xs, r0, nr, tail); break;
-    case 4: gemv_seg<WT, U, 4>(d, sg, g, fa, xs, r0, nr, tail); break;
-    default: gemv_seg<WT, U, 8>(d, sg, g, fa, xs, r0, nr, tail); break;
+    case 1: gemv_seg<WT, U, 1>(d, sg, g, fa, xs, r0, nr, tail, smem, ring, q, next, next_s); break;
+    case 2: gemv_seg<WT, U, 2>(d, sg, g, fa, xs, r0, nr, tail, smem, ring, q, next, next_s); break;
+    case 4: gemv_seg<WT, U, 4>(d, sg, g, fa, xs, r0, nr, tail, smem, ring, q, next, next_s); break;
+    default: gemv_seg<WT, U, 8>(d, sg, g, fa, xs, r0, nr, tail, smem, ring, q, next, next_s); break;
   }
 }
 
-__device__ void stage_gemv(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+// q: this CTA's count of ring tasks consumed so far (advanced here).
+// next / next_s: the following stage's descriptor (or nullptr) and its
+// shared-memory buffer, filled by the last compute warp during phase 2.
+__device__ void stage_gemv(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem, Ring* ring,
+                           uint32_t& q, const StageDesc* next, StageDesc* next_s) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rows = fa.B * d.rps;
   const int K = d.K;
   const bool norm = d.xsrc == X_NORM;
   float* xs = (float*)smem;
-  GemvSmemTail* tail = (GemvSmemTail*)(smem + kSmemX);
-  for (int i = tid; i < kMaxRows; i += kThreads) tail->ssq_row[i] = 0.f;
+  GemvSmemTail* tail = (GemvSmemTail*)(smem + kWorkBytes);
+  for (int i = tid; i < kMaxRows; i += kCThreads) tail->ssq_row[i] = 0.f;
 
-  // activation rows per tile; a norm stage keeps one more row's worth for the gains
-  int RT = kSmemX / (K * 4) - (norm ? 1 : 0);
-  RT = RT >= 8 ? 8 : RT >= 4 ? 4 : RT >= 2 ? 2 : 1;
-  while (RT > 1 && RT / 2 >= rows) RT /= 2;
+  int RT = ring_rt(d, fa.B);
+  const bool use_ring = RT > 0;
+  if (!use_ring) {
+    // activation rows per tile; a norm stage keeps one more row's worth for the gains
+    RT = kWorkBytes / (K * 4) - (norm ? 1 : 0);
+    RT = RT >= 8 ? 8 : RT >= 4 ? 4 : RT >= 2 ? 2 : 1;
+    while (RT > 1 && RT / 2 >= rows) RT /= 2;
+  }
   float* gs = xs + RT * K;
   const RowMap rm{d.rps, d.in_rps, d.in_off};
 
   for (int r0 = 0; r0 < rows; r0 += RT) {
     const int nr = min(RT, rows - r0);
-    __syncthreads();
+    cbar();
     // issue the sum-of-squares loads, the activation loads and the gain loads
     // together: one L2 round trip for the whole prologue
     float ssq_part = 0.f;
     if (norm && warp < nr) {
       const int ir = rm.in_row(r0 + warp);
-      for (int c = lane; c < g.G; c += 32) ssq_part += __ldcg(d.ssq + (size_t)c * kMaxRows + ir);
+      float v[kMaxGrid / 32];
+#pragma unroll
+      for (int i = 0; i < kMaxGrid / 32; ++i) {
+        const int c = lane + 32 * i;
+        v[i] = c < g.G ? __ldcg(d.ssq + (size_t)c * kMaxRows + ir) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kMaxGrid / 32; ++i) ssq_part += v[i];
     }
-    for (int idx = tid * 4; idx < nr * K; idx += kThreads * 4) {
+    for (int idx = tid * 4; idx < nr * K; idx += kCThreads * 4) {
       const int r = idx / K, k = idx - r * K;
       const int ir = rm.in_row(r0 + r);
       *reinterpret_cast<float4*>(xs + r * K + k) =
           __ldcg(reinterpret_cast<const float4*>(d.x + (size_t)ir * d.x_stride + k));
     }
+    if (d.seg[0].epi == E_RESID) {  // single-segment stage: residual operands of its epilogue
+      const Seg& sg = d.seg[0];
+      const SegShare sh(sg, K);
+      for (int idx = tid; idx < sh.nu * nr; idx += kCThreads) {
+        const int ul = idx / nr, r = idx - ul * nr;
+        tail->resid[ul * RT + r] =
+            __ldcg(sg.out + (size_t)out_row_of(sg, d.rps, r0 + r) * sg.out_stride + (sh.u0 + ul) * sg.unit);
+      }
+    }
     if (norm) {
       if (r0 == 0)
-        for (int k = tid * 4; k < K; k += kThreads * 4) {
+        for (int k = tid * 4; k < K; k += kCThreads * 4) {
           const uint2 gw = *reinterpret_cast<const uint2*>(d.gain + k);
           *reinterpret_cast<float4*>(gs + k) = make_float4(bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y));
         }
@@ -758,8 +1019,8 @@ __device__ void stage_gemv(const StageDesc& d, const Globals& g, const FrameArgs
         const float sum = warp_sum(ssq_part);
         if (lane == 0) tail->rfac[warp] = 1.0f / sqrtf(sum / (float)K + g.eps);
       }
-      __syncthreads();
-      for (int idx = tid * 4; idx < nr * K; idx += kThreads * 4) {
+      cbar();
+      for (int idx = tid * 4; idx < nr * K; idx += kCThreads * 4) {
         const int r = idx / K, k = idx - r * K;
         const float f = tail->rfac[r];
         float4 v = *reinterpret_cast<float4*>(xs + r * K + k);
@@ -771,98 +1032,80 @@ __device__ void stage_gemv(const StageDesc& d, const Globals& g, const FrameArgs
         *reinterpret_cast<float4*>(xs + r * K + k) = v;
       }
     }
-    __syncthreads();
+    cbar();
+    trace_mark(g, 1);
     for (int s = 0; s < d.nseg; ++s) {
       const Seg& sg = d.seg[s];
+      Ring* rg = use_ring ? ring : nullptr;
+      // the next descriptor is fetched once, in the last segment of the last row tile
+      const bool last = s == d.nseg - 1 && r0 + RT >= rows;
+      const StageDesc* nx = last ? next : nullptr;
       if (sg.scale) {
-        if (sg.unit == 2) gemv_seg_rt<int8_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail);
-        else gemv_seg_rt<int8_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail);
+        if (sg.unit == 2) gemv_seg_rt<int8_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail, smem, rg, q, nx, next_s);
+        else gemv_seg_rt<int8_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail, smem, rg, q, nx, next_s);
       } else {
-        if (sg.unit == 2) gemv_seg_rt<uint16_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail);
-        else gemv_seg_rt<uint16_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail);
+        if (sg.unit == 2) gemv_seg_rt<uint16_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail, smem, rg, q, nx, next_s);
+        else gemv_seg_rt<uint16_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail, smem, rg, q, nx, next_s);
       }
+      if (use_ring) q += (uint32_t)SegShare(sg, K).nslot;
     }
   }
   for (int s = 0; s < d.nseg; ++s) {
     const Seg& sg = d.seg[s];
+    if (sg.epi == E_QKV_T || sg.epi == E_QKV_CP) fence_proxy_async_global();  // K/V are read by bulk copies next
     if (!sg.ssq_out) continue;
-    for (int r = tid; r < rows; r += kThreads)
+    for (int r = tid; r < rows; r += kCThreads)
       sg.ssq_out[(size_t)blockIdx.x * kMaxRows + out_row_of(sg, d.rps, r)] = tail->ssq_row[r];
   }
 }
 
-// L2 prefetch of this CTA's weight rows of a GEMV stage (a hint: the bytes
-// stream from HBM while the grid waits at the barrier before that stage)
-__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
-  uint64_t a = (uint64_t)__cvta_generic_to_global(p);
-  uint64_t s = (a + 15) & ~15ull;
-  const uint64_t e = (a + bytes) & ~15ull;
-  while (s < e) {
-    const uint32_t n = (uint32_t)((e - s) < 65536ull ? (e - s) : 65536ull);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s), "r"(n) : "memory");
-    s += n;
-  }
-}
-
-__device__ void prefetch_stage(const StageDesc& d) {
-  if (d.type != ST_GEMV) return;
-  for (int s = 0; s < d.nseg; ++s) {
-    const Seg& sg = d.seg[s];
-    const int U = sg.unit;
-    const int units = sg.N / U;
-    const int u0 = (int)((long long)units * blockIdx.x / gridDim.x);
-    const int u1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x);
-    const size_t es = sg.scale ? 1 : 2;
-    prefetch_l2((const char*)sg.w + (size_t)u0 * U * d.K * es, (size_t)(u1 - u0) * U * d.K * es);
-  }
-}
-
 // ---------------------------------------------------------------------------
-// attention: one warp per (row, kv head[, split]); lanes own positions for
-// the scores and head dimensions for the value sum; online softmax
+// the producer warp: stream every ring-path task's weights, in the order the
+// compute warps consume them, into the ring (one elected lane issues)
 // ---------------------------------------------------------------------------
 
-// ---- TMA bulk copies into shared memory, tracked by an mbarrier ----
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void mbar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
-  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
-}
-// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst)),
-               "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for phase `parity` of `bar`, at most kBarrierTimeoutNs.
-__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_test(bar, parity)) {
-    if (global_timer_ns() - t0 > kBarrierTimeoutNs) {
-      set_err(err, QTTS_DEV_TIMEOUT);
-      return false;
+__device__ void producer(const StageDesc* prog, int s0, int s1, const Globals& g, const FrameArgs& fa,
+                         unsigned char* smem, Ring* ring) {
+  const uint64_t policy = l2_evict_first();
+  const uint32_t nsl = (uint32_t)g.ring_slots;
+  uint32_t q = 0;
+  bool ok = true;
+  for (int s = s0; s < s1 && ok; ++s) {
+    const StageDesc& d = prog[s];
+    if (d.type != ST_GEMV || ring_rt(d, fa.B) == 0) continue;
+    const int K = d.K;
+    for (int si = 0; si < d.nseg && ok; ++si) {
+      const Seg& sg = d.seg[si];
+      const SegShare sh(sg, K);
+      const int U = sg.unit;
+      const size_t es = sg.scale ? 1 : 2;
+      const unsigned char* W = (const unsigned char*)sg.w;
+      const size_t unit_bytes = (size_t)U * K * es;
+      for (int sl = 0; sl < sh.nslot; ++sl, ++q) {
+        const int ua = sl * sh.upslot, ub = min(sh.nu, ua + sh.upslot);
+        const uint32_t bytes = (uint32_t)((ub - ua) * unit_bytes);
+        const int slot = (int)(q % nsl);
+        if (!mbar_wait(&ring->empty[slot], ((q / nsl) & 1u) ^ 1u, g.err)) {
+          ok = false;
+          break;
+        }
+        trace_ring(g, q, 0);
+        *(volatile uint32_t*)&ring->seq[slot] = q / nsl;
+        mbar_arrive_expect_tx(&ring->full[slot], bytes);
+        bulk_load(ring_slot(smem, slot), W + (size_t)(sh.u0 + ua) * unit_bytes, bytes, &ring->full[slot], policy);
+      }
     }
   }
-  return true;
+  // before the warp leaves, every copy it issued has landed (so none writes
+  // into shared memory after the CTA is gone)
+  const uint32_t first = q > nsl ? q - nsl : 0;
+  for (uint32_t qq = first; qq < q; ++qq) {
+    if (!mbar_test(&ring->full[qq % nsl], (qq / nsl) & 1u)) {
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_test(&ring->full[qq % nsl], (qq / nsl) & 1u))
+        if (global_timer_ns() - t0 > kBarrierTimeoutNs) break;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -881,7 +1124,8 @@ struct AttnTile {
   uint64_t bar;
   uint64_t pad;
 };
-static_assert(kWarps * sizeof(AttnTile) <= kSmemBytes, "attention tiles");
+constexpr int kAttnWarps = 8;  // warps per CTA that run attention items
+static_assert(kAttnWarps * sizeof(AttnTile) <= kWorkBytes, "attention tiles");
 
 template <int HD, int GRP>
 struct AttnAcc {
@@ -970,9 +1214,10 @@ __device__ bool attn_fetch_fold(AttnTile& T, const uint16_t* ksrc, const uint16_
   __syncwarp();
   if (lane == 0) {
     fence_proxy_async_smem();
+    const uint64_t policy = l2_evict_first();
     mbar_arrive_expect_tx(&T.bar, 2 * bytes);
-    bulk_load(T.k, ksrc, bytes, &T.bar);
-    bulk_load(T.v, vsrc, bytes, &T.bar);
+    bulk_load(T.k, ksrc, bytes, &T.bar, policy);
+    bulk_load(T.v, vsrc, bytes, &T.bar, policy);
   }
   const bool ok = mbar_wait(&T.bar, parity, err);
   parity ^= 1u;
@@ -986,8 +1231,12 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
   constexpr int E = HD / 32;
   const int nkv = g.nkv;
   const int qstride = d.q_stride;
+  if (warp >= kAttnWarps) return;
   AttnTile& T = reinterpret_cast<AttnTile*>(smem)[warp];
-  if (lane == 0) mbar_init(&T.bar);
+  if (lane == 0) {
+    mbar_init(&T.bar, 1);
+    mbar_init_fence();
+  }
   __syncwarp();
   uint32_t parity = 0;
   // split plan, identical on every CTA (same inputs, same arithmetic): about
@@ -996,7 +1245,7 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
   int total = len;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-  const int target = g.G * kWarps;
+  const int target = g.G * kAttnWarps;
   int chunk = (total * nkv + target - 1) / target;
   chunk = ((chunk + kPage - 1) / kPage) * kPage;
   if (chunk < kMinChunk) chunk = kMinChunk;
@@ -1012,7 +1261,7 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
   const int layer = d.layer;
 
   // item i goes to CTA i % G, so the splits spread over the SMs first
-  for (int item = warp * g.G + blockIdx.x; item < n_items; item += g.G * kWarps) {
+  for (int item = warp * g.G + blockIdx.x; item < n_items; item += g.G * kAttnWarps) {
     const unsigned hit = __ballot_sync(0xffffffffu, incl > item);
     const int b = __ffs(hit) - 1;
     const int before = __shfl_sync(0xffffffffu, incl - nsp * nkv, b);
@@ -1110,12 +1359,16 @@ __device__ void stage_attn_cp(const StageDesc& d, const Globals& g, const FrameA
   const int nkv = g.nkvc;
   const int qstride = d.q_stride;
   const int rows = fa.B * d.rps;
+  if (warp >= kAttnWarps) return;
   AttnTile& T = reinterpret_cast<AttnTile*>(smem)[warp];
-  if (lane == 0) mbar_init(&T.bar);
+  if (lane == 0) {
+    mbar_init(&T.bar, 1);
+    mbar_init_fence();
+  }
   __syncwarp();
   uint32_t parity = 0;
   const float scale = rsqrtf((float)HD);
-  for (int item = warp * g.G + blockIdx.x; item < rows * nkv; item += g.G * kWarps) {
+  for (int item = warp * g.G + blockIdx.x; item < rows * nkv; item += g.G * kAttnWarps) {
     const int r = item / nkv, kvh = item % nkv;
     const int b = r / d.rps, p = r % d.rps;
     const int pos = d.pos_base + p;
@@ -1186,13 +1439,13 @@ __device__ void stage_sample(const StageDesc& d, const Globals& g, const FrameAr
     const float* src = d.table + (size_t)committed * g.Hc;
     float* dst = d.x_next + (size_t)row * g.Hc;
     float s = 0.f;
-    for (int k = threadIdx.x; k < g.Hc; k += kThreads) {
+    for (int k = threadIdx.x; k < g.Hc; k += kCThreads) {
       const float v = src[k];
       dst[k] = v;
       s += v * v;
     }
     s = block_sum(s, S.redv);
-    for (int c = threadIdx.x; c < g.G; c += kThreads) d.ssq_next[(size_t)c * kMaxRows + row] = (c == 0) ? s : 0.f;
+    for (int c = threadIdx.x; c < g.G; c += kCThreads) d.ssq_next[(size_t)c * kMaxRows + row] = (c == 0) ? s : 0.f;
   }
 }
 
@@ -1200,36 +1453,53 @@ __device__ void stage_sample(const StageDesc& d, const Globals& g, const FrameAr
 // the persistent frame kernel
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void trace_mark(const Globals& g, int s, int which) {
-  if (g.trace && threadIdx.x == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1)) {
-    const int slot = blockIdx.x == 0 ? 0 : 1;
-    g.trace[((size_t)slot * g.n_stages + s) * 2 + which] = global_timer_ns();
-  }
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     frame_kernel(const StageDesc* __restrict__ prog, int s0, int s1, Globals g, FrameArgs fa) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int sflag;
-  if (read_err(g.err)) return;  // a device error is sticky until qtts_frame_status clears it
-  if (g.prefetch > 1 && threadIdx.x == kThreads - 1)
-    for (int s = s0 + 1; s < min(s1, s0 + g.prefetch); ++s) prefetch_stage(prog[s]);
+  __shared__ Ring ring;
+  if (threadIdx.x == 0) {
+    sflag = read_err(g.err);  // a device error is sticky until qtts_frame_status clears it
+    for (int i = 0; i < kRingSlots; ++i) {
+      mbar_init(&ring.full[i], 1);
+      mbar_init(&ring.empty[i], 1);
+      ring.seq[i] = 0xFFFFFFFFu;
+      ring.done[i] = 0u;
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();  // the last barrier of all 16 warps: from here on, producer and compute warps part
+  if (sflag) return;
+  if ((threadIdx.x >> 5) == kProducerWarp) {
+    if ((threadIdx.x & 31) == 0) producer(prog, s0, s1, g, fa, smem, &ring);
+    return;
+  }
+  __shared__ StageDesc sdesc[2];
+  if ((threadIdx.x >> 5) == 0) fetch_desc(&prog[s0], &sdesc[s0 & 1]);
+  cbar();
+  uint32_t q = 0;
   unsigned bar = 0;
   for (int s = s0; s < s1; ++s) {
-    const StageDesc& d = prog[s];
-    trace_mark(g, s, 0);
-    if (g.prefetch > 0 && threadIdx.x == kThreads - 1 && s + g.prefetch < s1) prefetch_stage(prog[s + g.prefetch]);
+    const StageDesc& d = sdesc[s & 1];
+    const StageDesc* next = s + 1 < s1 ? &prog[s + 1] : nullptr;
+    StageDesc* next_s = &sdesc[(s + 1) & 1];
+    if (threadIdx.x == 0) g_trace_stage = s;
+    trace_mark(g, 0);
+    // stages other than GEMVs fetch the next descriptor up front, on a warp
+    // they leave idle (attention uses warps 0..7; the sampler's CTAs differ)
+    if (d.type != ST_GEMV && next && (threadIdx.x >> 5) == kCWarps - 1) fetch_desc(next, next_s);
     switch (d.type) {
       case ST_BEGIN:
         if (!stage_begin(g, fa, smem)) return;
         break;
-      case ST_GEMV: stage_gemv(d, g, fa, smem); break;
+      case ST_GEMV: stage_gemv(d, g, fa, smem, &ring, q, next, next_s); break;
       case ST_ATTN_T: stage_attn<true>(d, g, fa, smem); break;
       case ST_ATTN_CP: stage_attn<false>(d, g, fa, smem); break;
       case ST_SAMPLE: stage_sample(d, g, fa, smem); break;
       default: break;
     }
-    trace_mark(g, s, 1);
+    trace_mark(g, 7);
     if (s + 1 < s1) {
       bar += gridDim.x;
       if (!grid_sync(g, bar, &sflag)) return;
@@ -1238,10 +1508,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Sampling of caller-supplied logits [B][V] for codebook j (one CTA per
-// session): the same sampler the frame uses, without the next-input gather.
+// session, the compute warps of a frame CTA): the same sampler the frame
+// uses, without the next-input gather.
 __global__ void __launch_bounds__(kThreads, 1)
     sample_kernel(const float* __restrict__ logits, int V, int j, Globals g, FrameArgs fa) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
+  if ((threadIdx.x >> 5) >= kCWarps) return;
   const int b = blockIdx.x;
   SampleSmem& S = *reinterpret_cast<SampleSmem*>(smem);
   const qtts_session ss = fa.sess[b];

@@ -160,11 +160,12 @@ bool cfg_ok(const qtts_config& c, std::string& why) {
   for (int gg : {c.n_q_heads / c.n_kv_heads, c.cp_n_q_heads / c.cp_n_kv_heads})
     if (gg != 1 && gg != 2) return why = "GQA group must be 1 or 2", false;
   if (c.n_kv_heads > 32 || c.cp_n_kv_heads > 32) return why = "at most 32 kv heads", false;
-  // every GEMM K must be a multiple of 8 (vector loads) and one activation
-  // row of it must fit the GEMV's shared-memory tile
+  // every GEMM K must be a multiple of 16 (16-byte weight rows in int8 for
+  // the bulk copies) and one activation row plus the gains must fit the
+  // GEMV's shared-memory tile
   for (int k : {c.hidden, c.ffn, c.n_q_heads * c.head_dim, c.cp_hidden, c.cp_ffn, c.cp_n_q_heads * c.cp_head_dim}) {
-    if (k % 8) return why = "GEMM reduction sizes must be multiples of 8", false;
-    if ((size_t)k * 4 > (size_t)kSmemX) return why = "a GEMM reduction size exceeds the activation tile", false;
+    if (k % 16) return why = "GEMM reduction sizes must be multiples of 16", false;
+    if ((size_t)k * 8 > (size_t)kWorkBytes) return why = "a GEMM reduction size exceeds the activation tile", false;
   }
   if (!(c.rms_eps > 0.f) || !(c.rope_theta > 0.f) || !(c.cp_rope_theta > 0.f))
     return why = "eps and rope theta must be positive", false;
@@ -312,7 +313,7 @@ int check_gemv_tiles(qtts_model* m, const std::vector<StageDesc>& P) {
       const int units = sg.N / sg.unit;
       const int upc = (units + m->G - 1) / m->G;
       const int nkc = (d.K + 1023) / 1024;
-      if ((long long)upc * nkc * sg.unit * 8 > 2048 || upc * 8 > 512)
+      if ((long long)upc * nkc * sg.unit * 8 > 1536 || upc * 8 > 512)
         return fail(m, QTTS_E_INVALID, "a %d x %d GEMV share does not fit the %d-SM grid's shared memory", sg.N,
                     d.K, m->G);
     }
@@ -492,6 +493,7 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (!coop) return fail(nullptr, QTTS_E_CUDA, "device %d has no cooperative launch", device);
+  if (sms > kMaxGrid) return fail(nullptr, QTTS_E_CUDA, "device %d has more than %d SMs", device, kMaxGrid);
   int occ = 0;
   e = frame_kernel_occupancy(&occ);
   if (e != cudaSuccess || occ < 1)
@@ -514,7 +516,7 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
   g.Hc = c.cp_hidden; g.nqc = c.cp_n_q_heads; g.nkvc = c.cp_n_kv_heads; g.dc = c.cp_head_dim; g.Fc = c.cp_ffn;
   g.Vc = c.cp_vocab; g.eos_id = c.eos_id; g.n_codes = c.n_codes; g.seen_words = seen_words(c);
   g.max_context = c.max_context; g.eps = c.rms_eps; g.G = sms; g.pool_pages = c.kv_pool_pages;
-  g.prefetch = 0;
+  g.ring_slots = 8;
 
   const size_t kv_elems = (size_t)c.n_layers * c.kv_pool_pages * 2 * c.n_kv_heads * kPage * c.head_dim;
   if ((rc = dalloc(m, &m->kv_pool, kv_elems))) return bail(rc);
@@ -960,16 +962,16 @@ int qtts_set_option(qtts_model* m, int option, int value) {
     m->stepwise = value != 0;
     return QTTS_OK;
   }
-  if (option == QTTS_OPT_PREFETCH) {
-    if (value < 0 || value > 4) return fail(m, QTTS_E_INVALID, "prefetch distance must be 0..4");
-    m->g.prefetch = value;
+  if (option == QTTS_OPT_RING_SLOTS) {
+    if (value < 1 || value > 8) return fail(m, QTTS_E_INVALID, "ring slots must be 1..8");
+    m->g.ring_slots = value;
     return QTTS_OK;
   }
   if (option == QTTS_OPT_TRACE) {
     if (!m->loaded) return fail(m, QTTS_E_STATE, "load weights first");
     if (value && !m->trace_buf) {
       cudaSetDevice(m->device);
-      AL(m, m->trace_buf, (size_t)4 * m->n_stages);
+      AL(m, m->trace_buf, (size_t)16 * m->n_stages + 2 * 4096);
     }
     m->g.trace = value ? m->trace_buf : nullptr;
     return QTTS_OK;
@@ -982,7 +984,7 @@ int qtts_frame_trace(qtts_model* m, uint64_t* host, int capacity) {
   if (!m->trace_buf) return fail(m, QTTS_E_STATE, "tracing was never enabled");
   cudaSetDevice(m->device);
   CK(m, cudaStreamSynchronize(m->last_stream));
-  const int n = std::min(capacity, 4 * m->n_stages);
+  const int n = std::min(capacity, 16 * m->n_stages + 2 * 4096);
   CK(m, cudaMemcpy(host, m->trace_buf, (size_t)n * sizeof(uint64_t), cudaMemcpyDeviceToHost));
   return n;
 }

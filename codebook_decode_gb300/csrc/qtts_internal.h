@@ -18,9 +18,13 @@ constexpr int kPage = 16;
 constexpr int kMaxSplits = 128;          // split-K pieces per (session, kv head) in Talker attention
 constexpr int kMinChunk = 16;            // positions per split: at least one KV page
 constexpr int kMaxContext = kMaxSplits * kMinChunk;
-constexpr int kSmemX = 128 * 1024;       // GEMV activation tile (fp32 rows)
-constexpr int kSmemBytes = kSmemX + 32 * 1024;
+// dynamic shared memory: a work region (GEMV activation tile, attention
+// tiles, sampler), the GEMV partials, then the ring of weight slots
+constexpr int kWorkBytes = 80 * 1024;
+constexpr int kTailBytes = 12 * 1024;
+constexpr int kSmemBytes = kWorkBytes + kTailBytes + 128 * 1024;
 constexpr int kMaxVocab = 4096;
+constexpr int kMaxGrid = 256;            // persistent CTAs (SMs) the kernel supports
 
 enum StageType { ST_BEGIN = 0, ST_GEMV = 1, ST_ATTN_T = 2, ST_ATTN_CP = 3, ST_SAMPLE = 4 };
 enum XSrc { X_NORM = 0, X_PLAIN = 1 };
@@ -41,7 +45,7 @@ struct Seg {
   const uint16_t* bias;   // E_CPIN: optional bf16 bias [N]
 };
 
-struct StageDesc {
+struct alignas(16) StageDesc {
   int type;
   int rps;                // rows (positions) per session this stage works on
   int pos_base;           // Code-Predictor position of row p of a session: pos_base + p
@@ -96,8 +100,8 @@ struct Globals {
   int* committed;         // [kMaxBatch][16] codes fed forward (forced or sampled)
   unsigned* barrier;      // grid barrier counter (zeroed before each persistent launch)
   int* err;               // device error word (QTTS_DEV_*)
-  int prefetch;           // stages ahead whose weight slices are prefetched into L2 (0 = off)
   int n_stages;
+  int ring_slots;         // weight-ring slots in use (1..8): how far the producer may run ahead
   unsigned long long* trace;  // optional [2 CTAs][n_stages][start, end] %globaltimer stamps
 };
 

@@ -26,8 +26,8 @@ QTTS_E_TIMEOUT = -11
 (QTTS_DEV_OK, QTTS_DEV_BAD_SESSION, QTTS_DEV_BAD_PAGE, QTTS_DEV_BAD_SAMPLING, QTTS_DEV_BAD_CODE,
  QTTS_DEV_TIMEOUT) = range(6)
 QTTS_OPT_STEPWISE = 1
-QTTS_OPT_PREFETCH = 2
 QTTS_OPT_TRACE = 3
+QTTS_OPT_RING_SLOTS = 4
 
 
 class QttsError(RuntimeError):

@@ -254,19 +254,21 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
 /* Execution options (same results whatever their values):
  *   QTTS_OPT_STEPWISE  1: one launch per stage instead of one persistent
  *                      launch per frame (debugging aid). Default 0.
- *   QTTS_OPT_PREFETCH  stages ahead (0..4) whose weight rows each CTA asks
- *                      the L2 to fetch while the grid waits at a barrier.
- *                      Default 0.
- *   QTTS_OPT_TRACE     1: record %globaltimer stamps at the start and end of
- *                      every stage on the first and last CTA (qtts_frame_trace). */
+ *   QTTS_OPT_TRACE     1: record %globaltimer stamps inside every stage on
+ *                      the first and last CTA (qtts_frame_trace).
+ *   QTTS_OPT_RING_SLOTS 1..8: 16 KB weight slots per SM the producer warp may
+ *                      fill ahead of the compute warps. Default 8. */
 #define QTTS_OPT_STEPWISE 1
-#define QTTS_OPT_PREFETCH 2
 #define QTTS_OPT_TRACE 3
+#define QTTS_OPT_RING_SLOTS 4
 int qtts_set_option(qtts_model* m, int option, int value);
 
-/* Stage timestamps of the last frame run with QTTS_OPT_TRACE on: 4 values per
- * stage, [CTA 0 start, CTA 0 end] for every stage, then the same for the last
- * CTA (nanoseconds, %globaltimer). Synchronises the model's last stream.
+/* Stage timestamps of the last frame run with QTTS_OPT_TRACE on: 8 values
+ * per stage for CTA 0 (every stage in order), then the same for the last CTA
+ * (nanoseconds, %globaltimer; 0 = stage start, 1 after the GEMV prologue,
+ * 2 after its weight pass, 3 after its epilogues, 7 = stage end; unused
+ * marks keep older values); then, for CTA 0, 4096 pairs (issue, ready) of
+ * the weight ring's slot uses in order. Synchronises the model's last stream.
  * Returns the number of values written (<= capacity) or a negative error. */
 int qtts_frame_trace(qtts_model* m, uint64_t* host, int capacity);
 
