@@ -49,6 +49,21 @@ def measured_peak_gbs():
     return 6800.0, "fallback"
 
 
+def ncu_traffic(wl):
+    """DRAM bytes per frame-kernel launch from the committed ncu capture, or
+    None when the kernel source changed since it was taken or the capture was
+    of another workload."""
+    import hashlib
+    rec_path = os.path.join(ROOT, "codebook_decode_gb300", "ncu_traffic.json")
+    if not os.path.exists(rec_path):
+        return None
+    rec = json.load(open(rec_path))
+    src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_prefix"] or rec["workload"] != wl.name:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def kv_bytes_per_frame(d, kv_lens):
     """Algorithmic cache bytes of one frame: Talker K/V read over positions
     0..kv_len (new token included) and written at kv_len; Code-Predictor K/V
@@ -367,7 +382,7 @@ def main():
                        "parallelism": f"replicas x{ws}",
                        "l2": "inputs larger than L2: every frame streams the full weight set (GBs) through HBM"},
             "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": peak, "unit": "GB/s",
-                         "frac": r["achieved_gbs"] / peak, "traffic": None,
+                         "frac": r["achieved_gbs"] / peak, "traffic": ncu_traffic(wl),
                          "peak_kind": peak_kind, "kernel": "qtts::frame_kernel",
                          "bytes_per_launch": r["bytes_per_frame"], "launch_ms": r["frame_ms"]},
             "e2e": {"value": ws * r["e2e"]["value"], "unit": UNIT, "h2d_bytes_per_step": r["e2e"]["h2d"],
