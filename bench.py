@@ -186,7 +186,7 @@ def trace_summary(d, stamps):
                        for k, v in out.items()}}
 
 
-def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None):
+def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, trace_file=None):
     import torch
 
     from codebook_decode_gb300 import qtts
@@ -300,6 +300,15 @@ def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None):
         stamps = np.zeros(16 * len(stage_names(d)) + 2 * 4096, dtype=np.uint64)
         qtts.qtts_frame_trace(eng.m, stamps)
         res["trace"] = trace_summary(d, stamps)
+        if trace_file:  # every CTA's stage stamps, raw
+            qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_TRACE, 2)
+            eng.sess.copy_(sess0)
+            for _ in range(2):
+                eng.step(emb, None, want_logits=False, stream=stream)
+            G = torch.cuda.get_device_properties(local).multi_processor_count
+            raw = np.zeros(8 * G * len(stage_names(d)) + 2 * 4096, dtype=np.uint64)
+            qtts.qtts_frame_trace(eng.m, raw)
+            np.save(trace_file, raw)
     eng.release_pages()
     eng.close()
     return res
@@ -337,6 +346,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the B=8/B=32/INT8 side measurements")
     ap.add_argument("--oracle-frames", type=int, default=6)
     ap.add_argument("--trace", action="store_true", help="print a per-stage time breakdown to stderr")
+    ap.add_argument("--trace-file", default=None, help="with --trace: save every CTA's raw stage stamps (.npy)")
     ap.add_argument("--ring-slots", type=int, default=None, help="weight-ring depth per SM (library default 8)")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
@@ -368,7 +378,8 @@ def main():
     import torch
     w = synth.make_weights(wl.dims, 1000 + wl.seed)
     barrier(ws)
-    r = run_gpu(wl, args.steps, args.warmup, local, w, trace=args.trace, ring_slots=args.ring_slots)
+    r = run_gpu(wl, args.steps, args.warmup, local, w, trace=args.trace, ring_slots=args.ring_slots,
+                trace_file=args.trace_file)
     if args.trace:
         print(json.dumps(r["trace"]), file=sys.stderr)
     total_s = max_over_ranks(r["total_ms"] / 1e3, ws)

@@ -1,7 +1,9 @@
 // frame_kernel.cu -- one codec frame of the lockstep multi-codebook decode as
 // a single persistent kernel: one CTA per SM walks the frame's stage program
 // (Talker layers, codebook-0 head + projection, sampler, 15 Code-Predictor
-// steps) and the CTAs meet at a grid-wide barrier between dependent stages.
+// steps). Stages hand activations to one another as tagged words (value and
+// frame/stage tag in one 64-bit store), so a CTA starts a stage as soon as
+// the words it reads are there: no grid-wide barrier.
 //
 // The stage sequence follows "Qwen3-TTS Native v0.3.0", section "What
 // changed" (one batched call runs the talker and the 15-step code predictor
@@ -14,8 +16,8 @@
 // Inside a CTA, warps 0..14 compute and warp 15 is a producer: it walks the
 // same stage program and streams this CTA's share of every upcoming weight
 // matrix into a ring of shared-memory slots with TMA bulk copies, running
-// ahead across stage boundaries and grid barriers (weights do not depend on
-// activations), so HBM keeps streaming while the grid synchronises.
+// ahead across stage boundaries (weights do not depend on activations), so
+// HBM keeps streaming while the compute warps wait for their inputs.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -73,11 +75,6 @@ __device__ __forceinline__ int cbar_or(int pred) {
   return r;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -86,42 +83,88 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ int read_err(const int* e) { return *(const volatile int*)e; }
 __device__ __forceinline__ void set_err(int* e, int code) { atomicCAS(e, 0, code); }
 
-constexpr uint64_t kBarrierTimeoutNs = 2000000000ull;  // 2 s: a frame takes milliseconds
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: a frame takes milliseconds
 
-__device__ __forceinline__ void red_release_gpu(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// ---- tagged words (see StageDesc): one 64-bit access carries value and tag ----
+
+__device__ __forceinline__ uint64_t ll_word(uint32_t payload, uint32_t tag) {
+  return ((uint64_t)tag << 32) | payload;
 }
+__device__ __forceinline__ void st_ll(uint64_t* p, float v, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(ll_word(__float_as_uint(v), tag)) : "memory");
+}
+__device__ __forceinline__ void st_ll_raw(uint64_t* p, uint32_t payload, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(ll_word(payload, tag)) : "memory");
+}
+__device__ __forceinline__ void st_ll2(uint64_t* p, float v0, float v1, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(ll_word(__float_as_uint(v0), tag)),
+               "l"(ll_word(__float_as_uint(v1), tag))
+               : "memory");
+}
+__device__ __forceinline__ uint64_t ld_ll(const uint64_t* p) {
+  uint64_t a;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
+  return a;
+}
+// two words at a 16-byte aligned address (each word is its own atomic access)
+__device__ __forceinline__ void ld_ll2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ bool ll_ok(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+__device__ __forceinline__ float ll_val(uint64_t w) { return __uint_as_float((uint32_t)w); }
 
-// Grid-wide barrier of the compute warps, with a bounded wait. After the
-// compute warps' bar.sync, thread 0 adds one to the counter with release
-// semantics (publishing the whole CTA's writes) and polls it with acquire
-// loads until it reaches `target`. A wait that outlives the limit sets
-// QTTS_DEV_TIMEOUT, and an error word set elsewhere also ends the wait.
-// Returns false to make the CTA leave the frame.
-__device__ bool grid_sync(const Globals& g, unsigned target, volatile int* sflag) {
-  cbar();
-  if (threadIdx.x == 0) {
-    red_release_gpu(g.barrier, 1u);
-    int ok = 1;
-    if (ld_acquire_gpu(g.barrier) < target) {
-      const uint64_t t0 = global_timer_ns();
-      unsigned spins = 0;
-      while (ld_acquire_gpu(g.barrier) < target) {
-        if (read_err(g.err)) {
-          ok = 0;
-          break;
-        }
-        if ((++spins & 63u) == 0u && global_timer_ns() - t0 > kBarrierTimeoutNs) {
-          set_err(g.err, QTTS_DEV_TIMEOUT);
-          ok = 0;
-          break;
-        }
+// Re-read the word at p until it carries `tag` and return it; after the time
+// limit (sets QTTS_DEV_TIMEOUT) or once an error is set elsewhere, return 0
+// (no frame's tag is 0).
+__device__ __noinline__ uint64_t ll_wait(const uint64_t* p, uint32_t tag, int* err) {
+  const uint64_t t0 = global_timer_ns();
+  unsigned spins = 0;
+  for (;;) {
+    const uint64_t w = ld_ll(p);
+    if (ll_ok(w, tag)) return w;
+    if ((++spins & 15u) == 0u) {
+      if (read_err(err) || global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (!read_err(err)) set_err(err, QTTS_DEV_TIMEOUT);
+        return 0;
       }
     }
-    *sflag = ok;
   }
-  cbar();
-  return *sflag != 0;
+}
+// w: the first read of the word at p; true once it carries `tag`
+__device__ __forceinline__ bool ll_get(const uint64_t* p, uint32_t tag, uint64_t& w, int* err) {
+  if (ll_ok(w, tag)) return true;
+  w = ll_wait(p, tag, err);
+  return ll_ok(w, tag);
+}
+
+// Wait until both words of every pair ps[u] (u < N, ps[u] != nullptr) carry
+// tag t[u]; w holds the first reads. Every pass re-reads all pairs still
+// pending at once, so a late batch costs one round trip per pass, not one per
+// word. False after the time limit or once an error is set elsewhere.
+template <int N>
+__device__ __forceinline__ bool ll_settle(const uint64_t* const (&ps)[N], const uint32_t (&t)[N],
+                                          uint64_t (&w)[N][2], int* err) {
+  bool all = true;
+#pragma unroll
+  for (int u = 0; u < N; ++u)
+    if (ps[u]) all &= ll_ok(w[u][0], t[u]) & ll_ok(w[u][1], t[u]);
+  if (all) return true;
+  const uint64_t t0 = global_timer_ns();
+  unsigned spins = 0;
+  for (;;) {
+    all = true;
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+      if (ps[u] && !(ll_ok(w[u][0], t[u]) & ll_ok(w[u][1], t[u]))) {
+        ld_ll2(ps[u], w[u][0], w[u][1]);
+        all = false;
+      }
+    if (all) return true;
+    if ((++spins & 15u) == 0u && (read_err(err) || global_timer_ns() - t0 > kWaitTimeoutNs)) {
+      if (!read_err(err)) set_err(err, QTTS_DEV_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // deterministic sum over the compute threads (fixed combination order)
@@ -140,20 +183,23 @@ __device__ float block_sum(float v, float* red) {
   return red[kCWarps];
 }
 
-// Stage trace: with tracing on, thread 0 of the first and the last CTA
-// stamps %globaltimer at up to 8 points of every stage (0 start, 1 after the
-// GEMV prologue, 2 after its phase 1, 3 after its phase 2, 7 end).
+// Stage trace: with tracing on, thread 0 of the traced CTAs (the first and
+// the last, or all) stamps %globaltimer at up to 8 points of every stage (0
+// start, 1 after the GEMV prologue, 2 after its phase 1, 3 after its phase 2,
+// 4/5 around the first task's ring wait, 6 after its dot products, 7 end);
+// CTA 0 also stamps its weight-ring slot uses (issue, ready).
 constexpr int kTraceMarks = 8;
-constexpr int kTraceRing = 4096;  // ring uses traced per frame: issue and ready times on CTA 0
+constexpr int kTraceRing = 4096;
 __shared__ int g_trace_stage;
 __device__ __forceinline__ void trace_ring(const Globals& g, uint32_t q, int which) {
   if (g.trace && blockIdx.x == 0 && q < (uint32_t)kTraceRing)
-    g.trace[(size_t)2 * g.n_stages * kTraceMarks + (size_t)q * 2 + which] = global_timer_ns();
+    g.trace[(size_t)g.trace_ctas * g.n_stages * kTraceMarks + (size_t)q * 2 + which] = global_timer_ns();
 }
 __device__ __forceinline__ void trace_mark(const Globals& g, int which) {
-  if (g.trace && threadIdx.x == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1)) {
-    const int slot = blockIdx.x == 0 ? 0 : 1;
-    g.trace[((size_t)slot * g.n_stages + g_trace_stage) * kTraceMarks + which] = global_timer_ns();
+  if (g.trace && threadIdx.x == 0) {
+    int slot = (int)blockIdx.x;
+    if (g.trace_ctas == 2) slot = blockIdx.x == 0 ? 0 : blockIdx.x == gridDim.x - 1 ? 1 : -1;
+    if (slot >= 0) g.trace[((size_t)slot * g.n_stages + g_trace_stage) * kTraceMarks + which] = global_timer_ns();
   }
 }
 
@@ -202,19 +248,30 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for phase `parity` of `bar` to complete, at most kBarrierTimeoutNs; an
+// The same test, but a thread that finds the phase incomplete is suspended
+// until it completes or about `ns` nanoseconds pass: no issue slots are spent
+// spinning (the producer warp shares its SM sub-partition with compute warps).
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSuspendNs = 20000;  // recheck the error word and the time limit this often
+
+// Wait for phase `parity` of `bar` to complete, at most kWaitTimeoutNs; an
 // error word set elsewhere ends the wait too.
 __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  unsigned spins = 0;
-  while (!mbar_test(bar, parity)) {
-    if ((++spins & 15u) == 0u) {
-      if (read_err(err)) return false;
-      if (global_timer_ns() - t0 > kBarrierTimeoutNs) {
-        set_err(err, QTTS_DEV_TIMEOUT);
-        return false;
-      }
+  while (!mbar_test_sleep(bar, parity, kSuspendNs)) {
+    if (read_err(err)) return false;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      set_err(err, QTTS_DEV_TIMEOUT);
+      return false;
     }
   }
   return true;
@@ -377,7 +434,8 @@ struct SampleSmem {
   int sel_rem;
 };
 
-__device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, int j, const qtts_session& ss,
+// `row`: the raw logits, or nullptr when they are already in S.lp
+__device__ int sample_row(SampleSmem& S, const float* row, int V, int j, const qtts_session& ss,
                           uint32_t key0, uint32_t key1, uint32_t fctr, const uint32_t* seen, int eos_id,
                           int n_codes) {
   const int tid = threadIdx.x, lane = tid & 31;
@@ -391,7 +449,7 @@ __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, i
     k = ss.cp_top_k;
   }
   for (int v = tid; v < V; v += kCThreads) {
-    float l = row_cg ? __ldcg(row + v) : row[v];
+    float l = row ? row[v] : S.lp[v];
     if (j == 0) {
       if (v >= n_codes && v != eos_id) l = -INFINITY;
       if (v == eos_id && !ss.eos_allowed) l = -INFINITY;
@@ -521,23 +579,25 @@ __device__ int sample_row(SampleSmem& S, const float* row, bool row_cg, int V, i
 
 // ---------------------------------------------------------------------------
 // stage: begin -- validate every session (each CTA reaches the same verdict
-// from the same data, so no CTA waits on a barrier the others skipped), reset
-// the attention counters, load the Talker inputs
+// from the same data, so on bad input all CTAs leave together) and publish
+// the Talker input rows
 // ---------------------------------------------------------------------------
 
-__device__ bool stage_begin(const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+__shared__ int s_kv_len[kMaxBatch];  // each session's kv_len as this launch found it
+
+__device__ bool stage_begin(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa) {
   const int tid = threadIdx.x;
   int bad = 0;
   for (int b = tid; b < fa.B; b += kCThreads) {
     const qtts_session s = fa.sess[b];
-    const int kv = s.kv_len;
+    const int kv = s_kv_len[b];
     if (kv < 0 || kv + 1 > g.max_context || kv + 1 > fa.bt_stride * kPage) bad = QTTS_DEV_BAD_SESSION;
     if (!(s.temperature >= 0.f) || !isfinite(s.temperature) || !(s.cp_temperature >= 0.f) ||
         !isfinite(s.cp_temperature) || !(s.rep_penalty > 0.f) || !isfinite(s.rep_penalty))
       bad = QTTS_DEV_BAD_SAMPLING;
   }
   for (int b = 0; b < fa.B; ++b) {
-    const int kv = fa.sess[b].kv_len;
+    const int kv = s_kv_len[b];
     if (kv < 0 || kv + 1 > fa.bt_stride * kPage) continue;  // reported above
     const int np = kv / kPage + 1;
     for (int p = tid; p < np; p += kCThreads) {
@@ -554,21 +614,15 @@ __device__ bool stage_begin(const Globals& g, const FrameArgs& fa, unsigned char
   if (bad && blockIdx.x == 0) set_err(g.err, bad);
   if (cbar_or(bad)) return false;
 
-  if (blockIdx.x == 0)
-    for (int i = tid; i < kMaxBatch * g.nkv; i += kCThreads) g.attn_cnt[i] = 0;
-
-  float* red = (float*)smem;
   const int b = blockIdx.x;
-  float ss = 0.f;
   if (b < fa.B) {
-    for (int k = tid; k < g.H; k += kCThreads) {
-      const float x = bf2f(fa.in_embeds[(size_t)b * g.H + k]);
-      g.x_t[(size_t)b * g.H + k] = x;
-      ss += x * x;
+    const uint16_t* src = fa.in_embeds + (size_t)b * g.H;
+    uint64_t* dst = d.x_next + (size_t)b * g.H;
+    for (int k = tid * 2; k < g.H; k += kCThreads * 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(src + k);
+      st_ll2(dst + k, bf_lo(w), bf_hi(w), tag);
     }
   }
-  ss = block_sum(ss, red);
-  for (int r = tid; r < fa.B; r += kCThreads) g.ssq_t[(size_t)blockIdx.x * kMaxRows + r] = (r == b) ? ss : 0.f;
   return true;
 }
 
@@ -581,22 +635,24 @@ __device__ bool stage_begin(const Globals& g, const FrameArgs& fa, unsigned char
 // shared memory): the producer warp has already copied each task's weights
 // into a ring slot. Direct path (larger batches): lanes load the weights
 // themselves, once per tile of activation rows.
+// The RMSNorm of a row is x g / rms(x): every CTA reads the whole row anyway,
+// so it computes rms itself (fixed-order sums, the same on every CTA) and
+// applies 1/rms to the dot products.
 // ---------------------------------------------------------------------------
 
 constexpr int kKChunk = 1024;
 constexpr int kSub = kKChunk / 256;   // 16-byte vectors per lane per row per task
 constexpr int kPartFloats = 1536;
-constexpr int kSqFloats = 512;
+constexpr int kResidFloats = 512;
 constexpr int kRingSlots = 8;
 constexpr int kSlotBytes = 16384;     // whole weight rows, one bulk copy per slot
 static_assert(kWorkBytes + kTailBytes + kRingSlots * kSlotBytes <= kSmemBytes, "shared-memory plan");
 
 struct GemvSmemTail {
-  float rfac[8];
-  float ssq_row[kMaxRows];   // this CTA's sum of squares per stage row
-  float part[kPartFloats];   // phase-1 partial dot products [task][U][RT]
-  float sq[kSqFloats];       // phase-2 squares [unit][RT]
-  float resid[kSqFloats];    // E_RESID operands x[row][unit] [unit][RT], loaded in the prologue
+  float rfac[8];               // 1/rms of the tile's rows (1 without a norm)
+  float sqw[8][kWarps];        // per-warp sum-of-squares partials of the tile's rows
+  float part[kPartFloats];     // phase-1 partial dot products [task][U][RT]
+  float resid[kResidFloats];   // E_RESID operands x[row][unit] [unit][RT], read in the prologue
 };
 static_assert(sizeof(GemvSmemTail) <= kTailBytes, "GEMV shared-memory tail");
 
@@ -621,9 +677,10 @@ __device__ bool ring_wait_full(Ring* ring, int slot, uint32_t use, int* err) {
     const uint64_t t0 = global_timer_ns();
     unsigned spins = 0;
     while (ld_volatile_u32(&ring->seq[slot]) != use) {
+      __nanosleep(64);
       if ((++spins & 15u) == 0u) {
         if (read_err(err)) return false;
-        if (global_timer_ns() - t0 > kBarrierTimeoutNs) {
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
           set_err(err, QTTS_DEV_TIMEOUT);
           return false;
         }
@@ -652,8 +709,7 @@ __device__ __forceinline__ int ring_rt(const StageDesc& d, int B) {
   int RT = 1;
   while (RT < rows) RT *= 2;
   if (RT > 8) return 0;
-  const int need = (RT + (d.xsrc == X_NORM ? 1 : 0)) * d.K * 4;
-  if (need > kWorkBytes) return 0;
+  if (RT * d.K * 4 > kWorkBytes) return 0;
   for (int s = 0; s < d.nseg; ++s)  // a row unit must fit one slot
     if (d.seg[s].unit * d.K * (d.seg[s].scale ? 1 : 2) > kSlotBytes) return 0;
   return RT;
@@ -695,17 +751,20 @@ __device__ __forceinline__ uint16_t* talker_kv_ptr(const Globals& g, const Frame
          (((((size_t)layer * g.pool_pages + page) * 2 + kv) * g.nkv + head) * kPage + pos % kPage) * g.d;
 }
 
-// Code-Predictor cache of one layer: [session][K|V][kv head][16 positions][d]
-__device__ __forceinline__ uint16_t* cp_kv_ptr(const Globals& g, uint16_t* layer_base, int b, int pos, int kv,
-                                                int head) {
-  return layer_base + ((((size_t)b * 2 + kv) * g.nkvc + head) * kCodebooks + pos) * g.dc;
+// Code-Predictor cache of one layer, tagged words: [session][K|V][kv head]
+// [16 positions][d/2]; K word i holds dims (i, i + d/2), V word i dims
+// (2i, 2i + 1), as two bf16.
+__device__ __forceinline__ uint64_t* cp_kv_word(const Globals& g, uint64_t* layer_base, int b, int pos, int kv,
+                                                 int head) {
+  return layer_base + ((((size_t)b * 2 + kv) * g.nkvc + head) * kCodebooks + pos) * (g.dc / 2);
 }
 
 // Epilogue for one output unit (rows n0, n0+1 when U == 2) of stage row r.
-__device__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, int n0,
-                              float y0, float y1, int r, float resid, float& ssq_acc) {
+__device__ __forceinline__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, int n0,
+                              float y0, float y1, int r, float resid, uint32_t tag) {
   const int b = r / d.rps, p = r % d.rps;
   const int orow = out_row_of(sg, d.rps, r);
+  uint64_t* out = sg.out + (size_t)orow * sg.out_stride;
   switch (sg.epi) {
     case E_QKV_T:
     case E_QKV_CP: {
@@ -713,7 +772,7 @@ __device__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& 
       const int hd = talker ? g.d : g.dc;
       const int nq = talker ? g.nq : g.nqc;
       const int nkv = talker ? g.nkv : g.nkvc;
-      const int pos = talker ? fa.sess[b].kv_len : d.pos_base + p;
+      const int pos = talker ? s_kv_len[b] : d.pos_base + p;
       const int half = hd / 2;
       if (n0 < (nq + nkv) * hd) {
         // rows arrive as rotate-half pairs (i, i + hd/2) of one head
@@ -725,47 +784,52 @@ __device__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& 
         const float o0 = y0 * c - y1 * s;
         const float o1 = y1 * c + y0 * s;
         if (is_q) {
-          float* q = sg.out + (size_t)orow * sg.out_stride + head * hd;
-          q[i] = o0;
-          q[i + half] = o1;
+          st_ll(out + head * hd + i, o0, tag);
+          st_ll(out + head * hd + i + half, o1, tag);
+        } else if (talker) {
+          const uint16_t k0 = f2bf(o0), k1 = f2bf(o1);
+          uint16_t* kp = talker_kv_ptr(g, fa, d.layer, b, pos, 0, head);
+          kp[i] = k0;
+          kp[i + half] = k1;
+          uint64_t* kc = d.kvcur + (((size_t)b * 2 + 0) * nkv + head) * hd;
+          st_ll(kc + i, bf2f(k0), tag);
+          st_ll(kc + i + half, bf2f(k1), tag);
         } else {
-          uint16_t* kp =
-              talker ? talker_kv_ptr(g, fa, d.layer, b, pos, 0, head) : cp_kv_ptr(g, d.cp_kv, b, pos, 0, head);
-          kp[i] = f2bf(o0);
-          kp[i + half] = f2bf(o1);
+          st_ll_raw(cp_kv_word(g, d.cp_kv, b, pos, 0, head) + i, (uint32_t)f2bf(o0) | ((uint32_t)f2bf(o1) << 16),
+                    fa.tag0);
         }
       } else {
         const int rel = n0 - (nq + nkv) * hd;
         const int head = rel / hd, e = rel % hd;
-        uint16_t* vp =
-            talker ? talker_kv_ptr(g, fa, d.layer, b, pos, 1, head) : cp_kv_ptr(g, d.cp_kv, b, pos, 1, head);
-        vp[e] = f2bf(y0);
-        vp[e + 1] = f2bf(y1);
+        const uint16_t v0 = f2bf(y0), v1 = f2bf(y1);
+        if (talker) {
+          uint16_t* vp = talker_kv_ptr(g, fa, d.layer, b, pos, 1, head);
+          vp[e] = v0;
+          vp[e + 1] = v1;
+          st_ll2(d.kvcur + (((size_t)b * 2 + 1) * nkv + head) * hd + e, bf2f(v0), bf2f(v1), tag);
+        } else {
+          st_ll_raw(cp_kv_word(g, d.cp_kv, b, pos, 1, head) + e / 2, (uint32_t)v0 | ((uint32_t)v1 << 16), fa.tag0);
+        }
       }
       break;
     }
-    case E_RESID: {  // `resid`: x[orow][n0], loaded in the prologue
-      float* x = sg.out + (size_t)orow * sg.out_stride + n0;
-      const float v = resid + y0;
-      *x = v;
-      ssq_acc += v * v;
+    case E_RESID:  // `resid`: the residual x[orow][n0], read in the prologue
+      st_ll(out + n0, resid + y0, tag);
       break;
-    }
     case E_SWIGLU: {
       const float silu = y0 / (1.0f + expf(-y0));
-      sg.out[(size_t)orow * sg.out_stride + n0 / 2] = silu * y1;
+      st_ll(out + n0 / 2, silu * y1, tag);
       break;
     }
-    case E_LOGITS: {
-      sg.out[(size_t)orow * sg.out_stride + n0] = y0;
+    case E_LOGITS:
+      st_ll(out + n0, y0, tag);
+      if (n0 + 1 == sg.N && (sg.N & 1)) st_ll(out + n0 + 1, 0.f, tag);  // pad word: rows are read in pairs
       if (fa.logits_out) fa.logits_out[((size_t)b * kCodebooks + d.codebook) * g.V0 + n0] = y0;
       break;
-    }
     case E_CPIN: {
       float v = y0;
       if (sg.bias) v += bf2f(sg.bias[n0]);
-      sg.out[(size_t)orow * sg.out_stride + n0] = v;
-      ssq_acc += v * v;
+      st_ll(out + n0, v, tag);
       break;
     }
   }
@@ -834,229 +898,263 @@ __device__ __forceinline__ void task_fma(const typename Raw8<WT>::T (&raw)[kSub]
   }
 }
 
-// This CTA's share of one segment for stage rows [r0, r0 + nr): phase 1
-// spreads (unit, K-slice) tasks over the compute warps and leaves one partial
-// per task in shared memory; phase 2 gives each (unit, row) to one thread,
-// which sums the partials in K order and runs the epilogue. With `ring`,
-// task t's weights are in the ring slot of sequence index q + t.
+// This CTA's share of one segment for stage rows [r0, r0 + nr), in two
+// phases. Phase 1 spreads (unit, K-slice) tasks over the compute warps and
+// leaves one partial per task in shared memory (ring path: task t's weights
+// are in the ring slot of sequence index q + t / tasks per slot; direct path:
+// lanes load them). Phase 2 gives each (unit, row) to one thread, which sums
+// the partials in K order, scales by 1/rms and runs the epilogue. Each phase
+// is its own small function, so the code a stage runs stays in the
+// instruction cache from one layer to the next.
 template <typename WT, int U, int RT>
-__device__ void gemv_seg(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, const float* xs,
-                         int r0, int nr, GemvSmemTail* tail, unsigned char* smem, Ring* ring, uint32_t q,
-                         const StageDesc* next, StageDesc* next_s) {
+__device__ void gemv_p1_ring(const Seg& sg, int K, const Globals& g, const float* xs, int nr,
+                                          GemvSmemTail* tail, unsigned char* smem, Ring* ring, uint32_t q) {
   using R = Raw8<WT>;
-  const int K = d.K;
+  const SegShare sh(sg, K);
+  const int ntask = sh.nu * sh.nkc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t nsl = (uint32_t)g.ring_slots;
+  // tasks go round-robin over the warps; the warp that finishes a slot's
+  // last task frees the slot
+  for (int t = warp; t < ntask; t += kCWarps) {
+    const int ul = t / sh.nkc, kc = t - ul * sh.nkc;
+    const int sl = ul / sh.upslot;
+    const int ua = sl * sh.upslot;
+    const int slot_tasks = (min(sh.nu, ua + sh.upslot) - ua) * sh.nkc;
+    const uint32_t qq = q + (uint32_t)sl;
+    const int slot = (int)(qq % nsl);
+    // a failed wait (time limit or an error elsewhere) leaves zeros and the
+    // warp carries on to every CTA barrier; the frame is abandoned after
+    // the stage
+    if (t == 0) trace_mark(g, 4);
+    const bool got = ring_wait_full(ring, slot, qq / nsl, g.err);
+    if (t == 0) trace_mark(g, 5);
+    if (lane == 0 && kc == 0 && ul == ua) trace_ring(g, qq, 1);
+    const WT* rowp = (const WT*)ring_slot(smem, slot) + (size_t)(ul - ua) * U * K;
+    const int kb = kc * kKChunk + lane * 8;
+    typename R::T raw[kSub][U];
+#pragma unroll
+    for (int sb = 0; sb < kSub; ++sb)
+#pragma unroll
+      for (int i = 0; i < U; ++i)
+        raw[sb][i] = (got && kb + sb * 256 < K) ? R::lds(rowp + (size_t)i * K + kb + sb * 256) : typename R::T{};
+    float acc[U][RT];
+    task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
+    __syncwarp();
+    if (t == 0) trace_mark(g, 6);
+    if (lane == 0 && got) {
+      if (atomicAdd(&ring->done[slot], 1u) + 1u == (uint32_t)slot_tasks) {
+        ring->done[slot] = 0u;
+        mbar_arrive(&ring->empty[slot]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i)
+#pragma unroll
+      for (int r = 0; r < RT; ++r) {
+        const float v = warp_sum(acc[i][r]);
+        if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
+      }
+  }
+}
+
+template <typename WT, int U, int RT>
+__device__ void gemv_p1_direct(const Seg& sg, int K, const float* xs, int nr, GemvSmemTail* tail) {
+  using R = Raw8<WT>;
   const SegShare sh(sg, K);
   const int ntask = sh.nu * sh.nkc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WT* W = (const WT*)sg.w;
-  if (ring) {
-    // tasks go round-robin over the warps; the warp that finishes a slot's
-    // last task frees the slot
-    for (int t = warp; t < ntask; t += kCWarps) {
-      const int ul = t / sh.nkc, kc = t - ul * sh.nkc;
-      const int sl = ul / sh.upslot;
-      const int ua = sl * sh.upslot;
-      const int slot_tasks = (min(sh.nu, ua + sh.upslot) - ua) * sh.nkc;
-      const uint32_t qq = q + (uint32_t)sl;
-      const uint32_t nsl = (uint32_t)g.ring_slots;
-      const int slot = (int)(qq % nsl);
-      // a failed wait (time limit or an error elsewhere) leaves zeros and the
-      // warp carries on to every barrier; the frame is abandoned at the next
-      // grid barrier
-      const bool got = ring_wait_full(ring, slot, qq / nsl, g.err);
-      if (lane == 0 && kc == 0 && ul == ua) trace_ring(g, qq, 1);
-      const WT* rowp = (const WT*)ring_slot(smem, slot) + (size_t)(ul - ua) * U * K;
-      const int kb = kc * kKChunk + lane * 8;
-      typename R::T raw[kSub][U];
+  for (int t = warp; t < ntask; t += kCWarps) {
+    const int ul = t / sh.nkc, kc = t - ul * sh.nkc;
+    const int n0 = (sh.u0 + ul) * U;
+    const int kb = kc * kKChunk + lane * 8;
+    typename R::T raw[kSub][U];
 #pragma unroll
-      for (int sb = 0; sb < kSub; ++sb)
+    for (int sb = 0; sb < kSub; ++sb) {
+      const int k = kb + sb * 256;
 #pragma unroll
-        for (int i = 0; i < U; ++i)
-          raw[sb][i] = (got && kb + sb * 256 < K) ? R::lds(rowp + (size_t)i * K + kb + sb * 256) : typename R::T{};
-      float acc[U][RT];
-      task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
-      __syncwarp();
-      if (lane == 0 && got) {
-        if (atomicAdd(&ring->done[slot], 1u) + 1u == (uint32_t)slot_tasks) {
-          ring->done[slot] = 0u;
-          mbar_arrive(&ring->empty[slot]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < U; ++i)
-#pragma unroll
-        for (int r = 0; r < RT; ++r) {
-          const float v = warp_sum(acc[i][r]);
-          if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
-        }
+      for (int i = 0; i < U; ++i) raw[sb][i] = (k < K) ? R::load(W + (size_t)(n0 + i) * K + k) : typename R::T{};
     }
-  } else {
-    for (int t = warp; t < ntask; t += kCWarps) {
-      const int ul = t / sh.nkc, kc = t - ul * sh.nkc;
-      const int n0 = (sh.u0 + ul) * U;
-      const int kb = kc * kKChunk + lane * 8;
-      typename R::T raw[kSub][U];
+    float acc[U][RT];
+    task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
 #pragma unroll
-      for (int sb = 0; sb < kSub; ++sb) {
-        const int k = kb + sb * 256;
+    for (int i = 0; i < U; ++i)
 #pragma unroll
-        for (int i = 0; i < U; ++i) raw[sb][i] = (k < K) ? R::load(W + (size_t)(n0 + i) * K + k) : typename R::T{};
+      for (int r = 0; r < RT; ++r) {
+        const float v = warp_sum(acc[i][r]);
+        if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
       }
-      float acc[U][RT];
-      task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
-#pragma unroll
-      for (int i = 0; i < U; ++i)
-#pragma unroll
-        for (int r = 0; r < RT; ++r) {
-          const float v = warp_sum(acc[i][r]);
-          if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
-        }
-    }
   }
-  cbar();
-  trace_mark(g, 2);
-  if (next && (threadIdx.x >> 5) == kCWarps - 1) fetch_desc(next, next_s);
+}
+
+__device__ void gemv_p2(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa,
+                                     int r0, int nr, int RT, GemvSmemTail* tail, uint32_t tag) {
+  const int U = sg.unit;
+  const SegShare sh(sg, d.K);
   for (int idx = threadIdx.x; idx < sh.nu * nr; idx += kCThreads) {
     const int ul = idx / nr, r = idx - ul * nr;
     const int n0 = (sh.u0 + ul) * U;
-    float y[U];
-#pragma unroll
+    const float f = tail->rfac[r];
+    float y[2] = {0.f, 0.f};
     for (int i = 0; i < U; ++i) {
       float acc = 0.f;
       for (int kc = 0; kc < sh.nkc; ++kc) acc += tail->part[((ul * sh.nkc + kc) * U + i) * RT + r];
+      acc *= f;
       y[i] = sg.scale ? acc * sg.scale[n0 + i] : acc;
     }
-    float sqv = 0.f;
-    gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + r, tail->resid[ul * RT + r], sqv);
-    tail->sq[ul * RT + r] = sqv;
+    gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + r, tail->resid[ul * RT + r], tag);
   }
-  cbar();
-  trace_mark(g, 3);
-  if (sg.ssq_out)
-    for (int r = threadIdx.x; r < nr; r += kCThreads) {
-      float acc = 0.f;
-      for (int ul = 0; ul < sh.nu; ++ul) acc += tail->sq[ul * RT + r];
-      tail->ssq_row[r0 + r] += acc;
-    }
-  cbar();
 }
 
-template <typename WT, int U>
-__device__ void gemv_seg_rt(int RT, const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa,
-                            const float* xs, int r0, int nr, GemvSmemTail* tail, unsigned char* smem, Ring* ring,
-                            uint32_t q, const StageDesc* next, StageDesc* next_s) {
-  switch (RT) {
-    case 1: gemv_seg<WT, U, 1>(d, sg, g, fa, xs, r0, nr, tail, smem, ring, q, next, next_s); break;
-    case 2: gemv_seg<WT, U, 2>(d, sg, g, fa, xs, r0, nr, tail, smem, ring, q, next, next_s); break;
-    case 4: gemv_seg<WT, U, 4>(d, sg, g, fa, xs, r0, nr, tail, smem, ring, q, next, next_s); break;
-    default: gemv_seg<WT, U, 8>(d, sg, g, fa, xs, r0, nr, tail, smem, ring, q, next, next_s); break;
+// Phase 1 of one segment: the variant for the weight type, unit and tile height.
+__device__ void gemv_p1(const Seg& sg, int K, int RT, bool use_ring, const Globals& g, const float* xs, int nr,
+                        GemvSmemTail* tail, unsigned char* smem, Ring* ring, uint32_t q) {
+#define QTTS_P1(WT_, U_, RT_)                                                        \
+  if (use_ring) gemv_p1_ring<WT_, U_, RT_>(sg, K, g, xs, nr, tail, smem, ring, q); \
+  else gemv_p1_direct<WT_, U_, RT_>(sg, K, xs, nr, tail);                          \
+  return;
+#define QTTS_P1_RT(WT_, U_)       \
+  switch (RT) {                   \
+    case 1: QTTS_P1(WT_, U_, 1)   \
+    case 2: QTTS_P1(WT_, U_, 2)   \
+    case 4: QTTS_P1(WT_, U_, 4)   \
+    default: QTTS_P1(WT_, U_, 8)  \
   }
+  if (sg.scale) {
+    if (sg.unit == 2) { QTTS_P1_RT(int8_t, 2) }
+    else { QTTS_P1_RT(int8_t, 1) }
+  } else {
+    if (sg.unit == 2) { QTTS_P1_RT(uint16_t, 2) }
+    else { QTTS_P1_RT(uint16_t, 1) }
+  }
+#undef QTTS_P1_RT
+#undef QTTS_P1
 }
 
 // q: this CTA's count of ring tasks consumed so far (advanced here).
 // next / next_s: the following stage's descriptor (or nullptr) and its
 // shared-memory buffer, filled by the last compute warp during phase 2.
-__device__ void stage_gemv(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem, Ring* ring,
-                           uint32_t& q, const StageDesc* next, StageDesc* next_s) {
+__device__ bool stage_gemv(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+                           unsigned char* smem, Ring* ring, uint32_t& q, const StageDesc* next, StageDesc* next_s) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rows = fa.B * d.rps;
   const int K = d.K;
   const bool norm = d.xsrc == X_NORM;
   float* xs = (float*)smem;
   GemvSmemTail* tail = (GemvSmemTail*)(smem + kWorkBytes);
-  for (int i = tid; i < kMaxRows; i += kCThreads) tail->ssq_row[i] = 0.f;
 
   int RT = ring_rt(d, fa.B);
   const bool use_ring = RT > 0;
   if (!use_ring) {
-    // activation rows per tile; a norm stage keeps one more row's worth for the gains
-    RT = kWorkBytes / (K * 4) - (norm ? 1 : 0);
+    RT = kWorkBytes / (K * 4);
     RT = RT >= 8 ? 8 : RT >= 4 ? 4 : RT >= 2 ? 2 : 1;
     while (RT > 1 && RT / 2 >= rows) RT /= 2;
   }
-  float* gs = xs + RT * K;
   const RowMap rm{d.rps, d.in_rps, d.in_off};
+  const Seg& s0 = d.seg[0];
+  const bool has_resid = s0.epi == E_RESID;  // single-segment stage
+  const SegShare sh0(s0, K);
 
   for (int r0 = 0; r0 < rows; r0 += RT) {
     const int nr = min(RT, rows - r0);
     cbar();
-    // issue the sum-of-squares loads, the activation loads and the gain loads
-    // together: one L2 round trip for the whole prologue
-    float ssq_part = 0.f;
-    if (norm && warp < nr) {
-      const int ir = rm.in_row(r0 + warp);
-      float v[kMaxGrid / 32];
+    // (1) the tile's input words and this CTA's residual operands: every
+    //     load is issued before the first wait, one round trip for the lot
+    bool ok = true;
+    const int nres = has_resid ? sh0.nu * nr : 0;  // <= kResidFloats <= 2 * kCThreads
+    uint64_t rw[2] = {0, 0};
+    const uint64_t* rp[2] = {nullptr, nullptr};
 #pragma unroll
-      for (int i = 0; i < kMaxGrid / 32; ++i) {
-        const int c = lane + 32 * i;
-        v[i] = c < g.G ? __ldcg(d.ssq + (size_t)c * kMaxRows + ir) : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < kMaxGrid / 32; ++i) ssq_part += v[i];
-    }
-    for (int idx = tid * 4; idx < nr * K; idx += kCThreads * 4) {
-      const int r = idx / K, k = idx - r * K;
-      const int ir = rm.in_row(r0 + r);
-      *reinterpret_cast<float4*>(xs + r * K + k) =
-          __ldcg(reinterpret_cast<const float4*>(d.x + (size_t)ir * d.x_stride + k));
-    }
-    if (d.seg[0].epi == E_RESID) {  // single-segment stage: residual operands of its epilogue
-      const Seg& sg = d.seg[0];
-      const SegShare sh(sg, K);
-      for (int idx = tid; idx < sh.nu * nr; idx += kCThreads) {
+    for (int u = 0; u < 2; ++u) {
+      const int idx = tid + u * kCThreads;
+      if (idx < nres) {
         const int ul = idx / nr, r = idx - ul * nr;
-        tail->resid[ul * RT + r] =
-            __ldcg(sg.out + (size_t)out_row_of(sg, d.rps, r0 + r) * sg.out_stride + (sh.u0 + ul) * sg.unit);
+        rp[u] = s0.resid + (size_t)out_row_of(s0, d.rps, r0 + r) * s0.out_stride + (sh0.u0 + ul) * s0.unit;
+        rw[u] = ld_ll(rp[u]);
       }
     }
-    if (norm) {
-      if (r0 == 0)
-        for (int k = tid * 4; k < K; k += kCThreads * 4) {
-          const uint2 gw = *reinterpret_cast<const uint2*>(d.gain + k);
-          *reinterpret_cast<float4*>(gs + k) = make_float4(bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y));
+    {
+      constexpr int NB = 4;
+      const int npair = nr * K / 2;
+      for (int base = tid; base < npair; base += kCThreads * NB) {
+        uint64_t w[NB][2];
+        const uint64_t* ps[NB];
+        uint32_t tg[NB];
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          const int i = base + u * kCThreads;
+          ps[u] = nullptr;
+          tg[u] = 0;
+          w[u][0] = w[u][1] = 0;
+          if (i < npair) {
+            const int e = 2 * i, r = e / K, k = e - r * K;
+            ps[u] = d.x + (size_t)rm.in_row(r0 + r) * d.x_stride + k;
+            tg[u] = fa.tag0 + (uint32_t)d.x_ws[(r0 + r) % d.rps];
+            ld_ll2(ps[u], w[u][0], w[u][1]);
+          }
         }
-      if (warp < nr) {
-        const float sum = warp_sum(ssq_part);
-        if (lane == 0) tail->rfac[warp] = 1.0f / sqrtf(sum / (float)K + g.eps);
+        ok &= ll_settle<NB>(ps, tg, w, g.err);
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          const int i = base + u * kCThreads;
+          if (i < npair) *reinterpret_cast<float2*>(xs + 2 * i) = make_float2(ll_val(w[u][0]), ll_val(w[u][1]));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int idx = tid + u * kCThreads;
+      if (idx < nres) {
+        const int ul = idx / nr, r = idx - ul * nr;
+        ok &= ll_get(rp[u], fa.tag0 + (uint32_t)s0.r_ws[(r0 + r) % d.rps], rw[u], g.err);
+        tail->resid[ul * RT + r] = ll_val(rw[u]);
+      }
+    }
+    if (cbar_or(!ok)) return false;
+    // (2) RMSNorm: x <- g x in place, per-warp sums of squares of each row
+    if (norm) {
+      for (int r = 0; r < nr; ++r) {
+        float sq = 0.f;
+        for (int k = tid * 2; k < K; k += kCThreads * 2) {
+          float2 v = *reinterpret_cast<float2*>(xs + r * K + k);
+          sq = fmaf(v.x, v.x, sq);
+          sq = fmaf(v.y, v.y, sq);
+          const uint32_t gw = __ldg(reinterpret_cast<const unsigned*>(d.gain + k));
+          v.x *= bf_lo(gw);
+          v.y *= bf_hi(gw);
+          *reinterpret_cast<float2*>(xs + r * K + k) = v;
+        }
+        sq = warp_sum(sq);
+        if (lane == 0) tail->sqw[r][warp] = sq;
       }
       cbar();
-      for (int idx = tid * 4; idx < nr * K; idx += kCThreads * 4) {
-        const int r = idx / K, k = idx - r * K;
-        const float f = tail->rfac[r];
-        float4 v = *reinterpret_cast<float4*>(xs + r * K + k);
-        const float4 gg = *reinterpret_cast<const float4*>(gs + k);
-        v.x = v.x * f * gg.x;
-        v.y = v.y * f * gg.y;
-        v.z = v.z * f * gg.z;
-        v.w = v.w * f * gg.w;
-        *reinterpret_cast<float4*>(xs + r * K + k) = v;
-      }
     }
-    cbar();
     trace_mark(g, 1);
+    // 1/rms per row, ready for phase 2 (after the phase-1 barrier)
+    if (tid < nr) {
+      float f = 1.0f;
+      if (norm) {
+        float sum = 0.f;
+        for (int w2 = 0; w2 < kCWarps; ++w2) sum += tail->sqw[tid][w2];
+        f = 1.0f / sqrtf(sum / (float)K + g.eps);
+      }
+      tail->rfac[tid] = f;
+    }
     for (int s = 0; s < d.nseg; ++s) {
       const Seg& sg = d.seg[s];
-      Ring* rg = use_ring ? ring : nullptr;
+      gemv_p1(sg, K, RT, use_ring, g, xs, nr, tail, smem, ring, q);
+      cbar();
+      trace_mark(g, 2);
       // the next descriptor is fetched once, in the last segment of the last row tile
-      const bool last = s == d.nseg - 1 && r0 + RT >= rows;
-      const StageDesc* nx = last ? next : nullptr;
-      if (sg.scale) {
-        if (sg.unit == 2) gemv_seg_rt<int8_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail, smem, rg, q, nx, next_s);
-        else gemv_seg_rt<int8_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail, smem, rg, q, nx, next_s);
-      } else {
-        if (sg.unit == 2) gemv_seg_rt<uint16_t, 2>(RT, d, sg, g, fa, xs, r0, nr, tail, smem, rg, q, nx, next_s);
-        else gemv_seg_rt<uint16_t, 1>(RT, d, sg, g, fa, xs, r0, nr, tail, smem, rg, q, nx, next_s);
-      }
+      if (next && s == d.nseg - 1 && r0 + RT >= rows && warp == kCWarps - 1) fetch_desc(next, next_s);
+      gemv_p2(d, sg, g, fa, r0, nr, RT, tail, tag);
+      cbar();
+      trace_mark(g, 3);
       if (use_ring) q += (uint32_t)SegShare(sg, K).nslot;
     }
   }
-  for (int s = 0; s < d.nseg; ++s) {
-    const Seg& sg = d.seg[s];
-    if (sg.epi == E_QKV_T || sg.epi == E_QKV_CP) fence_proxy_async_global();  // K/V are read by bulk copies next
-    if (!sg.ssq_out) continue;
-    for (int r = tid; r < rows; r += kCThreads)
-      sg.ssq_out[(size_t)blockIdx.x * kMaxRows + out_row_of(sg, d.rps, r)] = tail->ssq_row[r];
-  }
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -1102,16 +1200,19 @@ __device__ void producer(const StageDesc* prog, int s0, int s1, const Globals& g
   for (uint32_t qq = first; qq < q; ++qq) {
     if (!mbar_test(&ring->full[qq % nsl], (qq / nsl) & 1u)) {
       const uint64_t t0 = global_timer_ns();
-      while (!mbar_test(&ring->full[qq % nsl], (qq / nsl) & 1u))
-        if (global_timer_ns() - t0 > kBarrierTimeoutNs) break;
+      while (!mbar_test_sleep(&ring->full[qq % nsl], (qq / nsl) & 1u, kSuspendNs))
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// attention: one warp per (row, kv head[, split]); the split's 16-position
-// tiles of K and V (one head of one page: 2 x 4 KB contiguous) arrive in
-// shared memory by TMA bulk copy; online softmax over the tiles
+// attention. Talker: one warp per (session, kv head, split); the split's
+// 16-position tiles of K and V (one head of one page: 2 x 4 KB contiguous)
+// arrive in shared memory by TMA bulk copy, the newest position (written this
+// frame) from the tagged K/V rows; online softmax over the tiles.
+// Code Predictor: five warps per (row, kv head), all positions from the
+// tagged cache in one round trip.
 // ---------------------------------------------------------------------------
 
 constexpr int kAttnMaxHD = 128;
@@ -1124,8 +1225,11 @@ struct AttnTile {
   uint64_t bar;
   uint64_t pad;
 };
-constexpr int kAttnWarps = 8;  // warps per CTA that run attention items
+constexpr int kAttnWarps = 8;  // warps per CTA that run Talker attention items
 static_assert(kAttnWarps * sizeof(AttnTile) <= kWorkBytes, "attention tiles");
+constexpr int kCpGroupWarps = 5;                      // warps per Code-Predictor attention item
+constexpr int kCpGroups = kCWarps / kCpGroupWarps;    // items in flight per CTA
+static_assert(kCpGroups >= 1 && kCpGroups * kCpGroupWarps <= kCWarps, "Code-Predictor attention groups");
 
 template <int HD, int GRP>
 struct AttnAcc {
@@ -1206,9 +1310,13 @@ __device__ void attn_tile(const AttnTile& T, int nvalid, float scale, AttnAcc<HD
 }
 
 // One 16-position tile by bulk copy (K then V of one head), then fold it in.
+// cur_row >= 0: row cur_row of the tile is the position this frame appends;
+// its K and V come from the tagged words (kw, vw: this lane's word pairs
+// 2(lane + 32u), +1), not from the cache.
 template <int HD, int GRP>
 __device__ bool attn_fetch_fold(AttnTile& T, const uint16_t* ksrc, const uint16_t* vsrc, int nvalid, float scale,
-                                uint32_t& parity, int* err, AttnAcc<HD, GRP>& A) {
+                                uint32_t& parity, int* err, AttnAcc<HD, GRP>& A, int cur_row,
+                                const uint64_t (&kw)[HD / 64][2], const uint64_t (&vw)[HD / 64][2]) {
   const int lane = threadIdx.x & 31;
   constexpr uint32_t bytes = kPage * HD * sizeof(uint16_t);
   __syncwarp();
@@ -1221,17 +1329,33 @@ __device__ bool attn_fetch_fold(AttnTile& T, const uint16_t* ksrc, const uint16_
   }
   const bool ok = mbar_wait(&T.bar, parity, err);
   parity ^= 1u;
-  if (ok) attn_tile<HD, GRP>(T, nvalid, scale, A);
+  if (ok) {
+    if (cur_row >= 0) {
+#pragma unroll
+      for (int u = 0; u < HD / 64; ++u) {
+        const int c = 2 * (lane + 32 * u);
+        const uint32_t kk = (uint32_t)f2bf(ll_val(kw[u][0])) | ((uint32_t)f2bf(ll_val(kw[u][1])) << 16);
+        const uint32_t vv = (uint32_t)f2bf(ll_val(vw[u][0])) | ((uint32_t)f2bf(ll_val(vw[u][1])) << 16);
+        *reinterpret_cast<uint32_t*>(T.k + cur_row * HD + c) = kk;
+        *reinterpret_cast<uint32_t*>(T.v + cur_row * HD + c) = vv;
+      }
+      __syncwarp();
+    }
+    attn_tile<HD, GRP>(T, nvalid, scale, A);
+  }
   return ok;
 }
 
 template <int HD, int GRP>
-__device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+__device__ bool stage_attn_talker(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+                                  unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int E = HD / 32;
+  constexpr int NQ = GRP * HD / 64;  // q word pairs per lane
+  constexpr int NC = HD / 64;        // current K (and V) word pairs per lane
   const int nkv = g.nkv;
   const int qstride = d.q_stride;
-  if (warp >= kAttnWarps) return;
+  if (warp >= kAttnWarps) return true;
   AttnTile& T = reinterpret_cast<AttnTile*>(smem)[warp];
   if (lane == 0) {
     mbar_init(&T.bar, 1);
@@ -1239,9 +1363,11 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
   }
   __syncwarp();
   uint32_t parity = 0;
+  bool ok = true;
+  const uint32_t tag_in = fa.tag0 + (uint32_t)d.q_ws;
   // split plan, identical on every CTA (same inputs, same arithmetic): about
   // one page-aligned split per warp of the grid
-  const int len = lane < fa.B ? fa.sess[lane].kv_len + 1 : 0;
+  const int len = lane < fa.B ? s_kv_len[lane] + 1 : 0;
   int total = len;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
@@ -1261,7 +1387,7 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
   const int layer = d.layer;
 
   // item i goes to CTA i % G, so the splits spread over the SMs first
-  for (int item = warp * g.G + blockIdx.x; item < n_items; item += g.G * kAttnWarps) {
+  for (int item = warp * g.G + blockIdx.x; item < n_items && ok; item += g.G * kAttnWarps) {
     const unsigned hit = __ballot_sync(0xffffffffu, incl > item);
     const int b = __ffs(hit) - 1;
     const int before = __shfl_sync(0xffffffffu, incl - nsp * nkv, b);
@@ -1270,22 +1396,57 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
     const int rem = item - before;
     const int kvh = rem / nsp_b, sp = rem % nsp_b;
     const int p0 = sp * chunk, p1 = min(p0 + chunk, len_b);
-    const float* qsrc = d.q + (size_t)b * qstride + kvh * GRP * HD;
+    const int cur = len_b - 1;          // the position this frame appends
+    const bool has_cur = p1 == len_b;   // ... lies in this split's last tile
+    // q and the current K/V words: all loads issued, then the waits
+    const uint64_t* qsrc = d.q + (size_t)b * qstride + kvh * GRP * HD;
+    const uint64_t* kc = d.kvcur + (((size_t)b * 2 + 0) * nkv + kvh) * HD;
+    const uint64_t* vc = d.kvcur + (((size_t)b * 2 + 1) * nkv + kvh) * HD;
+    uint64_t qw[NQ][2], kw[NC][2], vw[NC][2];
+    const uint64_t *pq[NQ], *pk[NC], *pv[NC];
+    uint32_t tq[NQ], tk[NC];
+#pragma unroll
+    for (int u = 0; u < NQ; ++u) {
+      pq[u] = qsrc + 2 * (lane + 32 * u);
+      tq[u] = tag_in;
+      ld_ll2(pq[u], qw[u][0], qw[u][1]);
+    }
+#pragma unroll
+    for (int u = 0; u < NC; ++u) {
+      kw[u][0] = kw[u][1] = vw[u][0] = vw[u][1] = 0;
+      pk[u] = has_cur ? kc + 2 * (lane + 32 * u) : nullptr;
+      pv[u] = has_cur ? vc + 2 * (lane + 32 * u) : nullptr;
+      tk[u] = tag_in;
+      if (has_cur) {
+        ld_ll2(pk[u], kw[u][0], kw[u][1]);
+        ld_ll2(pv[u], vw[u][0], vw[u][1]);
+      }
+    }
+    ok &= ll_settle<NQ>(pq, tq, qw, g.err);
+    ok &= ll_settle<NC>(pk, tk, kw, g.err);
+    ok &= ll_settle<NC>(pv, tk, vw, g.err);
     __syncwarp();
-    for (int e = lane; e < GRP * HD; e += 32) T.q[e] = __ldcg(qsrc + e);
+#pragma unroll
+    for (int u = 0; u < NQ; ++u) {
+      const int c = 2 * (lane + 32 * u);
+      T.q[c] = ll_val(qw[u][0]);
+      T.q[c + 1] = ll_val(qw[u][1]);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
     AttnAcc<HD, GRP> A;
     attn_init(A);
-    bool ok = true;
     for (int pt = p0; pt < p1 && ok; pt += kPage)
-      ok = attn_fetch_fold<HD, GRP>(T, talker_kv_ptr(g, fa, layer, b, pt, 0, kvh), talker_kv_ptr(g, fa, layer, b, pt, 1, kvh),
-                                    min(kPage, p1 - pt), scale, parity, g.err, A);
+      ok = attn_fetch_fold<HD, GRP>(T, talker_kv_ptr(g, fa, layer, b, pt, 0, kvh),
+                                    talker_kv_ptr(g, fa, layer, b, pt, 1, kvh), min(kPage, p1 - pt), scale, parity,
+                                    g.err, A, (has_cur && cur < pt + kPage) ? cur - pt : -1, kw, vw);
     if (!ok) break;
-    float* out = d.attn_out + (size_t)b * qstride + kvh * GRP * HD;
+    uint64_t* out = d.attn_out + (size_t)b * qstride + kvh * GRP * HD;
     if (nsp_b == 1) {
 #pragma unroll
       for (int j = 0; j < GRP; ++j)
 #pragma unroll
-        for (int e = 0; e < E; ++e) out[j * HD + lane * E + e] = A.o[j][e] / A.l[j];
+        for (int e = 0; e < E; ++e) st_ll(out + j * HD + lane * E + e, A.o[j][e] / A.l[j], tag);
     } else {
       // partial (m, l, o) per query head; the last split to finish combines
       float* part = g.attn_part + ((((size_t)b * nkv + kvh) * kMaxSplits + sp) * GRP) * (HD + 2);
@@ -1301,32 +1462,45 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
       }
       __threadfence();
       __syncwarp();
-      int old = 0;
-      if (lane == 0) old = atomicAdd(&g.attn_cnt[b * nkv + kvh], 1);
+      unsigned old = 0;
+      // arrivals wrap back to zero on the last one, ready for the next frame
+      if (lane == 0) old = atomicInc(&g.attn_cnt[((size_t)layer * kMaxBatch + b) * nkv + kvh], (unsigned)(nsp_b - 1));
       old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == nsp_b - 1) {
+      if (old == (unsigned)(nsp_b - 1)) {
         __threadfence();
         const float* base = g.attn_part + ((((size_t)b * nkv + kvh) * kMaxSplits) * GRP) * (HD + 2);
 #pragma unroll
         for (int j = 0; j < GRP; ++j) {
           // lanes own splits for the max and the denominator
           float M = -INFINITY;
-          for (int s2 = lane; s2 < nsp_b; s2 += 32) M = fmaxf(M, __ldcg(base + ((size_t)s2 * GRP + j) * (HD + 2)));
+          float ms[kMaxSplits / 32], ls[kMaxSplits / 32];
+#pragma unroll
+          for (int t = 0; t < kMaxSplits / 32; ++t) {
+            const int s2 = lane + 32 * t;
+            ms[t] = -INFINITY;
+            ls[t] = 0.f;
+            if (s2 < nsp_b) {
+              const float* ps = base + ((size_t)s2 * GRP + j) * (HD + 2);
+              ms[t] = __ldcg(ps);
+              ls[t] = __ldcg(ps + 1);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < kMaxSplits / 32; ++t) M = fmaxf(M, ms[t]);
           M = warp_max(M);
           float L = 0.f;
-          for (int s2 = lane; s2 < nsp_b; s2 += 32) {
-            const float* ps = base + ((size_t)s2 * GRP + j) * (HD + 2);
-            L += expf(__ldcg(ps) - M) * __ldcg(ps + 1);
-          }
+#pragma unroll
+          for (int t = 0; t < kMaxSplits / 32; ++t)
+            if (lane + 32 * t < nsp_b) L += expf(ms[t] - M) * ls[t];
           L = warp_sum(L);
-          // lanes own head dimensions for the weighted sum, 2 splits per batch
+          // lanes own head dimensions for the weighted sum, 4 splits per batch of loads
           float o[E];
 #pragma unroll
           for (int e = 0; e < E; ++e) o[e] = 0.f;
-          for (int s0 = 0; s0 < nsp_b; s0 += 2) {
-            float mv[2], ov[2][E];
+          for (int s0 = 0; s0 < nsp_b; s0 += 4) {
+            float mv[4], ov[4][E];
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
+            for (int u = 0; u < 4; ++u)
               if (s0 + u < nsp_b) {
                 const float* ps = base + ((size_t)(s0 + u) * GRP + j) * (HD + 2);
                 mv[u] = __ldcg(ps);
@@ -1334,7 +1508,7 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
                 for (int e = 0; e < E; ++e) ov[u][e] = __ldcg(ps + 2 + lane * E + e);
               }
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
+            for (int u = 0; u < 4; ++u)
               if (s0 + u < nsp_b) {
                 const float w = expf(mv[u] - M);
 #pragma unroll
@@ -1342,123 +1516,207 @@ __device__ void stage_attn_talker(const StageDesc& d, const Globals& g, const Fr
               }
           }
 #pragma unroll
-          for (int e = 0; e < E; ++e) out[j * HD + lane * E + e] = o[e] / L;
+          for (int e = 0; e < E; ++e) st_ll(out + j * HD + lane * E + e, o[e] / L, tag);
         }
-        if (lane == 0) g.attn_cnt[b * nkv + kvh] = 0;  // ready for the next layer
       }
     }
   }
   __syncwarp();
   if (lane == 0) mbar_inval(&T.bar);
+  return ok;
+}
+
+// named barrier of one Code-Predictor attention group (ids 2.. ; 1 is cbar)
+__device__ __forceinline__ void group_bar(int grp) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + grp), "n"(kCpGroupWarps * 32) : "memory");
 }
 
 template <int HD, int GRP>
-__device__ void stage_attn_cp(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+__device__ bool stage_attn_cp(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+                              unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / kCpGroupWarps, gw = warp - grp * kCpGroupWarps;
+  if (grp >= kCpGroups) return true;  // warps beyond the last whole group sit this stage out
+  constexpr int GT = kCpGroupWarps * 32;
+  const int gt = gw * 32 + lane;
   constexpr int E = HD / 32;
+  constexpr int HH = HD / 2;
+  // word pairs per item: q (GRP*HD words), then K and V (16 positions x HD/2 words each)
+  constexpr int NQ2 = GRP * HD / 2;
+  constexpr int NB = (NQ2 + 2 * kCodebooks * HD / 4 + GT - 1) / GT;
   const int nkv = g.nkvc;
-  const int qstride = d.q_stride;
   const int rows = fa.B * d.rps;
-  if (warp >= kAttnWarps) return;
-  AttnTile& T = reinterpret_cast<AttnTile*>(smem)[warp];
-  if (lane == 0) {
-    mbar_init(&T.bar, 1);
-    mbar_init_fence();
-  }
-  __syncwarp();
-  uint32_t parity = 0;
+  AttnTile& T = reinterpret_cast<AttnTile*>(smem)[grp];
+  const uint32_t tag_q = fa.tag0 + (uint32_t)d.q_ws, tag_kv = fa.tag0;
   const float scale = rsqrtf((float)HD);
-  for (int item = warp * g.G + blockIdx.x; item < rows * nkv; item += g.G * kAttnWarps) {
+  bool ok = true;
+  // item i goes to CTA i % G, then to the CTA's next group
+  for (int item = grp * g.G + blockIdx.x; item < rows * nkv; item += g.G * kCpGroups) {
     const int r = item / nkv, kvh = item % nkv;
     const int b = r / d.rps, p = r % d.rps;
-    const int pos = d.pos_base + p;
-    const float* qsrc = d.q + (size_t)r * qstride + kvh * GRP * HD;
-    __syncwarp();
-    for (int e = lane; e < GRP * HD; e += 32) T.q[e] = __ldcg(qsrc + e);
-    AttnAcc<HD, GRP> A;
-    attn_init(A);
-    if (!attn_fetch_fold<HD, GRP>(T, cp_kv_ptr(g, d.cp_kv, b, 0, 0, kvh), cp_kv_ptr(g, d.cp_kv, b, 0, 1, kvh), pos + 1,
-                                  scale, parity, g.err, A))
-      break;
-    float* out = d.attn_out + (size_t)r * qstride + kvh * GRP * HD;
+    const int npos = d.pos_base + p + 1;  // positions 0..pos, all written this frame
+    const int nk2 = npos * HD / 4;
+    const int total = NQ2 + 2 * nk2;
+    const uint64_t* qsrc = d.q + (size_t)r * d.q_stride + kvh * GRP * HD;
+    const uint64_t* kb = cp_kv_word(g, d.cp_kv, b, 0, 0, kvh);
+    const uint64_t* vb = cp_kv_word(g, d.cp_kv, b, 0, 1, kvh);
+    uint64_t w[NB][2];
+    const uint64_t* ps[NB];
+    uint32_t tg[NB];
 #pragma unroll
-    for (int j = 0; j < GRP; ++j)
+    for (int u = 0; u < NB; ++u) {
+      const int i = gt + u * GT;
+      ps[u] = nullptr;
+      tg[u] = i < NQ2 ? tag_q : tag_kv;
+      w[u][0] = w[u][1] = 0;
+      if (i < total) {
+        ps[u] = i < NQ2 ? qsrc + 2 * i : i < NQ2 + nk2 ? kb + 2 * (i - NQ2) : vb + 2 * (i - NQ2 - nk2);
+        ld_ll2(ps[u], w[u][0], w[u][1]);
+      }
+    }
+    ok &= ll_settle<NB>(ps, tg, w, g.err);
 #pragma unroll
-      for (int e = 0; e < E; ++e) out[j * HD + lane * E + e] = A.o[j][e] / A.l[j];
+    for (int u = 0; u < NB; ++u) {
+      const int i = gt + u * GT;
+      if (i < total) {
+        if (i < NQ2) {
+          T.q[2 * i] = ll_val(w[u][0]);
+          T.q[2 * i + 1] = ll_val(w[u][1]);
+        } else if (i < NQ2 + nk2) {
+          const int c = 2 * (i - NQ2), pos = c / HH, wi = c - pos * HH;  // words wi, wi + 1
+          uint16_t* kr = T.k + pos * HD;
+          kr[wi] = (uint16_t)w[u][0];
+          kr[wi + HH] = (uint16_t)(w[u][0] >> 16);
+          kr[wi + 1] = (uint16_t)w[u][1];
+          kr[wi + 1 + HH] = (uint16_t)(w[u][1] >> 16);
+        } else {
+          const int c = 2 * (i - NQ2 - nk2), pos = c / HH, wi = c - pos * HH;
+          *reinterpret_cast<uint2*>(T.v + pos * HD + 2 * wi) = make_uint2((uint32_t)w[u][0], (uint32_t)w[u][1]);
+        }
+      }
+    }
+    group_bar(grp);
+    if (gw == 0) {
+      AttnAcc<HD, GRP> A;
+      attn_init(A);
+      attn_tile<HD, GRP>(T, npos, scale, A);
+      uint64_t* out = d.attn_out + (size_t)r * d.q_stride + kvh * GRP * HD;
+#pragma unroll
+      for (int j = 0; j < GRP; ++j)
+#pragma unroll
+        for (int e = 0; e < E; ++e) st_ll(out + j * HD + lane * E + e, A.o[j][e] / A.l[j], tag);
+    }
+    group_bar(grp);
   }
-  __syncwarp();
-  if (lane == 0) mbar_inval(&T.bar);
+  return ok;
 }
 
 template <bool TALKER>
-__device__ void stage_attn(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+__device__ bool stage_attn(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+                           unsigned char* smem) {
   const int hd = TALKER ? g.d : g.dc;
   const int grp = TALKER ? g.nq / g.nkv : g.nqc / g.nkvc;
-#define QTTS_ATTN_CASE(H_, G_)                             \
-  if (hd == H_ && grp == G_) {                             \
-    if (TALKER) stage_attn_talker<H_, G_>(d, g, fa, smem); \
-    else stage_attn_cp<H_, G_>(d, g, fa, smem);            \
-    return;                                                \
-  }
+#define QTTS_ATTN_CASE(H_, G_)                                           \
+  if (hd == H_ && grp == G_)                                             \
+    return TALKER ? stage_attn_talker<H_, G_>(d, tag, g, fa, smem)       \
+                  : stage_attn_cp<H_, G_>(d, tag, g, fa, smem);
   QTTS_ATTN_CASE(128, 2)
   QTTS_ATTN_CASE(64, 2)
   QTTS_ATTN_CASE(128, 1)
   QTTS_ATTN_CASE(64, 1)
 #undef QTTS_ATTN_CASE
+  return true;
 }
 
 // ---------------------------------------------------------------------------
 // stage: sampler for codebook j (one CTA per session), then the next
 // Code-Predictor input: the projected embedding row T_j[c] of the committed
-// code, with its sum of squares for the next stage's RMSNorm
+// code
 // ---------------------------------------------------------------------------
 
-__device__ void stage_sample(const StageDesc& d, const Globals& g, const FrameArgs& fa, unsigned char* smem) {
+__device__ bool stage_sample(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+                             unsigned char* smem) {
   const int b = blockIdx.x;
-  if (b >= fa.B) return;
+  if (b >= fa.B) return true;
+  const int tid = threadIdx.x;
   SampleSmem& S = *reinterpret_cast<SampleSmem*>(smem);
   const int j = d.codebook;
+  const int V = d.V;
+  // the session's logits, tagged by the head stage
+  {
+    constexpr int NB = (kMaxVocab / 2 + kCThreads - 1) / kCThreads;
+    const uint32_t tl = fa.tag0 + (uint32_t)d.l_ws;
+    const uint64_t* src = d.logits + (size_t)b * d.x_stride;
+    const int npair = (V + 1) / 2;  // rows are padded to an even length
+    bool ok = true;
+    uint64_t w[NB][2];
+    const uint64_t* ps[NB];
+    uint32_t tg[NB];
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int i = tid + u * kCThreads;
+      w[u][0] = w[u][1] = 0;
+      ps[u] = i < npair ? src + 2 * i : nullptr;
+      tg[u] = tl;
+      if (i < npair) ld_ll2(ps[u], w[u][0], w[u][1]);
+    }
+    ok &= ll_settle<NB>(ps, tg, w, g.err);
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int i = tid + u * kCThreads;
+      if (i < npair) {
+        S.lp[2 * i] = ll_val(w[u][0]);
+        if (2 * i + 1 < V) S.lp[2 * i + 1] = ll_val(w[u][1]);
+      }
+    }
+    if (cbar_or(!ok)) return false;
+  }
   const qtts_session ss = fa.sess[b];
   const qtts_rng rs = fa.rng[b];
   const uint32_t* seen = (j == 0 && fa.seen) ? fa.seen + (size_t)b * g.seen_words : nullptr;
-  const int code = sample_row(S, g.logits + (size_t)b * g.V0, true, d.V, j, ss, rs.key0, rs.key1, rs.frame_ctr,
-                              seen, g.eos_id, g.n_codes);
+  const int code = sample_row(S, nullptr, V, j, ss, rs.key0, rs.key1, rs.frame_ctr, seen, g.eos_id, g.n_codes);
   const int committed = fa.forced ? fa.forced[(size_t)b * kCodebooks + j] : code;
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     fa.codes_out[(size_t)b * kCodebooks + j] = code;
-    g.committed[(size_t)b * kCodebooks + j] = committed;
     if (j == 0) {
       if (fa.seen) fa.seen[(size_t)b * g.seen_words + (committed >> 5)] |= 1u << (committed & 31);
       fa.eos_out[b] = (uint8_t)(code == g.eos_id);
-      fa.sess[b].kv_len = ss.kv_len + 1;
+      fa.sess[b].kv_len = s_kv_len[b] + 1;
     }
     if (j == kCodebooks - 1) fa.rng[b].frame_ctr = rs.frame_ctr + 1u;
   }
   if (d.table) {
     const int row = b * d.next_rps + d.next_off;
     const float* src = d.table + (size_t)committed * g.Hc;
-    float* dst = d.x_next + (size_t)row * g.Hc;
-    float s = 0.f;
-    for (int k = threadIdx.x; k < g.Hc; k += kCThreads) {
-      const float v = src[k];
-      dst[k] = v;
-      s += v * v;
+    uint64_t* dst = d.x_next + (size_t)row * g.Hc;
+    for (int k = tid * 2; k < g.Hc; k += kCThreads * 2) {
+      const float2 v = *reinterpret_cast<const float2*>(src + k);
+      st_ll2(dst + k, v.x, v.y, tag);
     }
-    s = block_sum(s, S.redv);
-    for (int c = threadIdx.x; c < g.G; c += kCThreads) d.ssq_next[(size_t)c * kMaxRows + row] = (c == 0) ? s : 0.f;
   }
+  return true;
 }
 
 // ---------------------------------------------------------------------------
 // the persistent frame kernel
 // ---------------------------------------------------------------------------
 
-
 __global__ void __launch_bounds__(kThreads, 1)
-    frame_kernel(const StageDesc* __restrict__ prog, int s0, int s1, Globals g, FrameArgs fa) {
+    frame_kernel(const StageDesc* __restrict__ prog, int s0, int s1, Globals g_param, FrameArgs fa_param) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int sflag;
   __shared__ Ring ring;
+  // The stage functions take the frame constants by reference: keep them in
+  // shared memory. (A reference to a kernel parameter would put a copy on
+  // every thread's stack, and with nearly all of the SM's unified L1/shared
+  // memory given to shared memory, stack reads go out to L2.)
+  __shared__ Globals g;
+  __shared__ FrameArgs fa;
+  if (threadIdx.x == 0) {
+    g = g_param;
+    fa = fa_param;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     sflag = read_err(g.err);  // a device error is sticky until qtts_frame_status clears it
     for (int i = 0; i < kRingSlots; ++i) {
@@ -1469,6 +1727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init_fence();
   }
+  for (int b = threadIdx.x; b < fa.B; b += kThreads) s_kv_len[b] = fa.sess[b].kv_len;
   __syncthreads();  // the last barrier of all 16 warps: from here on, producer and compute warps part
   if (sflag) return;
   if ((threadIdx.x >> 5) == kProducerWarp) {
@@ -1479,7 +1738,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if ((threadIdx.x >> 5) == 0) fetch_desc(&prog[s0], &sdesc[s0 & 1]);
   cbar();
   uint32_t q = 0;
-  unsigned bar = 0;
   for (int s = s0; s < s1; ++s) {
     const StageDesc& d = sdesc[s & 1];
     const StageDesc* next = s + 1 < s1 ? &prog[s + 1] : nullptr;
@@ -1487,23 +1745,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) g_trace_stage = s;
     trace_mark(g, 0);
     // stages other than GEMVs fetch the next descriptor up front, on a warp
-    // they leave idle (attention uses warps 0..7; the sampler's CTAs differ)
+    // they leave idle or finish with (Talker attention uses warps 0..7)
     if (d.type != ST_GEMV && next && (threadIdx.x >> 5) == kCWarps - 1) fetch_desc(next, next_s);
+    const uint32_t tag = fa.tag0 + (uint32_t)s;
+    bool ok = true;
     switch (d.type) {
-      case ST_BEGIN:
-        if (!stage_begin(g, fa, smem)) return;
-        break;
-      case ST_GEMV: stage_gemv(d, g, fa, smem, &ring, q, next, next_s); break;
-      case ST_ATTN_T: stage_attn<true>(d, g, fa, smem); break;
-      case ST_ATTN_CP: stage_attn<false>(d, g, fa, smem); break;
-      case ST_SAMPLE: stage_sample(d, g, fa, smem); break;
+      case ST_BEGIN: ok = stage_begin(d, tag, g, fa); break;
+      case ST_GEMV: ok = stage_gemv(d, tag, g, fa, smem, &ring, q, next, next_s); break;
+      case ST_ATTN_T: ok = stage_attn<true>(d, tag, g, fa, smem); break;
+      case ST_ATTN_CP: ok = stage_attn<false>(d, tag, g, fa, smem); break;
+      case ST_SAMPLE: ok = stage_sample(d, tag, g, fa, smem); break;
       default: break;
     }
     trace_mark(g, 7);
-    if (s + 1 < s1) {
-      bar += gridDim.x;
-      if (!grid_sync(g, bar, &sflag)) return;
-    }
+    // no grid barrier: the next stage waits on the tags of the words it reads
+    if (cbar_or(!ok)) return;
   }
 }
 
@@ -1519,8 +1775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const qtts_session ss = fa.sess[b];
   const qtts_rng rs = fa.rng[b];
   const uint32_t* seen = (j == 0 && fa.seen) ? fa.seen + (size_t)b * g.seen_words : nullptr;
-  const int code = sample_row(S, logits + (size_t)b * V, false, V, j, ss, rs.key0, rs.key1, rs.frame_ctr, seen,
-                              g.eos_id, g.n_codes);
+  const int code = sample_row(S, logits + (size_t)b * V, V, j, ss, rs.key0, rs.key1, rs.frame_ctr, seen, g.eos_id,
+                              g.n_codes);
   if (threadIdx.x == 0) fa.codes_out[b] = code;
 }
 
@@ -1534,6 +1790,9 @@ cudaError_t frame_kernel_occupancy(int* blocks_per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, frame_kernel, kThreads, kSmemBytes);
 }
 
+// Persistent mode needs every CTA resident at once (CTAs wait on one
+// another's words), hence the cooperative launch; stepwise mode runs one
+// stage per launch, whose inputs all come from earlier launches.
 cudaError_t launch_frame(const StageDesc* prog, int n_stages, const Globals& g, const FrameArgs& fa, bool stepwise,
                          cudaStream_t stream) {
   if (stepwise) {
@@ -1544,8 +1803,6 @@ cudaError_t launch_frame(const StageDesc* prog, int n_stages, const Globals& g, 
     }
     return cudaSuccess;
   }
-  cudaError_t e = cudaMemsetAsync(g.barrier, 0, sizeof(unsigned), stream);
-  if (e != cudaSuccess) return e;
   int s0 = 0, s1 = n_stages;
   Globals gg = g;
   FrameArgs ff = fa;

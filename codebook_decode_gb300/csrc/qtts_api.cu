@@ -44,6 +44,22 @@ struct Spec {
   void* dst;  // K_COPY destination
 };
 
+// Tagged activation buffers (see StageDesc): two copies of each per-layer
+// kind, used by alternate layers, so a layer never overwrites words the
+// previous layer's readers may still be polling.
+struct Acts {
+  uint64_t* xin = nullptr;                    // Talker input rows [kMaxBatch][H]
+  uint64_t *q[2] = {}, *kvcur[2] = {}, *att[2] = {}, *xmid[2] = {}, *xout[2] = {}, *act[2] = {};
+  uint64_t* logits0 = nullptr;                // [kMaxBatch][V0 padded even]
+  uint64_t* cpx = nullptr;                    // Code-Predictor step-1 inputs [kMaxBatch][2][Hc]
+  uint64_t *qc[2] = {}, *attc[2] = {}, *xmidc[2] = {}, *xoutc[2] = {}, *actc[2] = {};
+  uint64_t* logitsc[2] = {};                  // [kMaxBatch][Vc padded even]
+  uint64_t* xnext[2] = {};                    // [kMaxBatch][Hc]
+  uint64_t* cpkv = nullptr;                   // [cp_layers][kMaxBatch][2][nkvc][16][dc/2]
+  uint64_t* base = nullptr;
+  size_t words = 0;
+};
+
 }  // namespace
 
 struct qtts_model {
@@ -68,7 +84,8 @@ struct qtts_model {
   std::vector<int32_t> free_ids;
   std::vector<uint8_t> page_used;
 
-  uint16_t* cp_kv = nullptr;
+  Acts acts;
+  uint32_t frame_seq = 0;  // frames launched since the buffers were last cleared
   unsigned long long* trace_buf = nullptr;
   Globals g{};
   StageDesc* prog_dev[2] = {nullptr, nullptr};
@@ -178,8 +195,8 @@ int seen_words(const qtts_config& c) { return (c.vocab0 + 31) / 32; }
 // stage program
 // --------------------------------------------------------------------------
 
-Seg make_seg(const LinW& L, bool i8, int unit, int epi, float* out, int out_stride, int out_rps, int out_off,
-             float* ssq_out, const uint16_t* bias) {
+Seg make_seg(const LinW& L, bool i8, int unit, int epi, uint64_t* out, int out_stride, int out_rps, int out_off,
+             const uint64_t* resid, int r_ws0, int r_ws1, const uint16_t* bias) {
   Seg s{};
   s.w = i8 ? (const void*)L.q : (const void*)L.w;
   s.scale = i8 ? L.s : nullptr;
@@ -190,13 +207,15 @@ Seg make_seg(const LinW& L, bool i8, int unit, int epi, float* out, int out_stri
   s.out_stride = out_stride;
   s.out_rps = out_rps;
   s.out_off = out_off;
-  s.ssq_out = ssq_out;
+  s.resid = resid;
+  s.r_ws[0] = r_ws0;
+  s.r_ws[1] = r_ws1;
   s.bias = bias;
   return s;
 }
 
-StageDesc gemv(int rps, int pos_base, int layer, int K, int xsrc, const float* x, int x_stride, int in_rps,
-               int in_off, const float* ssq, const uint16_t* gain) {
+StageDesc gemv(int rps, int pos_base, int layer, int K, int xsrc, const uint64_t* x, int x_stride, int in_rps,
+               int in_off, int x_ws0, int x_ws1, const uint16_t* gain) {
   StageDesc d{};
   d.type = ST_GEMV;
   d.rps = rps;
@@ -208,13 +227,17 @@ StageDesc gemv(int rps, int pos_base, int layer, int K, int xsrc, const float* x
   d.x_stride = x_stride;
   d.in_rps = in_rps;
   d.in_off = in_off;
-  d.ssq = ssq;
+  d.x_ws[0] = x_ws0;
+  d.x_ws[1] = x_ws1;
   d.gain = gain;
   d.nseg = 1;
   return d;
 }
 
-// The frame as a sequence of stages separated by grid barriers:
+int even(int v) { return (v + 1) & ~1; }
+
+// The frame as a sequence of stages; each reads tagged words that earlier
+// stages wrote (x_ws / r_ws / q_ws / l_ws name the writing stage):
 //   begin; Talker x L_T: [norm+QKV+RoPE+KV append] [attention] [O + residual]
 //   [norm+gate|up+SwiGLU] [down + residual]; [final norm + codebook-0 head
 //   + projection of h_t]; [sampler 0 + T_0 gather];
@@ -222,22 +245,32 @@ StageDesc gemv(int rps, int pos_base, int layer, int K, int xsrc, const float* x
 //   per session at j = 1), [final norm + head j], [sampler j + T_j gather].
 std::vector<StageDesc> build_program(qtts_model* m, bool i8) {
   const qtts_config& c = m->cfg;
-  Globals& g = m->g;
-  const int qs = std::max(c.n_q_heads * c.head_dim, c.cp_n_q_heads * c.cp_head_dim);
-  const int hs = std::max(c.ffn, c.cp_ffn);
+  const Acts& A = m->acts;
   std::vector<StageDesc> P;
   StageDesc b{};
   b.type = ST_BEGIN;
   b.rps = 1;
+  b.x_next = A.xin;
   P.push_back(b);
-  auto layer_stages = [&](const LayerW& L, bool talker, int l, int rps, int pos_base, uint16_t* cp_kv) {
+  // the current residual stream: buffer, row layout and writing stage per position
+  struct Cur {
+    const uint64_t* x;
+    int rps, ws[2];
+  };
+  auto layer_stages = [&](const LayerW& L, bool talker, int l, int par, int rps, int pos_base, uint64_t* cp_kv,
+                          Cur& cur) {
     const int H = talker ? c.hidden : c.cp_hidden;
     const int F = talker ? c.ffn : c.cp_ffn;
     const int qw = talker ? c.n_q_heads * c.head_dim : c.cp_n_q_heads * c.cp_head_dim;
-    float* x = talker ? g.x_t : g.x_c;
-    float* ssq = talker ? g.ssq_t : g.ssq_c;
-    StageDesc d = gemv(rps, pos_base, l, H, X_NORM, x, H, rps, 0, ssq, L.in_norm);
-    d.seg[0] = make_seg(L.qkv, i8, 2, talker ? E_QKV_T : E_QKV_CP, g.q, qs, rps, 0, nullptr, nullptr);
+    uint64_t* q = talker ? A.q[par] : A.qc[par];
+    uint64_t* att = talker ? A.att[par] : A.attc[par];
+    uint64_t* xmid = talker ? A.xmid[par] : A.xmidc[par];
+    uint64_t* xout = talker ? A.xout[par] : A.xoutc[par];
+    uint64_t* act = talker ? A.act[par] : A.actc[par];
+    const int sq = (int)P.size();
+    StageDesc d = gemv(rps, pos_base, l, H, X_NORM, cur.x, H, cur.rps, 0, cur.ws[0], cur.ws[1], L.in_norm);
+    d.seg[0] = make_seg(L.qkv, i8, 2, talker ? E_QKV_T : E_QKV_CP, q, qw, rps, 0, nullptr, 0, 0, nullptr);
+    d.kvcur = talker ? A.kvcur[par] : nullptr;
     d.cp_kv = cp_kv;
     P.push_back(d);
     StageDesc a{};
@@ -245,60 +278,78 @@ std::vector<StageDesc> build_program(qtts_model* m, bool i8) {
     a.rps = rps;
     a.pos_base = pos_base;
     a.layer = l;
-    a.q = g.q;
-    a.attn_out = g.attn;
-    a.q_stride = qs;
+    a.q = q;
+    a.q_ws = sq;
+    a.attn_out = att;
+    a.q_stride = qw;
+    a.kvcur = d.kvcur;
     a.cp_kv = cp_kv;
     P.push_back(a);
-    d = gemv(rps, pos_base, l, qw, X_PLAIN, g.attn, qs, rps, 0, nullptr, nullptr);
-    d.seg[0] = make_seg(L.o, i8, 1, E_RESID, x, H, rps, 0, ssq, nullptr);
+    d = gemv(rps, pos_base, l, qw, X_PLAIN, att, qw, rps, 0, sq + 1, sq + 1, nullptr);
+    d.seg[0] = make_seg(L.o, i8, 1, E_RESID, xmid, H, rps, 0, cur.x, cur.ws[0], cur.ws[1], nullptr);
     P.push_back(d);
-    d = gemv(rps, pos_base, l, H, X_NORM, x, H, rps, 0, ssq, L.post_norm);
-    d.seg[0] = make_seg(L.gu, i8, 2, E_SWIGLU, g.h, hs, rps, 0, nullptr, nullptr);
+    d = gemv(rps, pos_base, l, H, X_NORM, xmid, H, rps, 0, sq + 2, sq + 2, L.post_norm);
+    d.seg[0] = make_seg(L.gu, i8, 2, E_SWIGLU, act, F, rps, 0, nullptr, 0, 0, nullptr);
     P.push_back(d);
-    d = gemv(rps, pos_base, l, F, X_PLAIN, g.h, hs, rps, 0, nullptr, nullptr);
-    d.seg[0] = make_seg(L.down, i8, 1, E_RESID, x, H, rps, 0, ssq, nullptr);
+    d = gemv(rps, pos_base, l, F, X_PLAIN, act, F, rps, 0, sq + 3, sq + 3, nullptr);
+    d.seg[0] = make_seg(L.down, i8, 1, E_RESID, xout, H, rps, 0, xmid, sq + 2, sq + 2, nullptr);
     P.push_back(d);
+    cur = Cur{xout, rps, {sq + 4, sq + 4}};
   };
-  for (int l = 0; l < c.n_layers; ++l) layer_stages(m->tl[l], true, l, 1, 0, nullptr);
-  StageDesc h = gemv(1, 0, 0, c.hidden, X_NORM, g.x_t, c.hidden, 1, 0, g.ssq_t, m->final_norm);
+  Cur cur{A.xin, 1, {0, 0}};
+  for (int l = 0; l < c.n_layers; ++l) layer_stages(m->tl[l], true, l, l & 1, 1, 0, nullptr, cur);
+  const int sh = (int)P.size();
+  StageDesc h = gemv(1, 0, 0, c.hidden, X_NORM, cur.x, c.hidden, 1, 0, cur.ws[0], cur.ws[1], m->final_norm);
   h.codebook = 0;
   h.nseg = 2;
-  h.seg[0] = make_seg(m->head0, i8, 1, E_LOGITS, g.logits, c.vocab0, 1, 0, nullptr, nullptr);
-  h.seg[1] = make_seg(m->proj, i8, 1, E_CPIN, g.x_c, c.cp_hidden, 2, 0, g.ssq_c, m->proj_b);
+  h.seg[0] = make_seg(m->head0, i8, 1, E_LOGITS, A.logits0, even(c.vocab0), 1, 0, nullptr, 0, 0, nullptr);
+  h.seg[1] = make_seg(m->proj, i8, 1, E_CPIN, A.cpx, c.cp_hidden, 2, 0, nullptr, 0, 0, m->proj_b);
   P.push_back(h);
+  const int ss = (int)P.size();
   StageDesc s{};
   s.type = ST_SAMPLE;
   s.rps = 1;
   s.codebook = 0;
   s.V = c.vocab0;
+  s.logits = A.logits0;
+  s.l_ws = sh;
+  s.x_stride = even(c.vocab0);
   s.table = i8 ? m->T_i8[0] : m->T_bf[0];
-  s.x_next = g.x_c;
-  s.ssq_next = g.ssq_c;
+  s.x_next = A.cpx;
   s.next_rps = 2;
   s.next_off = 1;
   P.push_back(s);
-  const size_t cp_layer_stride = (size_t)kMaxBatch * 2 * kCodebooks * c.cp_n_kv_heads * c.cp_head_dim;
+  const size_t cp_layer_words = (size_t)kMaxBatch * 2 * c.cp_n_kv_heads * kCodebooks * (c.cp_head_dim / 2);
+  Cur cc{A.cpx, 2, {sh, ss}};  // step 1: position 0 = P(h_t) from the head stage, 1 = T_0[c_0] from sampler 0
   for (int j = 1; j < kCodebooks; ++j) {
     const int rps = j == 1 ? 2 : 1;
     const int pos_base = j == 1 ? 0 : j;
     for (int l = 0; l < c.cp_layers; ++l)
-      layer_stages(m->cl[l], false, l, rps, pos_base, m->cp_kv + l * cp_layer_stride);
-    StageDesc hd = gemv(1, 0, 0, c.cp_hidden, X_NORM, g.x_c, c.cp_hidden, rps, rps - 1, g.ssq_c, m->cp_final_norm);
+      layer_stages(m->cl[l], false, l, ((j - 1) * c.cp_layers + l) & 1, rps, pos_base, A.cpkv + l * cp_layer_words,
+                   cc);
+    const int shj = (int)P.size();
+    // codebook j's logits come from position j: the last row of the session
+    StageDesc hd = gemv(1, 0, 0, c.cp_hidden, X_NORM, cc.x, c.cp_hidden, rps, rps - 1, cc.ws[rps - 1],
+                        cc.ws[rps - 1], m->cp_final_norm);
     hd.codebook = j;
-    hd.seg[0] = make_seg(m->cp_head[j], i8, 1, E_LOGITS, g.logits, c.vocab0, 1, 0, nullptr, nullptr);
+    hd.seg[0] = make_seg(m->cp_head[j], i8, 1, E_LOGITS, A.logitsc[j & 1], even(c.cp_vocab), 1, 0, nullptr, 0, 0,
+                         nullptr);
     P.push_back(hd);
+    const int ssj = (int)P.size();
     StageDesc sj{};
     sj.type = ST_SAMPLE;
     sj.rps = 1;
     sj.codebook = j;
     sj.V = c.cp_vocab;
+    sj.logits = A.logitsc[j & 1];
+    sj.l_ws = shj;
+    sj.x_stride = even(c.cp_vocab);
     sj.table = (j < kCodebooks - 1) ? (i8 ? m->T_i8[j] : m->T_bf[j]) : nullptr;
-    sj.x_next = g.x_c;
-    sj.ssq_next = g.ssq_c;
+    sj.x_next = A.xnext[j & 1];
     sj.next_rps = 1;
     sj.next_off = 0;
     P.push_back(sj);
+    cc = Cur{A.xnext[j & 1], 1, {ssj, ssj}};
   }
   return P;
 }
@@ -458,6 +509,14 @@ int build_tables(qtts_model* m, bool i8) {
   return QTTS_OK;
 }
 
+size_t trace_words(const qtts_model* m, int ctas) { return (size_t)8 * ctas * m->n_stages + 2 * 4096; }
+
+// An abandoned frame can leave attention split counters part-way; clear them
+// whenever a device error is reported.
+cudaError_t reset_split_counters(qtts_model* m) {
+  return cudaMemset(m->g.attn_cnt, 0, sizeof(unsigned) * m->cfg.n_layers * kMaxBatch * m->cfg.n_kv_heads);
+}
+
 }  // namespace
 
 // ==========================================================================
@@ -553,21 +612,44 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
       return bail(fail(m, QTTS_E_CUDA, "RoPE table upload failed"));
     g.rope_cos = a; g.rope_sin = b; g.cp_rope_cos = cc; g.cp_rope_sin = dd;
   }
-  const int qs = std::max(c.n_q_heads * c.head_dim, c.cp_n_q_heads * c.cp_head_dim);
-  const int hs = std::max(c.ffn, c.cp_ffn);
   const int grp = c.n_q_heads / c.n_kv_heads;
-  if ((rc = dalloc(m, &g.x_t, (size_t)kMaxBatch * c.hidden)) ||
-      (rc = dalloc(m, &g.x_c, (size_t)kMaxRows * c.cp_hidden)) || (rc = dalloc(m, &g.ssq_t, (size_t)sms * kMaxRows)) ||
-      (rc = dalloc(m, &g.ssq_c, (size_t)sms * kMaxRows)) || (rc = dalloc(m, &g.q, (size_t)kMaxRows * qs)) ||
-      (rc = dalloc(m, &g.attn, (size_t)kMaxRows * qs)) || (rc = dalloc(m, &g.h, (size_t)kMaxRows * hs)) ||
-      (rc = dalloc(m, &g.logits, (size_t)kMaxBatch * c.vocab0)) ||
-      (rc = dalloc(m, &g.attn_part, (size_t)kMaxBatch * c.n_kv_heads * kMaxSplits * grp * (c.head_dim + 2))) ||
-      (rc = dalloc(m, &g.attn_cnt, (size_t)kMaxBatch * c.n_kv_heads)) ||
-      (rc = dalloc(m, &g.committed, (size_t)kMaxBatch * kCodebooks)) || (rc = dalloc(m, &g.barrier, 1)) ||
-      (rc = dalloc(m, &g.err, 1)))
+  if ((rc = dalloc(m, &g.attn_part, (size_t)kMaxBatch * c.n_kv_heads * kMaxSplits * grp * (c.head_dim + 2))) ||
+      (rc = dalloc(m, &g.attn_cnt, (size_t)c.n_layers * kMaxBatch * c.n_kv_heads)) || (rc = dalloc(m, &g.err, 1)))
     return bail(rc);
-  if ((rc = dalloc(m, &m->cp_kv, (size_t)c.cp_layers * kMaxBatch * 2 * kCodebooks * c.cp_n_kv_heads * c.cp_head_dim)))
-    return bail(rc);
+  // tagged activation buffers, one arena (zero tags never match a frame's)
+  {
+    Acts& A = m->acts;
+    const size_t B = kMaxBatch, R = kMaxRows;
+    const size_t qt = (size_t)c.n_q_heads * c.head_dim, qc = (size_t)c.cp_n_q_heads * c.cp_head_dim;
+    std::vector<std::pair<uint64_t**, size_t>> parts = {{&A.xin, B * c.hidden},
+                                                        {&A.logits0, B * even(c.vocab0)},
+                                                        {&A.cpx, B * 2 * c.cp_hidden}};
+    for (int i = 0; i < 2; ++i) {
+      parts.push_back({&A.q[i], B * qt});
+      parts.push_back({&A.kvcur[i], B * 2 * c.n_kv_heads * c.head_dim});
+      parts.push_back({&A.att[i], B * qt});
+      parts.push_back({&A.xmid[i], B * c.hidden});
+      parts.push_back({&A.xout[i], B * c.hidden});
+      parts.push_back({&A.act[i], B * c.ffn});
+      parts.push_back({&A.qc[i], R * qc});
+      parts.push_back({&A.attc[i], R * qc});
+      parts.push_back({&A.xmidc[i], R * c.cp_hidden});
+      parts.push_back({&A.xoutc[i], R * c.cp_hidden});
+      parts.push_back({&A.actc[i], R * c.cp_ffn});
+      parts.push_back({&A.logitsc[i], B * even(c.cp_vocab)});
+      parts.push_back({&A.xnext[i], B * c.cp_hidden});
+    }
+    parts.push_back({&A.cpkv, (size_t)c.cp_layers * B * 2 * c.cp_n_kv_heads * kCodebooks * (c.cp_head_dim / 2)});
+    size_t total = 0;
+    for (auto& pr : parts) total += (pr.second + 31) & ~(size_t)31;  // 256-byte aligned pieces
+    if ((rc = dalloc(m, &A.base, total))) return bail(rc);
+    A.words = total;
+    size_t off = 0;
+    for (auto& pr : parts) {
+      *pr.first = A.base + off;
+      off += (pr.second + 31) & ~(size_t)31;
+    }
+  }
   // staging for the host-buffer frame
   m->st_bt_cap = (c.max_context + kPage - 1) / kPage;
   if ((rc = dalloc(m, &m->st_sess, kMaxBatch)) || (rc = dalloc(m, &m->st_bt, (size_t)kMaxBatch * m->st_bt_cap)) ||
@@ -847,6 +929,16 @@ int qtts_frame_step(qtts_model* m, int B, qtts_session* sess, const int32_t* bt,
   fa.logits_out = logits_out;
   cudaStream_t s = (cudaStream_t)stream;
   const bool i8 = m->use_int8;
+  // tag base: stage s of this frame writes tag0 + s; tags only grow, so no
+  // word left by an earlier frame matches. Before they would wrap, the
+  // buffers are cleared and the count restarts.
+  if ((uint64_t)(m->frame_seq + 2) * (uint64_t)m->n_stages >= 0xFFFFFFFFull) {
+    CK(m, cudaDeviceSynchronize());
+    CK(m, cudaMemset(m->acts.base, 0, m->acts.words * sizeof(uint64_t)));
+    m->frame_seq = 0;
+  }
+  ++m->frame_seq;
+  fa.tag0 = m->frame_seq * (uint32_t)m->n_stages;
   const cudaError_t e = launch_frame(m->prog_dev[i8 ? 1 : 0], m->n_stages, m->g, fa, m->stepwise, s);
   m->last_stream = s;
   if (e != cudaSuccess) return cuda_fail(m, e, "frame launch");
@@ -904,7 +996,10 @@ int qtts_frame_step_host(qtts_model* m, int B, qtts_session* sess, const int32_t
   CK(m, cudaStreamSynchronize(s));
   int derr = 0;
   CK(m, cudaMemcpy(&derr, m->g.err, 4, cudaMemcpyDeviceToHost));
-  if (derr) return fail(m, derr == QTTS_DEV_TIMEOUT ? QTTS_E_TIMEOUT : QTTS_E_DEVICE, "device error %d", derr);
+  if (derr) {
+    CK(m, reset_split_counters(m));
+    return fail(m, derr == QTTS_DEV_TIMEOUT ? QTTS_E_TIMEOUT : QTTS_E_DEVICE, "device error %d", derr);
+  }
   return QTTS_OK;
 }
 
@@ -914,7 +1009,10 @@ int qtts_frame_status(qtts_model* m, int* device_err) {
   CK(m, cudaStreamSynchronize(m->last_stream));
   int derr = 0;
   CK(m, cudaMemcpy(&derr, m->g.err, 4, cudaMemcpyDeviceToHost));
-  if (derr) CK(m, cudaMemset(m->g.err, 0, 4));
+  if (derr) {
+    CK(m, cudaMemset(m->g.err, 0, 4));
+    CK(m, reset_split_counters(m));
+  }
   if (device_err) *device_err = derr;
   if (derr) return fail(m, derr == QTTS_DEV_TIMEOUT ? QTTS_E_TIMEOUT : QTTS_E_DEVICE, "device error %d", derr);
   return QTTS_OK;
@@ -969,11 +1067,13 @@ int qtts_set_option(qtts_model* m, int option, int value) {
   }
   if (option == QTTS_OPT_TRACE) {
     if (!m->loaded) return fail(m, QTTS_E_STATE, "load weights first");
+    if (value < 0 || value > 2) return fail(m, QTTS_E_INVALID, "trace must be 0, 1 or 2");
     if (value && !m->trace_buf) {
       cudaSetDevice(m->device);
-      AL(m, m->trace_buf, (size_t)16 * m->n_stages + 2 * 4096);
+      AL(m, m->trace_buf, trace_words(m, m->G));
     }
     m->g.trace = value ? m->trace_buf : nullptr;
+    m->g.trace_ctas = value == 2 ? m->G : 2;
     return QTTS_OK;
   }
   return fail(m, QTTS_E_INVALID, "unknown option %d", option);
@@ -984,7 +1084,7 @@ int qtts_frame_trace(qtts_model* m, uint64_t* host, int capacity) {
   if (!m->trace_buf) return fail(m, QTTS_E_STATE, "tracing was never enabled");
   cudaSetDevice(m->device);
   CK(m, cudaStreamSynchronize(m->last_stream));
-  const int n = std::min(capacity, 16 * m->n_stages + 2 * 4096);
+  const int n = (int)std::min((size_t)capacity, trace_words(m, m->g.trace_ctas));
   CK(m, cudaMemcpy(host, m->trace_buf, (size_t)n * sizeof(uint64_t), cudaMemcpyDeviceToHost));
   return n;
 }

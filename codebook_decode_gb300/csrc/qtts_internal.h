@@ -9,7 +9,7 @@
 
 namespace qtts {
 
-constexpr int kThreads = 512;            // one persistent CTA per SM
+constexpr int kThreads = 384;            // one persistent CTA per SM
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxBatch = 32;
 constexpr int kMaxRows = 2 * kMaxBatch;  // Code-Predictor step 1 runs two positions per session
@@ -30,6 +30,12 @@ enum StageType { ST_BEGIN = 0, ST_GEMV = 1, ST_ATTN_T = 2, ST_ATTN_CP = 3, ST_SA
 enum XSrc { X_NORM = 0, X_PLAIN = 1 };
 enum Epi { E_QKV_T = 0, E_QKV_CP = 1, E_RESID = 2, E_SWIGLU = 3, E_LOGITS = 4, E_CPIN = 5 };
 
+// Activations pass between stages (and CTAs) as tagged 8-byte words: the
+// payload in the low 32 bits, in the high 32 bits the tag of the frame and
+// stage that wrote it (frame tag base + stage index). A consumer re-reads a
+// word until the tag is the one it expects, so stages need no grid barrier.
+// Payload: one fp32 value, except in the Code-Predictor cache (two bf16).
+
 // One weight segment of a GEMV stage: rows [0, N) of W, split over the grid
 // in units of `unit` rows, each finished by epilogue `epi`.
 struct Seg {
@@ -38,10 +44,11 @@ struct Seg {
   int N;
   int unit;               // 2: rows come in (RoPE pair | gate,up | v pair) pairs
   int epi;
-  float* out;             // destination rows (see Epi)
-  int out_stride;         // floats per destination row
+  int out_stride;         // words per destination row
   int out_rps, out_off;   // destination row of (session b, position p) = b*out_rps + out_off + p
-  float* ssq_out;         // E_RESID / E_CPIN: per-CTA sum-of-squares partials [G][kMaxRows]
+  int r_ws[2];            // E_RESID: stage that wrote the residual row of position p
+  uint64_t* out;          // tagged destination rows
+  const uint64_t* resid;  // E_RESID: residual rows, laid out like `out`
   const uint16_t* bias;   // E_CPIN: optional bf16 bias [N]
 };
 
@@ -51,26 +58,29 @@ struct alignas(16) StageDesc {
   int pos_base;           // Code-Predictor position of row p of a session: pos_base + p
   int layer;
   int codebook;           // head / sample stages
-  // GEMV input X [rows][K]
+  // GEMV input X [rows][K] (tagged words)
   int K;
   int xsrc;
   int in_rps, in_off;     // input row of (b, p) = b*in_rps + in_off + p
-  int x_stride;           // floats per input row
-  const float* x;
-  const float* ssq;       // X_NORM: partials [G][kMaxRows] of the input rows
-  const uint16_t* gain;   // X_NORM gain [K]
+  int x_stride;           // words per input row
+  int x_ws[2];            // stage that wrote the input row of position p
   int nseg;
+  const uint64_t* x;
+  const uint16_t* gain;   // X_NORM gain [K]
   Seg seg[2];
   // attention: q [rows][q_stride] in, attn_out [rows][q_stride] out
-  const float* q;
-  float* attn_out;
+  const uint64_t* q;
+  uint64_t* attn_out;
   int q_stride;
-  uint16_t* cp_kv;        // Code-Predictor cache of this layer [kMaxBatch][2][nkv][16][d]
+  int q_ws;               // stage that wrote q (and the current K/V)
+  uint64_t* kvcur;        // Talker: this frame's K and V rows [kMaxBatch][2][nkv][d]
+  uint64_t* cp_kv;        // Code-Predictor cache of this layer [kMaxBatch][2][nkv][16][d/2]
   // sampler
   int V;
+  int l_ws;               // stage that wrote the logits
+  const uint64_t* logits; // [kMaxBatch][V] tagged
   const float* table;     // projected embedding table T_j [V_j][Hc] fp32 (nullptr for j = 15)
-  float* x_next;
-  float* ssq_next;
+  uint64_t* x_next;       // begin: Talker input rows; sampler: next Code-Predictor input rows
   int next_rps, next_off;
 };
 
@@ -87,26 +97,18 @@ struct Globals {
   const float* rope_sin;
   const float* cp_rope_cos;  // [16][dc/2]
   const float* cp_rope_sin;
-  float* x_t;             // Talker residual [kMaxBatch][H]
-  float* x_c;             // Code-Predictor residual [kMaxRows][Hc]
-  float* ssq_t;           // [G][kMaxRows]
-  float* ssq_c;
-  float* q;               // [kMaxRows][max(nq*d, nqc*dc)]
-  float* attn;            // same shape
-  float* h;               // [kMaxRows][max(F, Fc)]
-  float* logits;          // [kMaxBatch][V0]
   float* attn_part;       // [kMaxBatch][nkv][kMaxSplits][grp][d + 2]
-  int* attn_cnt;          // [kMaxBatch][nkv]
-  int* committed;         // [kMaxBatch][16] codes fed forward (forced or sampled)
-  unsigned* barrier;      // grid barrier counter (zeroed before each persistent launch)
+  unsigned* attn_cnt;     // [layer][kMaxBatch][nkv] split arrivals (wrap to 0 on the last)
   int* err;               // device error word (QTTS_DEV_*)
   int n_stages;
   int ring_slots;         // weight-ring slots in use (1..8): how far the producer may run ahead
-  unsigned long long* trace;  // optional [2 CTAs][n_stages][start, end] %globaltimer stamps
+  unsigned long long* trace;  // optional [trace_ctas][n_stages][8] %globaltimer stamps, then ring events
+  int trace_ctas;         // 2: the first and the last CTA; G: every CTA
 };
 
 struct FrameArgs {
   int B;
+  uint32_t tag0;          // this frame's tag base: a word written by stage s carries tag0 + s
   qtts_session* sess;
   const int32_t* bt;
   int bt_stride;

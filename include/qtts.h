@@ -255,7 +255,8 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
  *   QTTS_OPT_STEPWISE  1: one launch per stage instead of one persistent
  *                      launch per frame (debugging aid). Default 0.
  *   QTTS_OPT_TRACE     1: record %globaltimer stamps inside every stage on
- *                      the first and last CTA (qtts_frame_trace).
+ *                      the first and last CTA (qtts_frame_trace); 2: on
+ *                      every CTA. 0 (default): off.
  *   QTTS_OPT_RING_SLOTS 1..8: 16 KB weight slots per SM the producer warp may
  *                      fill ahead of the compute warps. Default 8. */
 #define QTTS_OPT_STEPWISE 1
@@ -265,11 +266,13 @@ int qtts_set_option(qtts_model* m, int option, int value);
 
 /* Stage timestamps of the last frame run with QTTS_OPT_TRACE on: 8 values
  * per stage for CTA 0 (every stage in order), then the same for the last CTA
- * (nanoseconds, %globaltimer; 0 = stage start, 1 after the GEMV prologue,
- * 2 after its weight pass, 3 after its epilogues, 7 = stage end; unused
- * marks keep older values); then, for CTA 0, 4096 pairs (issue, ready) of
- * the weight ring's slot uses in order. Synchronises the model's last stream.
- * Returns the number of values written (<= capacity) or a negative error. */
+ * (trace 1) or for CTAs 1, 2, ... in order (trace 2) (nanoseconds,
+ * %globaltimer; 0 = stage start, 1 after the GEMV prologue, 2 after its
+ * weight pass, 3 after its epilogues, 4 and 5 around the first weight task's
+ * ring wait, 6 after that task's dot products, 7 = stage end; unused marks
+ * keep older values); then, for CTA 0, 4096 pairs (issue, ready) of the weight ring's
+ * slot uses in order. Synchronises the model's last stream. Returns the
+ * number of values written (<= capacity) or a negative error. */
 int qtts_frame_trace(qtts_model* m, uint64_t* host, int capacity);
 
 /* Bytes of weights one frame streams (the roofline's numerator, without KV):
