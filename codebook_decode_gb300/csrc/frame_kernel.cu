@@ -648,12 +648,26 @@ constexpr int kRingSlots = 8;
 constexpr int kSlotBytes = 16384;     // whole weight rows, one bulk copy per slot
 static_assert(kWorkBytes + kTailBytes + kRingSlots * kSlotBytes <= kSmemBytes, "shared-memory plan");
 
+// Ring-path epilogue operands, loaded in the prologue while the input words
+// are polled (the ring path leaves `part` unused)
+struct EpiCache {
+  float cs[8][64];             // RoPE cos / sin at each tile row's position (d <= 128)
+  float sn[8][64];
+  int page[8];                 // Talker: KV page of each tile row's appended position
+  float scale[2][128];         // int8 row scales of this CTA's share, per segment
+};
+constexpr int kScaleCache = 128;
+
 struct GemvSmemTail {
   float rfac[8];               // 1/rms of the tile's rows (1 without a norm)
   float sqw[8][kWarps];        // per-warp sum-of-squares partials of the tile's rows
-  float part[kPartFloats];     // phase-1 partial dot products [task][U][RT]
+  union {
+    float part[kPartFloats];   // direct path: phase-1 partial dot products [task][U][RT]
+    EpiCache ec;               // ring path
+  };
   float resid[kResidFloats];   // E_RESID operands x[row][unit] [unit][RT], read in the prologue
 };
+static_assert(sizeof(EpiCache) <= kPartFloats * sizeof(float), "epilogue cache");
 static_assert(sizeof(GemvSmemTail) <= kTailBytes, "GEMV shared-memory tail");
 
 // full[x]: the slot's bytes have landed (producer arms it, the bulk copy
@@ -751,6 +765,12 @@ __device__ __forceinline__ uint16_t* talker_kv_ptr(const Globals& g, const Frame
          (((((size_t)layer * g.pool_pages + page) * 2 + kv) * g.nkv + head) * kPage + pos % kPage) * g.d;
 }
 
+// KV pool address for a page id already checked against the pool
+__device__ __forceinline__ uint16_t* kv_ptr_page(const Globals& g, int layer, int page, int pos, int kv, int head) {
+  return g.kv_pool +
+         (((((size_t)layer * g.pool_pages + page) * 2 + kv) * g.nkv + head) * kPage + pos % kPage) * g.d;
+}
+
 // Code-Predictor cache of one layer, tagged words: [session][K|V][kv head]
 // [16 positions][d/2]; K word i holds dims (i, i + d/2), V word i dims
 // (2i, 2i + 1), as two bf16.
@@ -760,8 +780,11 @@ __device__ __forceinline__ uint64_t* cp_kv_word(const Globals& g, uint64_t* laye
 }
 
 // Epilogue for one output unit (rows n0, n0+1 when U == 2) of stage row r.
-__device__ __forceinline__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& g, const FrameArgs& fa, int n0,
-                              float y0, float y1, int r, float resid, uint32_t tag) {
+// ec: the prologue's cache of RoPE factors and pages (ring path; row r of the
+// stage is row rt of the tile), or nullptr to read them from global memory.
+__device__ __forceinline__ void gemv_epilogue(const StageDesc& d, const Seg& sg, const Globals& g,
+                                              const FrameArgs& fa, int n0, float y0, float y1, int r, int rt,
+                                              float resid, uint32_t tag, const EpiCache* ec) {
   const int b = r / d.rps, p = r % d.rps;
   const int orow = out_row_of(sg, d.rps, r);
   uint64_t* out = sg.out + (size_t)orow * sg.out_stride;
@@ -779,8 +802,8 @@ __device__ __forceinline__ void gemv_epilogue(const StageDesc& d, const Seg& sg,
         const bool is_q = n0 < nq * hd;
         const int rel = is_q ? n0 : n0 - nq * hd;
         const int head = rel / hd, i = (rel % hd) / 2;
-        const float c = talker ? g.rope_cos[(size_t)pos * half + i] : g.cp_rope_cos[pos * half + i];
-        const float s = talker ? g.rope_sin[(size_t)pos * half + i] : g.cp_rope_sin[pos * half + i];
+        const float c = ec ? ec->cs[rt][i] : talker ? g.rope_cos[(size_t)pos * half + i] : g.cp_rope_cos[pos * half + i];
+        const float s = ec ? ec->sn[rt][i] : talker ? g.rope_sin[(size_t)pos * half + i] : g.cp_rope_sin[pos * half + i];
         const float o0 = y0 * c - y1 * s;
         const float o1 = y1 * c + y0 * s;
         if (is_q) {
@@ -788,7 +811,8 @@ __device__ __forceinline__ void gemv_epilogue(const StageDesc& d, const Seg& sg,
           st_ll(out + head * hd + i + half, o1, tag);
         } else if (talker) {
           const uint16_t k0 = f2bf(o0), k1 = f2bf(o1);
-          uint16_t* kp = talker_kv_ptr(g, fa, d.layer, b, pos, 0, head);
+          uint16_t* kp = ec ? kv_ptr_page(g, d.layer, ec->page[rt], pos, 0, head)
+                            : talker_kv_ptr(g, fa, d.layer, b, pos, 0, head);
           kp[i] = k0;
           kp[i + half] = k1;
           uint64_t* kc = d.kvcur + (((size_t)b * 2 + 0) * nkv + head) * hd;
@@ -803,7 +827,8 @@ __device__ __forceinline__ void gemv_epilogue(const StageDesc& d, const Seg& sg,
         const int head = rel / hd, e = rel % hd;
         const uint16_t v0 = f2bf(y0), v1 = f2bf(y1);
         if (talker) {
-          uint16_t* vp = talker_kv_ptr(g, fa, d.layer, b, pos, 1, head);
+          uint16_t* vp = ec ? kv_ptr_page(g, d.layer, ec->page[rt], pos, 1, head)
+                            : talker_kv_ptr(g, fa, d.layer, b, pos, 1, head);
           vp[e] = v0;
           vp[e + 1] = v1;
           st_ll2(d.kvcur + (((size_t)b * 2 + 1) * nkv + head) * hd + e, bf2f(v0), bf2f(v1), tag);
@@ -858,15 +883,19 @@ struct Raw8<int8_t> {
   }
 };
 
-// One task's partial dot products: U rows x up to 1024 of K against nr
-// activation rows, from registers already holding the weight vectors.
-template <typename WT, int U, int RT>
-__device__ __forceinline__ void task_fma(const typename Raw8<WT>::T (&raw)[kSub][U], const float* xs, int K, int kb,
-                                         int nr, float (&acc)[U][RT]) {
+template <int U, int RT>
+__device__ __forceinline__ void zero_acc(float (&acc)[U][RT]) {
 #pragma unroll
   for (int i = 0; i < U; ++i)
 #pragma unroll
     for (int r = 0; r < RT; ++r) acc[i][r] = 0.f;
+}
+
+// Add one task's dot products to acc: U rows x up to 1024 of K against nr
+// activation rows, from registers already holding the weight vectors.
+template <typename WT, int U, int RT>
+__device__ __forceinline__ void task_fma(const typename Raw8<WT>::T (&raw)[kSub][U], const float* xs, int K, int kb,
+                                         int nr, float (&acc)[U][RT]) {
 #pragma unroll
   for (int sb = 0; sb < kSub; ++sb) {
     const int k = kb + sb * 256;
@@ -906,44 +935,49 @@ __device__ __forceinline__ void task_fma(const typename Raw8<WT>::T (&raw)[kSub]
 // the partials in K order, scales by 1/rms and runs the epilogue. Each phase
 // is its own small function, so the code a stage runs stays in the
 // instruction cache from one layer to the next.
+// Ring path (few activation rows): each warp takes whole output units of the
+// CTA's share, streams every K-chunk of the unit from its ring slot into
+// register accumulators, reduces once across lanes and runs the epilogue
+// itself (lane r for activation row r): no partials in shared memory, no
+// second pass. The warp that finishes a slot's last unit frees the slot.
 template <typename WT, int U, int RT>
-__device__ void gemv_p1_ring(const Seg& sg, int K, const Globals& g, const float* xs, int nr,
-                                          GemvSmemTail* tail, unsigned char* smem, Ring* ring, uint32_t q) {
+__device__ void gemv_ring(const StageDesc& d, const Seg& sg, int si, const SegShare& sh, const Globals& g,
+                          const FrameArgs& fa, const float* xs, int r0, int nr, GemvSmemTail* tail,
+                          unsigned char* smem, Ring* ring, uint32_t q, uint32_t tag) {
   using R = Raw8<WT>;
-  const SegShare sh(sg, K);
-  const int ntask = sh.nu * sh.nkc;
+  const int K = d.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t nsl = (uint32_t)g.ring_slots;
-  // tasks go round-robin over the warps; the warp that finishes a slot's
-  // last task frees the slot
-  for (int t = warp; t < ntask; t += kCWarps) {
-    const int ul = t / sh.nkc, kc = t - ul * sh.nkc;
+  const uint32_t nsl = (uint32_t)g.ring_slots, nsl_shift = (uint32_t)(__ffs(g.ring_slots) - 1);
+  for (int ul = warp; ul < sh.nu; ul += kCWarps) {
     const int sl = ul / sh.upslot;
     const int ua = sl * sh.upslot;
-    const int slot_tasks = (min(sh.nu, ua + sh.upslot) - ua) * sh.nkc;
     const uint32_t qq = q + (uint32_t)sl;
-    const int slot = (int)(qq % nsl);
+    const int slot = (int)(qq & (nsl - 1u));
     // a failed wait (time limit or an error elsewhere) leaves zeros and the
     // warp carries on to every CTA barrier; the frame is abandoned after
     // the stage
-    if (t == 0) trace_mark(g, 4);
-    const bool got = ring_wait_full(ring, slot, qq / nsl, g.err);
-    if (t == 0) trace_mark(g, 5);
-    if (lane == 0 && kc == 0 && ul == ua) trace_ring(g, qq, 1);
+    if (ul == 0) trace_mark(g, 4);
+    const bool got = ring_wait_full(ring, slot, qq >> nsl_shift, g.err);
+    if (ul == 0) trace_mark(g, 5);
+    if (lane == 0 && ul == ua) trace_ring(g, qq, 1);
     const WT* rowp = (const WT*)ring_slot(smem, slot) + (size_t)(ul - ua) * U * K;
-    const int kb = kc * kKChunk + lane * 8;
-    typename R::T raw[kSub][U];
-#pragma unroll
-    for (int sb = 0; sb < kSub; ++sb)
-#pragma unroll
-      for (int i = 0; i < U; ++i)
-        raw[sb][i] = (got && kb + sb * 256 < K) ? R::lds(rowp + (size_t)i * K + kb + sb * 256) : typename R::T{};
     float acc[U][RT];
-    task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
+    zero_acc(acc);
+    for (int kc = 0; kc < sh.nkc; ++kc) {
+      const int kb = kc * kKChunk + lane * 8;
+      typename R::T raw[kSub][U];
+#pragma unroll
+      for (int sb = 0; sb < kSub; ++sb)
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+          raw[sb][i] = (got && kb + sb * 256 < K) ? R::lds(rowp + (size_t)i * K + kb + sb * 256) : typename R::T{};
+      task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
+    }
     __syncwarp();
-    if (t == 0) trace_mark(g, 6);
+    if (ul == 0) trace_mark(g, 6);
     if (lane == 0 && got) {
-      if (atomicAdd(&ring->done[slot], 1u) + 1u == (uint32_t)slot_tasks) {
+      const int slot_units = min(sh.nu, ua + sh.upslot) - ua;
+      if (atomicAdd(&ring->done[slot], 1u) + 1u == (uint32_t)slot_units) {
         ring->done[slot] = 0u;
         mbar_arrive(&ring->empty[slot]);
       }
@@ -951,10 +985,34 @@ __device__ void gemv_p1_ring(const Seg& sg, int K, const Globals& g, const float
 #pragma unroll
     for (int i = 0; i < U; ++i)
 #pragma unroll
-      for (int r = 0; r < RT; ++r) {
-        const float v = warp_sum(acc[i][r]);
-        if (lane == 0) tail->part[(t * U + i) * RT + r] = v;
+      for (int r = 0; r < RT; ++r) acc[i][r] = warp_sum(acc[i][r]);
+    if (lane < nr) {
+      const int n0 = (sh.u0 + ul) * U;
+      float y[U];
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        float v = acc[i][0];
+#pragma unroll
+        for (int r = 1; r < RT; ++r)
+          if (lane == r) v = acc[i][r];
+        v *= tail->rfac[lane];
+        if (sg.scale) v *= ul * U + i < kScaleCache ? tail->ec.scale[si][ul * U + i] : sg.scale[n0 + i];
+        y[i] = v;
       }
+      gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + lane, lane, tail->resid[ul * RT + lane], tag, &tail->ec);
+    }
+  }
+}
+
+template <typename WT, int U>
+__device__ void gemv_ring_rt(int RT, const StageDesc& d, const Seg& sg, int si, const SegShare& sh, const Globals& g,
+                             const FrameArgs& fa, const float* xs, int r0, int nr, GemvSmemTail* tail,
+                             unsigned char* smem, Ring* ring, uint32_t q, uint32_t tag) {
+  switch (RT) {
+    case 1: gemv_ring<WT, U, 1>(d, sg, si, sh, g, fa, xs, r0, nr, tail, smem, ring, q, tag); break;
+    case 2: gemv_ring<WT, U, 2>(d, sg, si, sh, g, fa, xs, r0, nr, tail, smem, ring, q, tag); break;
+    case 4: gemv_ring<WT, U, 4>(d, sg, si, sh, g, fa, xs, r0, nr, tail, smem, ring, q, tag); break;
+    default: gemv_ring<WT, U, 8>(d, sg, si, sh, g, fa, xs, r0, nr, tail, smem, ring, q, tag); break;
   }
 }
 
@@ -977,6 +1035,7 @@ __device__ void gemv_p1_direct(const Seg& sg, int K, const float* xs, int nr, Ge
       for (int i = 0; i < U; ++i) raw[sb][i] = (k < K) ? R::load(W + (size_t)(n0 + i) * K + k) : typename R::T{};
     }
     float acc[U][RT];
+    zero_acc(acc);
     task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
 #pragma unroll
     for (int i = 0; i < U; ++i)
@@ -1003,23 +1062,19 @@ __device__ void gemv_p2(const StageDesc& d, const Seg& sg, const Globals& g, con
       acc *= f;
       y[i] = sg.scale ? acc * sg.scale[n0 + i] : acc;
     }
-    gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + r, tail->resid[ul * RT + r], tag);
+    gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + r, r, tail->resid[ul * RT + r], tag, nullptr);
   }
 }
 
-// Phase 1 of one segment: the variant for the weight type, unit and tile height.
-__device__ void gemv_p1(const Seg& sg, int K, int RT, bool use_ring, const Globals& g, const float* xs, int nr,
-                        GemvSmemTail* tail, unsigned char* smem, Ring* ring, uint32_t q) {
-#define QTTS_P1(WT_, U_, RT_)                                                        \
-  if (use_ring) gemv_p1_ring<WT_, U_, RT_>(sg, K, g, xs, nr, tail, smem, ring, q); \
-  else gemv_p1_direct<WT_, U_, RT_>(sg, K, xs, nr, tail);                          \
-  return;
-#define QTTS_P1_RT(WT_, U_)       \
-  switch (RT) {                   \
-    case 1: QTTS_P1(WT_, U_, 1)   \
-    case 2: QTTS_P1(WT_, U_, 2)   \
-    case 4: QTTS_P1(WT_, U_, 4)   \
-    default: QTTS_P1(WT_, U_, 8)  \
+// Phase 1 of one segment on the direct path: the variant for the weight
+// type, unit and tile height.
+__device__ void gemv_p1(const Seg& sg, int K, int RT, const float* xs, int nr, GemvSmemTail* tail) {
+#define QTTS_P1_RT(WT_, U_)                                           \
+  switch (RT) {                                                       \
+    case 1: gemv_p1_direct<WT_, U_, 1>(sg, K, xs, nr, tail); return;  \
+    case 2: gemv_p1_direct<WT_, U_, 2>(sg, K, xs, nr, tail); return;  \
+    case 4: gemv_p1_direct<WT_, U_, 4>(sg, K, xs, nr, tail); return;  \
+    default: gemv_p1_direct<WT_, U_, 8>(sg, K, xs, nr, tail); return; \
   }
   if (sg.scale) {
     if (sg.unit == 2) { QTTS_P1_RT(int8_t, 2) }
@@ -1029,7 +1084,44 @@ __device__ void gemv_p1(const Seg& sg, int K, int RT, bool use_ring, const Globa
     else { QTTS_P1_RT(uint16_t, 1) }
   }
 #undef QTTS_P1_RT
-#undef QTTS_P1
+}
+
+// One warp loads the ring-path epilogue operands of a row tile: RoPE factors
+// and KV pages of the rows' positions (QKV stages) and the int8 row scales of
+// the CTA's share.
+__device__ void fill_epi_cache(const StageDesc& d, const Globals& g, const FrameArgs& fa, int r0, int nr, int K,
+                               EpiCache* ec) {
+  const int lane = threadIdx.x & 31;
+  const Seg& s0 = d.seg[0];
+  if (s0.epi == E_QKV_T || s0.epi == E_QKV_CP) {
+    const bool talker = s0.epi == E_QKV_T;
+    const int half = (talker ? g.d : g.dc) / 2;
+    for (int r = 0; r < nr; ++r) {
+      const int b = (r0 + r) / d.rps, p = (r0 + r) % d.rps;
+      const int pos = talker ? s_kv_len[b] : d.pos_base + p;
+      const float* cs = talker ? g.rope_cos + (size_t)pos * half : g.cp_rope_cos + pos * half;
+      const float* sn = talker ? g.rope_sin + (size_t)pos * half : g.cp_rope_sin + pos * half;
+      for (int i = lane; i < half; i += 32) {
+        ec->cs[r][i] = cs[i];
+        ec->sn[r][i] = sn[i];
+      }
+      if (talker && lane == 0) {
+        int page = fa.bt[(size_t)b * fa.bt_stride + pos / kPage];
+        if (page < 0 || page >= g.pool_pages) {  // validated in stage_begin; stay in bounds regardless
+          set_err(g.err, QTTS_DEV_BAD_PAGE);
+          page = 0;
+        }
+        ec->page[r] = page;
+      }
+    }
+  }
+  for (int si = 0; si < d.nseg; ++si) {
+    const Seg& sg = d.seg[si];
+    if (!sg.scale) continue;
+    const SegShare sh(sg, K);
+    const int n = min(sh.nu * sg.unit, kScaleCache);
+    for (int i = lane; i < n; i += 32) ec->scale[si][i] = sg.scale[sh.u0 * sg.unit + i];
+  }
 }
 
 // q: this CTA's count of ring tasks consumed so far (advanced here).
@@ -1074,6 +1166,7 @@ __device__ bool stage_gemv(const StageDesc& d, uint32_t tag, const Globals& g, c
         rw[u] = ld_ll(rp[u]);
       }
     }
+    if (use_ring && warp == kCWarps - 1) fill_epi_cache(d, g, fa, r0, nr, K, &tail->ec);
     {
       constexpr int NB = 4;
       const int npair = nr * K / 2;
@@ -1143,15 +1236,31 @@ __device__ bool stage_gemv(const StageDesc& d, uint32_t tag, const Globals& g, c
     }
     for (int s = 0; s < d.nseg; ++s) {
       const Seg& sg = d.seg[s];
-      gemv_p1(sg, K, RT, use_ring, g, xs, nr, tail, smem, ring, q);
-      cbar();
-      trace_mark(g, 2);
+      const SegShare sh = s == 0 ? sh0 : SegShare(sg, K);
       // the next descriptor is fetched once, in the last segment of the last row tile
-      if (next && s == d.nseg - 1 && r0 + RT >= rows && warp == kCWarps - 1) fetch_desc(next, next_s);
-      gemv_p2(d, sg, g, fa, r0, nr, RT, tail, tag);
-      cbar();
-      trace_mark(g, 3);
-      if (use_ring) q += (uint32_t)SegShare(sg, K).nslot;
+      const bool fetch = next && s == d.nseg - 1 && r0 + RT >= rows;
+      if (use_ring) {
+        if (fetch && warp == kCWarps - 1) fetch_desc(next, next_s);
+        if (sg.scale) {
+          if (sg.unit == 2) gemv_ring_rt<int8_t, 2>(RT, d, sg, s, sh, g, fa, xs, r0, nr, tail, smem, ring, q, tag);
+          else gemv_ring_rt<int8_t, 1>(RT, d, sg, s, sh, g, fa, xs, r0, nr, tail, smem, ring, q, tag);
+        } else {
+          if (sg.unit == 2) gemv_ring_rt<uint16_t, 2>(RT, d, sg, s, sh, g, fa, xs, r0, nr, tail, smem, ring, q, tag);
+          else gemv_ring_rt<uint16_t, 1>(RT, d, sg, s, sh, g, fa, xs, r0, nr, tail, smem, ring, q, tag);
+        }
+        q += (uint32_t)sh.nslot;
+        cbar();
+        trace_mark(g, 2);
+        trace_mark(g, 3);
+      } else {
+        gemv_p1(sg, K, RT, xs, nr, tail);
+        cbar();
+        trace_mark(g, 2);
+        if (fetch && warp == kCWarps - 1) fetch_desc(next, next_s);
+        gemv_p2(d, sg, g, fa, r0, nr, RT, tail, tag);
+        cbar();
+        trace_mark(g, 3);
+      }
     }
   }
   return true;
@@ -1327,7 +1436,7 @@ __device__ bool attn_fetch_fold(AttnTile& T, const uint16_t* ksrc, const uint16_
     bulk_load(T.k, ksrc, bytes, &T.bar, policy);
     bulk_load(T.v, vsrc, bytes, &T.bar, policy);
   }
-  const bool ok = mbar_wait(&T.bar, parity, err);
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&T.bar, parity, err));  // one verdict per warp
   parity ^= 1u;
   if (ok) {
     if (cur_row >= 0) {
@@ -1611,14 +1720,141 @@ __device__ bool stage_attn_cp(const StageDesc& d, uint32_t tag, const Globals& g
   return ok;
 }
 
+// Talker attention for few, short sessions: one CTA per (session, kv head).
+// Its attention warps take the 16-position tiles round-robin (each tile by
+// TMA bulk copy, the newest position from the tagged K/V rows), then the
+// CTA combines the warps' partial softmax states in shared memory, in warp
+// order. No cross-CTA split, so no partials in global memory, fences or
+// arrival counters.
+constexpr int kCtaAttnMaxTiles = 4 * kAttnWarps;  // contexts up to 512 positions take this path
+
+template <int HD, int GRP>
+__device__ bool stage_attn_talker_cta(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+                                      unsigned char* smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int E = HD / 32;
+  constexpr int NQ = GRP * HD / 64;  // q word pairs per lane
+  constexpr int NC = HD / 64;        // current K (and V) word pairs per lane
+  constexpr int PS = HD + 2;         // one partial: m, l, o[HD]
+  const int nkv = g.nkv;
+  const int qstride = d.q_stride;
+  const uint32_t tag_in = fa.tag0 + (uint32_t)d.q_ws;
+  const float scale = rsqrtf((float)HD);
+  AttnTile* tiles = reinterpret_cast<AttnTile*>(smem);
+  float* part = reinterpret_cast<float*>(smem + kWorkBytes);  // [kAttnWarps][GRP][PS]
+  static_assert(kAttnWarps * GRP * PS * sizeof(float) <= kTailBytes, "attention partials");
+  if (warp < kAttnWarps && lane == 0) {
+    mbar_init(&tiles[warp].bar, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  uint32_t parity = 0;
+  bool ok = true;
+  for (int item = blockIdx.x; item < fa.B * nkv; item += g.G) {  // the same trip count on every warp
+    const int b = item / nkv, kvh = item - (item / nkv) * nkv;
+    const int len = s_kv_len[b] + 1, cur = len - 1;
+    const int ntile = (len + kPage - 1) / kPage;
+    if (warp < kAttnWarps) {
+      AttnTile& T = tiles[warp];
+      AttnAcc<HD, GRP> A;
+      attn_init(A);
+      ok = __all_sync(0xffffffffu, ok);
+      if (warp < ntile && ok) {
+        const bool has_cur = (ntile - 1) % kAttnWarps == warp;  // this warp folds the last tile
+        const uint64_t* qsrc = d.q + (size_t)b * qstride + kvh * GRP * HD;
+        const uint64_t* kc = d.kvcur + (((size_t)b * 2 + 0) * nkv + kvh) * HD;
+        const uint64_t* vc = d.kvcur + (((size_t)b * 2 + 1) * nkv + kvh) * HD;
+        uint64_t qw[NQ][2], kw[NC][2], vw[NC][2];
+        const uint64_t *pq[NQ], *pk[NC], *pv[NC];
+        uint32_t tq[NQ], tk[NC];
+#pragma unroll
+        for (int u = 0; u < NQ; ++u) {
+          pq[u] = qsrc + 2 * (lane + 32 * u);
+          tq[u] = tag_in;
+          ld_ll2(pq[u], qw[u][0], qw[u][1]);
+        }
+#pragma unroll
+        for (int u = 0; u < NC; ++u) {
+          kw[u][0] = kw[u][1] = vw[u][0] = vw[u][1] = 0;
+          pk[u] = has_cur ? kc + 2 * (lane + 32 * u) : nullptr;
+          pv[u] = has_cur ? vc + 2 * (lane + 32 * u) : nullptr;
+          tk[u] = tag_in;
+          if (has_cur) {
+            ld_ll2(pk[u], kw[u][0], kw[u][1]);
+            ld_ll2(pv[u], vw[u][0], vw[u][1]);
+          }
+        }
+        ok &= ll_settle<NQ>(pq, tq, qw, g.err);
+        ok &= ll_settle<NC>(pk, tk, kw, g.err);
+        ok &= ll_settle<NC>(pv, tk, vw, g.err);
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < NQ; ++u) {
+          const int c = 2 * (lane + 32 * u);
+          T.q[c] = ll_val(qw[u][0]);
+          T.q[c + 1] = ll_val(qw[u][1]);
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        for (int t = warp; t < ntile && ok; t += kAttnWarps) {
+          const int pt = t * kPage;
+          ok = attn_fetch_fold<HD, GRP>(T, talker_kv_ptr(g, fa, d.layer, b, pt, 0, kvh),
+                                        talker_kv_ptr(g, fa, d.layer, b, pt, 1, kvh), min(kPage, len - pt), scale,
+                                        parity, g.err, A, t == ntile - 1 ? cur - pt : -1, kw, vw);
+        }
+      }
+      float* pw = part + (size_t)warp * GRP * PS;
+#pragma unroll
+      for (int j = 0; j < GRP; ++j) {
+        if (lane == 0) {
+          pw[j * PS] = A.m[j];
+          pw[j * PS + 1] = A.l[j];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) pw[j * PS + 2 + lane * E + e] = A.o[j][e];
+      }
+    }
+    cbar();
+    const int nw = min(ntile, kAttnWarps);
+    uint64_t* out = d.attn_out + (size_t)b * qstride + kvh * GRP * HD;
+    for (int idx = threadIdx.x; idx < GRP * HD; idx += kCThreads) {
+      const int j = idx / HD, e = idx - j * HD;
+      float M = -INFINITY;
+      for (int w = 0; w < nw; ++w) M = fmaxf(M, part[(w * GRP + j) * PS]);
+      float L = 0.f, o = 0.f;
+      for (int w = 0; w < nw; ++w) {
+        const float* pw = part + (w * GRP + j) * PS;
+        const float wt = expf(pw[0] - M);
+        L = fmaf(wt, pw[1], L);
+        o = fmaf(wt, pw[2 + e], o);
+      }
+      st_ll(out + idx, o / L, tag);
+    }
+    cbar();  // the tiles and partials are reused by the next item
+  }
+  __syncwarp();
+  if (warp < kAttnWarps && lane == 0) mbar_inval(&tiles[warp].bar);
+  return ok;
+}
+
+// The CTA-per-head path when every (session, kv head) gets its own CTA in
+// one round and the longest context fits its tiles; else the split path.
+__device__ __forceinline__ bool talker_attn_by_cta(const Globals& g, const FrameArgs& fa) {
+  if (fa.B * g.nkv > g.G) return false;
+  int longest = 0;
+  for (int b = 0; b < fa.B; ++b) longest = max(longest, s_kv_len[b] + 1);
+  return (longest + kPage - 1) / kPage <= kCtaAttnMaxTiles;
+}
+
 template <bool TALKER>
 __device__ bool stage_attn(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
                            unsigned char* smem) {
   const int hd = TALKER ? g.d : g.dc;
   const int grp = TALKER ? g.nq / g.nkv : g.nqc / g.nkvc;
-#define QTTS_ATTN_CASE(H_, G_)                                           \
-  if (hd == H_ && grp == G_)                                             \
-    return TALKER ? stage_attn_talker<H_, G_>(d, tag, g, fa, smem)       \
+  const bool by_cta = TALKER && talker_attn_by_cta(g, fa);
+#define QTTS_ATTN_CASE(H_, G_)                                                                  \
+  if (hd == H_ && grp == G_)                                                                    \
+    return TALKER ? (by_cta ? stage_attn_talker_cta<H_, G_>(d, tag, g, fa, smem)                \
+                            : stage_attn_talker<H_, G_>(d, tag, g, fa, smem))                   \
                   : stage_attn_cp<H_, G_>(d, tag, g, fa, smem);
   QTTS_ATTN_CASE(128, 2)
   QTTS_ATTN_CASE(64, 2)

@@ -1061,7 +1061,8 @@ int qtts_set_option(qtts_model* m, int option, int value) {
     return QTTS_OK;
   }
   if (option == QTTS_OPT_RING_SLOTS) {
-    if (value < 1 || value > 8) return fail(m, QTTS_E_INVALID, "ring slots must be 1..8");
+    if (value != 1 && value != 2 && value != 4 && value != 8)
+      return fail(m, QTTS_E_INVALID, "ring slots must be 1, 2, 4 or 8");
     m->g.ring_slots = value;
     return QTTS_OK;
   }

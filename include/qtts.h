@@ -257,8 +257,8 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
  *   QTTS_OPT_TRACE     1: record %globaltimer stamps inside every stage on
  *                      the first and last CTA (qtts_frame_trace); 2: on
  *                      every CTA. 0 (default): off.
- *   QTTS_OPT_RING_SLOTS 1..8: 16 KB weight slots per SM the producer warp may
- *                      fill ahead of the compute warps. Default 8. */
+ *   QTTS_OPT_RING_SLOTS 1, 2, 4 or 8: 16 KB weight slots per SM the producer
+ *                      warp may fill ahead of the compute warps. Default 8. */
 #define QTTS_OPT_STEPWISE 1
 #define QTTS_OPT_TRACE 3
 #define QTTS_OPT_RING_SLOTS 4
