@@ -137,6 +137,33 @@ __device__ __forceinline__ bool ll_get(const uint64_t* p, uint32_t tag, uint64_t
   return ll_ok(w, tag);
 }
 
+// ll_settle for N pairs at base + u * stride (u < n), all with one tag.
+template <int N>
+__device__ __forceinline__ bool ll_settle_strided(const uint64_t* base, int stride, int n, uint32_t tag,
+                                                  uint64_t (&w)[N][2], int* err) {
+  bool all = true;
+#pragma unroll
+  for (int u = 0; u < N; ++u)
+    if (u < n) all &= ll_ok(w[u][0], tag) & ll_ok(w[u][1], tag);
+  if (all) return true;
+  const uint64_t t0 = global_timer_ns();
+  unsigned spins = 0;
+  for (;;) {
+    all = true;
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+      if (u < n && !(ll_ok(w[u][0], tag) & ll_ok(w[u][1], tag))) {
+        ld_ll2(base + (size_t)u * stride, w[u][0], w[u][1]);
+        all = false;
+      }
+    if (all) return true;
+    if ((++spins & 15u) == 0u && (read_err(err) || global_timer_ns() - t0 > kWaitTimeoutNs)) {
+      if (!read_err(err)) set_err(err, QTTS_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Wait until both words of every pair ps[u] (u < N, ps[u] != nullptr) carry
 // tag t[u]; w holds the first reads. Every pass re-reads all pairs still
 // pending at once, so a late batch costs one round trip per pass, not one per
@@ -275,6 +302,57 @@ __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
     }
   }
   return true;
+}
+
+// ---- 5th-generation tensor cores: tcgen05 MMA with TMEM accumulators ----
+// Operands sit in shared memory in the canonical K-major layout without
+// swizzle: 8 rows x 16 bytes per core matrix, `lbo` bytes between core
+// matrices along K, `sbo` bytes between them along M (or N).
+
+__device__ __forceinline__ uint64_t tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);  // descriptor version 1, no swizzle
+}
+// kind::f16 instruction: fp32 accumulator, bf16 A and B, both K-major, M x N
+__host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc)
+      : "memory");
+}
+// arrive once on `bar` when every MMA this thread issued so far has completed
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+constexpr uint32_t kTmemCols = 128;  // the accumulator: 128 lanes (weight rows) x up to 128 columns
+// one warp
+__device__ __forceinline__ void tc_alloc(uint32_t* dst) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+               "n"(kTmemCols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t tmem) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+}
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread)
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 // ---------------------------------------------------------------------------
@@ -585,7 +663,7 @@ __device__ int sample_row(SampleSmem& S, const float* row, int V, int j, const q
 
 __shared__ int s_kv_len[kMaxBatch];  // each session's kv_len as this launch found it
 
-__device__ bool stage_begin(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa) {
+__device__ __noinline__ bool stage_begin(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa) {
   const int tid = threadIdx.x;
   int bad = 0;
   for (int b = tid; b < fa.B; b += kCThreads) {
@@ -646,7 +724,11 @@ constexpr int kPartFloats = 1536;
 constexpr int kResidFloats = 512;
 constexpr int kRingSlots = 8;
 constexpr int kSlotBytes = 16384;     // whole weight rows, one bulk copy per slot
-static_assert(kWorkBytes + kTailBytes + kRingSlots * kSlotBytes <= kSmemBytes, "shared-memory plan");
+static_assert(kWorkBytes + kTailBytes + kRingSlots * kSlotBytes + kTcOverread <= kSmemBytes, "shared-memory plan");
+// a K step's 128-lane A operand spans (the slice's two 8-column steps of K)
+// at most 16 core-matrix rows past its start: 15 x 128 + one K step of the
+// smallest (8-row) slice + 128 bytes past the slot's end
+static_assert(15 * 128 + kTcRows * 16 + 128 <= kTcOverread, "tensor-path over-read guard");
 
 // Ring-path epilogue operands, loaded in the prologue while the input words
 // are polled (the ring path leaves `part` unused)
@@ -728,6 +810,37 @@ __device__ __forceinline__ int ring_rt(const StageDesc& d, int B) {
     if (d.seg[s].unit * d.K * (d.seg[s].scale ? 1 : 2) > kSlotBytes) return 0;
   return RT;
 }
+
+// How a GEMV stage runs for batch B: ring path (few rows: CUDA-core dot
+// products from the weight ring), tensor path (8..64 rows, bf16 weights with a
+// tensor-tile copy, K a multiple of 128: tcgen05 MMAs from the weight ring),
+// else direct path (CUDA cores, weights loaded by the lanes). The producer
+// and the compute warps evaluate the same rule.
+enum GemvMode { GM_RING = 0, GM_TC = 1, GM_DIRECT = 2 };
+constexpr int kTcMinRows = 8;
+__device__ __forceinline__ int gemv_mode(const StageDesc& d, int B) {
+  const int rows = B * d.rps;
+  bool tc = rows >= kTcMinRows && rows <= 64 && d.K % kTcK == 0;
+  for (int s = 0; s < d.nseg; ++s) tc = tc && d.seg[s].wt != nullptr;
+  if (tc) return GM_TC;
+  return ring_rt(d, B) > 0 ? GM_RING : GM_DIRECT;
+}
+
+// This CTA's share of a segment on the tensor path: 16-row groups [g0, g0 + ng);
+// per 128-wide K chunk, slots of up to 4 group tiles (16 KB).
+struct TcShare {
+  int g0, rows;      // rows [8 g0, 8 g0 + rows) of the segment (rows = 0: nothing to do)
+  int kstep_bytes;   // bytes of the slice per 16-wide K step
+  int kps, nslot;    // K steps per ring slot, ring slots of the segment
+  __device__ TcShare(const Seg& sg, int K) {
+    const unsigned ngroups = (unsigned)((sg.N + kTcRows - 1) / kTcRows);
+    g0 = (int)(ngroups * blockIdx.x / gridDim.x);
+    rows = ((int)(ngroups * (blockIdx.x + 1) / gridDim.x) - g0) * kTcRows;
+    kstep_bytes = rows * 32;
+    kps = rows ? kSlotBytes / kstep_bytes : 1;
+    nslot = rows ? (K / 16 + kps - 1) / kps : 0;
+  }
+};
 
 // This CTA's share of one segment: units [u0, u0 + nu), each cut into nkc
 // K-slices (the tasks); on the ring path, slots of `upslot` whole units.
@@ -1124,11 +1237,207 @@ __device__ void fill_epi_cache(const StageDesc& d, const Globals& g, const Frame
   }
 }
 
+// Tensor-path state kept across stages in shared memory.
+struct TcState {
+  uint64_t xfree[2];  // MMAs reading X buffer b have completed
+  uint64_t done;      // every MMA of the current segment has completed
+  uint32_t tmem;      // TMEM base (kTmemCols columns)
+  uint32_t xuse;      // X-buffer fills so far (buffer = xuse & 1)
+  uint32_t nseg;      // tensor segments finished so far (phase of `done`)
+};
+
+constexpr int kTcXBytes = 32 * 1024;  // one activation buffer (a pass of 128-wide K chunks)
+static_assert(2 * kTcXBytes <= kWorkBytes, "tensor-path A tiles");
+static_assert(kTcMaxRows * 128 * 4 <= kWorkBytes, "tensor-path results");
+constexpr int kTcIssuer = kCWarps - 1;    // the warp whose lane 0 issues the MMAs
+constexpr int kTcStagers = kCWarps - 1;   // warps 0.. that stage activations
+constexpr int kTcPairs = (kTcXBytes / 4 / 2 + kTcStagers * 32 - 1) / (kTcStagers * 32);  // word pairs per stager thread per pass
+
+// Tensor path of a GEMV stage (8..64 activation rows, bf16 weights): one
+// tcgen05 MMA per 16-wide K step, M = 128 lanes holding the activation rows
+// twice, bf16 high parts (times the RMSNorm gain) in lanes 0..rows-1 and the
+// bf16 low parts x - hi in lanes rows..2 rows-1, so hi + lo carries about 16
+// mantissa bits of each fp32 activation (the other lanes read whatever follows
+// in the activation buffers and are never used), and N = this CTA's weight
+// rows (its packed slice, streamed through the ring). The accumulator stays in
+// TMEM over all of K. Stager warps fill 32 KB activation tiles (several
+// 128-wide K chunks per pass, two buffers) while the issuer's MMAs read the
+// other buffer; a commit frees each weight slot and activation buffer when its
+// MMAs are done. The epilogue adds the hi and lo lanes, applies 1/rms and runs
+// the stage's epilogue.
+__device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+                              unsigned char* smem, Ring* ring, TcState* ts, uint32_t& q) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rows = fa.B * d.rps;
+  const int K = d.K, nch = K / kTcK, nks = K / 16;
+  const bool norm = d.xsrc == X_NORM;
+  const RowMap rm{d.rps, d.in_rps, d.in_off};
+  const uint32_t nsl = (uint32_t)g.ring_slots, nsl_shift = (uint32_t)(__ffs(g.ring_slots) - 1);
+  // activation tile of one 128-wide K chunk: meff rows (hi and lo of each
+  // activation row, rounded up to 16), lbo bytes per 8-column step of K
+  const int meff = (2 * rows + 15) / 16 * 16;
+  const int lbo = meff / 8 * 128;
+  const int tile_bytes = meff * kTcK * 2;
+  const int cpp = kTcXBytes / tile_bytes;  // K chunks per pass
+  const int npass = (nch + cpp - 1) / cpp;
+  const int tpr = kTcStagers * 32 / rows;  // stager threads per activation row
+  const int srow = tid / tpr, sub = tid - srow * tpr;
+  const uint64_t* xrow = srow < rows ? d.x + (size_t)rm.in_row(srow) * d.x_stride : nullptr;
+  const uint32_t row_tag = srow < rows ? fa.tag0 + (uint32_t)d.x_ws[srow % d.rps] : 0u;
+  float* ssq = reinterpret_cast<float*>(smem + kWorkBytes);  // [kTcStagers * 32] per-thread partial sums of squares
+  bool ok = true;
+  uint32_t xuse = ts->xuse, nseg = ts->nseg;
+  for (int si = 0; si < d.nseg; ++si) {
+    const Seg& sg = d.seg[si];
+    const TcShare sh(sg, K);
+    if (sh.rows == 0) continue;  // no rows of this segment on this CTA (the same on all its threads)
+    float sq = 0.f;              // this thread's share of its row's sum of squares
+    int slot_j = -1, slot = 0;   // issuer: the weight slot in use
+    uint32_t wa = 0;
+    const uint32_t idesc = tc_idesc_bf16(128, sh.rows);
+    // Stager thread t takes activation row t / tpr and every tpr-th K pair of it.
+    for (int pass = 0; pass < npass; ++pass, ++xuse) {
+      const int b = (int)(xuse & 1u);
+      unsigned char* xb = smem + b * kTcXBytes;
+      const int c0 = pass * cpp, c1 = min(nch, c0 + cpp);
+      if (warp < kTcStagers) {
+        // the MMAs of this buffer's previous fill are done with it
+        if (xuse >= 2) ok &= mbar_wait(&ts->xfree[b], ((xuse >> 1) - 1u) & 1u, g.err);
+        const int npair = (c1 - c0) * (kTcK / 2);  // pairs of this row in the pass
+        for (int j0 = sub; j0 < npair && srow < rows; j0 += kTcPairs * tpr) {
+          uint64_t w[kTcPairs][2];
+          const int n = min(kTcPairs, (npair - j0 + tpr - 1) / tpr);  // this thread's pairs j0 + u tpr, u < n
+          const uint64_t* base = xrow + c0 * kTcK + 2 * j0;
+#pragma unroll
+          for (int u = 0; u < kTcPairs; ++u) {
+            w[u][0] = w[u][1] = 0;
+            if (u < n) ld_ll2(base + (size_t)u * 2 * tpr, w[u][0], w[u][1]);
+          }
+          ok &= ll_settle_strided<kTcPairs>(base, 2 * tpr, n, row_tag, w, g.err);
+#pragma unroll
+          for (int u = 0; u < kTcPairs; ++u) {
+            if (u >= n) continue;
+            const int j = j0 + u * tpr;
+            const int cc = (2 * j) / kTcK, kl = (2 * j) % kTcK;  // chunk within the pass, K within the chunk
+            float x0 = ll_val(w[u][0]), x1 = ll_val(w[u][1]);
+            if (norm) {
+              sq = fmaf(x0, x0, sq);
+              sq = fmaf(x1, x1, sq);
+              const uint32_t gw = __ldg(reinterpret_cast<const unsigned*>(d.gain + (c0 + cc) * kTcK + kl));
+              x0 *= bf_lo(gw);
+              x1 *= bf_hi(gw);
+            }
+            const uint16_t h0 = f2bf(x0), h1 = f2bf(x1);
+            const uint16_t l0 = f2bf(x0 - bf2f(h0)), l1 = f2bf(x1 - bf2f(h1));
+            // element (m, k) of a chunk tile: core matrix (k/8, m/8) at (k/8) lbo + (m/8) 128, row m%8, column k%8
+            unsigned char* ct = xb + cc * tile_bytes + (kl >> 3) * lbo + (kl & 7) * 2;
+            *reinterpret_cast<uint32_t*>(ct + (srow >> 3) * 128 + (srow & 7) * 16) = h0 | ((uint32_t)h1 << 16);
+            const int lr = rows + srow;
+            *reinterpret_cast<uint32_t*>(ct + (lr >> 3) * 128 + (lr & 7) * 16) = l0 | ((uint32_t)l1 << 16);
+          }
+        }
+        fence_proxy_async_smem();  // the activation tiles are read by the tensor cores (async proxy)
+      }
+      cbar();
+      if (pass == 0) trace_mark(g, 1);
+      if (warp == kTcIssuer && lane == 0) {
+        tc_fence_after();
+        // activation K step cs of the pass starts at xb + 2 cs lbo (a chunk tile is 16 lbo bytes)
+        const int s_end = c1 * (kTcK / 16);
+        for (int s = c0 * (kTcK / 16); s < s_end;) {
+          const int j = s / sh.kps;
+          if (j != slot_j) {  // next weight slot
+            slot_j = j;
+            const uint32_t qq = q + (uint32_t)j;
+            slot = (int)(qq & (nsl - 1u));
+            ok &= ring_wait_full(ring, slot, qq >> nsl_shift, g.err);
+            trace_ring(g, qq, 1);
+            wa = smem_addr(ring_slot(smem, slot));
+          }
+          const int slot_end = min(nks, (j + 1) * sh.kps);
+          const int e = min(s_end, slot_end);
+          uint64_t da = tc_smem_desc(smem_addr(xb) + (uint32_t)((s - c0 * (kTcK / 16)) * 2 * lbo), lbo, 128);
+          uint64_t db = tc_smem_desc(wa + (uint32_t)((s - j * sh.kps) * sh.kstep_bytes), sh.rows * 16, 128);
+          const uint64_t da_step = (uint64_t)((2 * lbo) >> 4), db_step = (uint64_t)(sh.kstep_bytes >> 4);
+          for (; s < e; ++s) {  // descriptors advance in their 16-byte address field
+            tc_mma(ts->tmem, da, db, idesc, s > 0);
+            da += da_step;
+            db += db_step;
+          }
+          if (s == slot_end) tc_commit(&ring->empty[slot]);  // the slot is free once these MMAs are done
+        }
+        tc_commit(&ts->xfree[b]);
+        if (pass == npass - 1) tc_commit(&ts->done);
+      }
+      __syncwarp();
+    }
+    q += (uint32_t)sh.nslot;
+    // all MMAs of the segment are done: read the accumulators
+    ok &= mbar_wait(&ts->done, nseg & 1u, g.err);
+    ++nseg;
+    trace_mark(g, 2);
+    tc_fence_after();
+    float* res = reinterpret_cast<float*>(smem);  // [lane: hi rows, lo rows][slice row], over the activation tiles
+    if (warp < 4 && 32 * warp < 2 * rows) {
+      const int m = 32 * warp + lane;  // TMEM lane
+      for (int cb = 0; cb < sh.rows / 16; ++cb) {
+        float v[16];
+        tc_ld16(ts->tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(cb * 16), v);
+        if (m < 2 * rows)
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) res[m * sh.rows + cb * 16 + jj] = v[jj];
+      }
+    }
+    tc_fence_before();
+    if (norm && warp < kTcStagers) ssq[tid] = sq;
+    if (cbar_or(!ok)) return false;
+    // epilogue: one thread per (unit, activation row)
+    const int U = sg.unit;
+    const int nunits = sh.rows / U;
+    for (int idx = tid; idx < nunits * rows; idx += kCThreads) {
+      const int ul = idx / rows, r = idx - ul * rows;
+      const int n0 = sh.g0 * kTcRows + ul * U;
+      if (n0 >= sg.N) continue;  // padding rows of the last group
+      float f = 1.0f;
+      if (norm) {  // the row's partial sums, in thread order
+        float t = 0.f;
+        for (int i = 0; i < tpr; ++i) t += ssq[r * tpr + i];
+        f = 1.0f / sqrtf(t / (float)K + g.eps);
+      }
+      float y[2];
+      for (int i = 0; i < U; ++i) {
+        const int col = ul * U + i;
+        y[i] = (res[r * sh.rows + col] + res[(rows + r) * sh.rows + col]) * f;
+      }
+      float resid = 0.f;
+      if (sg.epi == E_RESID) {
+        const uint64_t* p = sg.resid + (size_t)out_row_of(sg, d.rps, r) * sg.out_stride + n0;
+        uint64_t w = ld_ll(p);
+        ok &= ll_get(p, fa.tag0 + (uint32_t)sg.r_ws[r % d.rps], w, g.err);
+        resid = ll_val(w);
+      }
+      gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r, r, resid, tag, nullptr);
+    }
+    cbar();  // the results are read; the next fill may overwrite them
+    trace_mark(g, 3);
+  }
+  if (tid == 0) {
+    ts->xuse = xuse;
+    ts->nseg = nseg;
+  }
+  return ok;
+}
+
 // q: this CTA's count of ring tasks consumed so far (advanced here).
 // next / next_s: the following stage's descriptor (or nullptr) and its
 // shared-memory buffer, filled by the last compute warp during phase 2.
-__device__ bool stage_gemv(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
-                           unsigned char* smem, Ring* ring, uint32_t& q, const StageDesc* next, StageDesc* next_s) {
+__device__ __noinline__ bool stage_gemv(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+                           unsigned char* smem, Ring* ring, TcState* ts, uint32_t& q, const StageDesc* next,
+                           StageDesc* next_s) {
+  if (gemv_mode(d, fa.B) == GM_TC) {
+    if (next && (threadIdx.x >> 5) == kCWarps - 2) fetch_desc(next, next_s);
+    return stage_gemv_tc(d, tag, g, fa, smem, ring, ts, q);
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rows = fa.B * d.rps;
   const int K = d.K;
@@ -1279,8 +1588,30 @@ __device__ void producer(const StageDesc* prog, int s0, int s1, const Globals& g
   bool ok = true;
   for (int s = s0; s < s1 && ok; ++s) {
     const StageDesc& d = prog[s];
-    if (d.type != ST_GEMV || ring_rt(d, fa.B) == 0) continue;
+    if (d.type != ST_GEMV) continue;
+    const int mode = gemv_mode(d, fa.B);
+    if (mode == GM_DIRECT) continue;
     const int K = d.K;
+    if (mode == GM_TC) {
+      for (int si = 0; si < d.nseg && ok; ++si) {
+        const TcShare sh(d.seg[si], K);
+        const unsigned char* W = (const unsigned char*)d.seg[si].wt + (size_t)sh.g0 * kTcRows * K * 2;
+        const int nks = K / 16;
+        for (int j = 0; j < sh.nslot; ++j, ++q) {
+          const uint32_t bytes = (uint32_t)(min(nks, (j + 1) * sh.kps) - j * sh.kps) * sh.kstep_bytes;
+          const int slot = (int)(q % nsl);
+          if (!mbar_wait(&ring->empty[slot], ((q / nsl) & 1u) ^ 1u, g.err)) {
+            ok = false;
+            break;
+          }
+          trace_ring(g, q, 0);
+          *(volatile uint32_t*)&ring->seq[slot] = q / nsl;
+          mbar_arrive_expect_tx(&ring->full[slot], bytes);
+          bulk_load(ring_slot(smem, slot), W + (size_t)j * sh.kps * sh.kstep_bytes, bytes, &ring->full[slot], policy);
+        }
+      }
+      continue;
+    }
     for (int si = 0; si < d.nseg && ok; ++si) {
       const Seg& sg = d.seg[si];
       const SegShare sh(sg, K);
@@ -1456,7 +1787,7 @@ __device__ bool attn_fetch_fold(AttnTile& T, const uint16_t* ksrc, const uint16_
 }
 
 template <int HD, int GRP>
-__device__ bool stage_attn_talker(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+__device__ __noinline__ bool stage_attn_talker(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
                                   unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int E = HD / 32;
@@ -1641,7 +1972,7 @@ __device__ __forceinline__ void group_bar(int grp) {
 }
 
 template <int HD, int GRP>
-__device__ bool stage_attn_cp(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+__device__ __noinline__ bool stage_attn_cp(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
                               unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / kCpGroupWarps, gw = warp - grp * kCpGroupWarps;
@@ -1729,7 +2060,7 @@ __device__ bool stage_attn_cp(const StageDesc& d, uint32_t tag, const Globals& g
 constexpr int kCtaAttnMaxTiles = 4 * kAttnWarps;  // contexts up to 512 positions take this path
 
 template <int HD, int GRP>
-__device__ bool stage_attn_talker_cta(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+__device__ __noinline__ bool stage_attn_talker_cta(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
                                       unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int E = HD / 32;
@@ -1870,7 +2201,7 @@ __device__ bool stage_attn(const StageDesc& d, uint32_t tag, const Globals& g, c
 // code
 // ---------------------------------------------------------------------------
 
-__device__ bool stage_sample(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
+__device__ __noinline__ bool stage_sample(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
                              unsigned char* smem) {
   const int b = blockIdx.x;
   if (b >= fa.B) return true;
@@ -1971,8 +2302,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   __shared__ StageDesc sdesc[2];
-  if ((threadIdx.x >> 5) == 0) fetch_desc(&prog[s0], &sdesc[s0 & 1]);
+  __shared__ TcState tcs;
+  if ((threadIdx.x >> 5) == 0) {
+    fetch_desc(&prog[s0], &sdesc[s0 & 1]);
+    tc_alloc(&tcs.tmem);  // TMEM accumulators of the tensor path, released before the CTA leaves
+    if (threadIdx.x == 0) {
+      mbar_init(&tcs.xfree[0], 1);
+      mbar_init(&tcs.xfree[1], 1);
+      mbar_init(&tcs.done, 1);
+      mbar_init_fence();
+      tcs.xuse = 0u;
+      tcs.nseg = 0u;
+    }
+  }
+  tc_fence_before();
   cbar();
+  tc_fence_after();
   uint32_t q = 0;
   for (int s = s0; s < s1; ++s) {
     const StageDesc& d = sdesc[s & 1];
@@ -1985,9 +2330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (d.type != ST_GEMV && next && (threadIdx.x >> 5) == kCWarps - 1) fetch_desc(next, next_s);
     const uint32_t tag = fa.tag0 + (uint32_t)s;
     bool ok = true;
+    // each stage function is compiled on its own (not inlined): its registers
+    // are allocated for it alone, so none spills to local memory, which with
+    // nearly all of L1 given to shared memory would be served from L2
     switch (d.type) {
       case ST_BEGIN: ok = stage_begin(d, tag, g, fa); break;
-      case ST_GEMV: ok = stage_gemv(d, tag, g, fa, smem, &ring, q, next, next_s); break;
+      case ST_GEMV: ok = stage_gemv(d, tag, g, fa, smem, &ring, &tcs, q, next, next_s); break;
       case ST_ATTN_T: ok = stage_attn<true>(d, tag, g, fa, smem); break;
       case ST_ATTN_CP: ok = stage_attn<false>(d, tag, g, fa, smem); break;
       case ST_SAMPLE: ok = stage_sample(d, tag, g, fa, smem); break;
@@ -1995,7 +2343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     trace_mark(g, 7);
     // no grid barrier: the next stage waits on the tags of the words it reads
-    if (cbar_or(!ok)) return;
+    if (cbar_or(!ok)) break;
+  }
+  // every TMEM read is done (each tensor stage ends at a barrier after its loads)
+  if ((threadIdx.x >> 5) == 0) {
+    tc_fence_after();
+    tc_dealloc(tcs.tmem);
   }
 }
 

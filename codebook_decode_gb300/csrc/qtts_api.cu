@@ -22,6 +22,7 @@ thread_local std::string g_create_error;
 
 struct LinW {
   uint16_t* w = nullptr;  // bf16 [N][K], GPU row order
+  uint16_t* t = nullptr;  // the same as tensor-core tiles (K % 128 == 0 only)
   int8_t* q = nullptr;    // int8 [N][K]
   float* s = nullptr;     // [N]
   int N = 0, K = 0;
@@ -199,6 +200,7 @@ Seg make_seg(const LinW& L, bool i8, int unit, int epi, uint64_t* out, int out_s
              const uint64_t* resid, int r_ws0, int r_ws1, const uint16_t* bias) {
   Seg s{};
   s.w = i8 ? (const void*)L.q : (const void*)L.w;
+  s.wt = i8 ? nullptr : L.t;
   s.scale = i8 ? L.s : nullptr;
   s.N = L.N;
   s.unit = unit;
@@ -374,6 +376,13 @@ int check_gemv_tiles(qtts_model* m, const std::vector<StageDesc>& P) {
 
 int upload_program(qtts_model* m, bool i8) {
   std::vector<StageDesc> P = build_program(m, i8);
+  // the tensor path's MMA covers a CTA's whole row slice: at most kTcMaxRows rows
+  for (StageDesc& d : P)
+    for (int si = 0; si < d.nseg; ++si) {
+      Seg& sg = d.seg[si];
+      const int groups = (sg.N + kTcRows - 1) / kTcRows;
+      if ((groups + m->G - 1) / m->G * kTcRows > kTcMaxRows) sg.wt = nullptr;
+    }
   int rc;
   if ((rc = check_gemv_tiles(m, P))) return rc;
   StageDesc*& dst = m->prog_dev[i8 ? 1 : 0];
@@ -515,6 +524,19 @@ size_t trace_words(const qtts_model* m, int ctas) { return (size_t)8 * ctas * m-
 // whenever a device error is reported.
 cudaError_t reset_split_counters(qtts_model* m) {
   return cudaMemset(m->g.attn_cnt, 0, sizeof(unsigned) * m->cfg.n_layers * kMaxBatch * m->cfg.n_kv_heads);
+}
+
+// Tensor-core tile copies of every bf16 GEMM weight whose K is a multiple of
+// 128 (the layout the large-batch GEMV stages stream).
+int build_tensor_tiles(qtts_model* m) {
+  for (LinW* L : all_lins(m)) {
+    if (L->K % kTcK) continue;
+    const size_t nr = (size_t)(L->N + kTcRows - 1) / kTcRows * kTcRows;
+    if (!L->t) AL(m, L->t, nr * L->K);
+    CK(m, launch_tile_weights(L->w, L->N, L->K, m->G, L->t, 0));
+  }
+  CK(m, cudaDeviceSynchronize());
+  return QTTS_OK;
 }
 
 }  // namespace
@@ -736,6 +758,7 @@ int qtts_load_weights(qtts_model* m, const qtts_tensor* t, int n) {
   cudaFree(dmap);
   if (rc) return rc;
   if ((rc = build_tables(m, false))) return rc;
+  if ((rc = build_tensor_tiles(m))) return rc;
   if ((rc = upload_program(m, false))) return rc;
   m->loaded = true;
   return QTTS_OK;

@@ -22,7 +22,12 @@ constexpr int kMaxContext = kMaxSplits * kMinChunk;
 // tiles, sampler), the GEMV partials, then the ring of weight slots
 constexpr int kWorkBytes = 80 * 1024;
 constexpr int kTailBytes = 12 * 1024;
-constexpr int kSmemBytes = kWorkBytes + kTailBytes + 128 * 1024;
+// the last: a guard band after the ring. A tensor-path MMA reads 128 weight
+// rows from its ring slot while a CTA's slice may have fewer; the extra rows
+// (whose results are never used) read past the slot's data, at most
+// kTcOverread bytes, which must stay inside the allocation.
+constexpr int kTcOverread = 4 * 1024;
+constexpr int kSmemBytes = kWorkBytes + kTailBytes + 128 * 1024 + kTcOverread;
 constexpr int kMaxVocab = 4096;
 constexpr int kMaxGrid = 256;            // persistent CTAs (SMs) the kernel supports
 
@@ -50,7 +55,18 @@ struct Seg {
   uint64_t* out;          // tagged destination rows
   const uint64_t* resid;  // E_RESID: residual rows, laid out like `out`
   const uint16_t* bias;   // E_CPIN: optional bf16 bias [N]
+  const uint16_t* wt;     // bf16 weights as tensor-core tiles (see kTcTile*), or nullptr
 };
+
+// Tensor-core copy of a bf16 weight matrix, packed per CTA of the
+// persistent grid: rows are split into 16-row groups, CTA c of G takes groups
+// [n_groups c / G, n_groups (c+1) / G), i.e. rows [r0, r0 + rows_c), and its
+// slice starts at element r0 * K and is one K-major canonical tile without
+// swizzle: core matrix (k/8, row/8) of 8 rows x 8 bf16 at element
+// ((k/8) * rows_c/8 + row/8) * 64, row-major inside. Rows past N are zero.
+constexpr int kTcRows = 16;
+constexpr int kTcK = 128;
+constexpr int kTcMaxRows = 128;  // rows of one CTA's slice (the MMA's N)
 
 struct alignas(16) StageDesc {
   int type;
@@ -137,6 +153,8 @@ cudaError_t launch_project_table(const uint16_t* E, int rows, int H, const uint1
                                  const float* P8s, const uint16_t* bias, int Hc, float* T, cudaStream_t s);
 cudaError_t launch_kv_scatter(uint16_t* pool, int pool_pages, int nkv, int d, int layer, int n_tok,
                               const int32_t* pages, uint16_t* k, uint16_t* v, int to_pool, cudaStream_t s);
+// Requires K % kTcK == 0; t holds ceil(N / 16) * 16 * K bf16; G: the grid the slices are cut for.
+cudaError_t launch_tile_weights(const uint16_t* w, int N, int K, int G, uint16_t* t, cudaStream_t s);
 struct EmbedTables {
   const uint16_t* e[kCodebooks];
   int rows[kCodebooks];

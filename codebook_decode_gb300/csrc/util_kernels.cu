@@ -158,4 +158,31 @@ cudaError_t launch_feedback(int B, int H, const int32_t* codes, const uint16_t* 
   return cudaGetLastError();
 }
 
+// Row-major bf16 W [N][K] -> the per-CTA tensor-core slices (layout in
+// qtts_internal.h): one thread per 8-element run (one 16-byte core-matrix
+// row).
+__global__ void tile_weights_kernel(const uint16_t* w, int N, int K, int n_groups, int G, uint16_t* t) {
+  const size_t runs = (size_t)n_groups * kTcRows * (K / 8);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < runs; i += (size_t)gridDim.x * blockDim.x) {
+    const int n = (int)(i / (K / 8)), k = (int)(i % (K / 8)) * 8;
+    const int grp = n / kTcRows;
+    // the CTA whose share holds group grp: share(c) = [n_groups c / G, n_groups (c+1) / G)
+    int c = (int)((long long)grp * G / n_groups);
+    while (c + 1 < G && (long long)n_groups * (c + 1) / G <= grp) ++c;
+    while (c > 0 && (long long)n_groups * c / G > grp) --c;
+    const int g0 = (int)((long long)n_groups * c / G), g1 = (int)((long long)n_groups * (c + 1) / G);
+    const int rows_c = (g1 - g0) * kTcRows, nl = n - g0 * kTcRows;
+    const size_t off = (size_t)g0 * kTcRows * K + ((size_t)(k / 8) * (rows_c / 8) + nl / 8) * 64 + (nl % 8) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N) v = *reinterpret_cast<const uint4*>(w + (size_t)n * K + k);
+    *reinterpret_cast<uint4*>(t + off) = v;
+  }
+}
+
+cudaError_t launch_tile_weights(const uint16_t* w, int N, int K, int G, uint16_t* t, cudaStream_t s) {
+  const int n_groups = (N + kTcRows - 1) / kTcRows;
+  tile_weights_kernel<<<1024, 256, 0, s>>>(w, N, K, n_groups, G, t);
+  return cudaGetLastError();
+}
+
 }  // namespace qtts
