@@ -69,8 +69,8 @@ class Workload:
 WORKLOADS = {
     "tiny": Workload("tiny", TINY, 1, ("fixed", 32), ("fixed", 0), 16, 0.0, 1, 1.0, False, False, 0),
     "full_b1": Workload("full_b1", FULL, 1, ("fixed", 128), ("fixed", 0), 64, 0.9, 50, 1.05, True, False, 1),
-    # full widths with 4 Talker layers: a small case for profiler captures
-    "full4l_b1": Workload("full4l_b1", Dims(**{**FULL.as_dict(), "n_layers": 4}), 1, ("fixed", 128), ("fixed", 0),
+    # full widths with 2 Talker layers: a small case for profiler captures
+    "full2l_b1": Workload("full2l_b1", Dims(**{**FULL.as_dict(), "n_layers": 2}), 1, ("fixed", 128), ("fixed", 0),
                           64, 0.9, 50, 1.05, True, False, 1),
     "full_b8": Workload("full_b8", FULL, 8, ("uniform", 64, 512), ("fixed", 0), 128, 0.9, 50, 1.05, True,
                         False, 2),
