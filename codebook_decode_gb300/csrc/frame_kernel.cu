@@ -2382,17 +2382,16 @@ cudaError_t frame_kernel_occupancy(int* blocks_per_sm) {
 // Persistent mode needs every CTA resident at once (CTAs wait on one
 // another's words), hence the cooperative launch; stepwise mode runs one
 // stage per launch, whose inputs all come from earlier launches.
-cudaError_t launch_frame(const StageDesc* prog, int n_stages, const Globals& g, const FrameArgs& fa, bool stepwise,
+cudaError_t launch_frame(const StageDesc* prog, int s0, int s1, const Globals& g, const FrameArgs& fa, bool stepwise,
                          cudaStream_t stream) {
   if (stepwise) {
-    for (int s = 0; s < n_stages; ++s) {
+    for (int s = s0; s < s1; ++s) {
       frame_kernel<<<g.G, kThreads, kSmemBytes, stream>>>(prog, s, s + 1, g, fa);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
   }
-  int s0 = 0, s1 = n_stages;
   Globals gg = g;
   FrameArgs ff = fa;
   void* args[] = {(void*)&prog, (void*)&s0, (void*)&s1, (void*)&gg, (void*)&ff};

@@ -91,6 +91,10 @@ struct qtts_model {
   Globals g{};
   StageDesc* prog_dev[2] = {nullptr, nullptr};
   int n_stages = 0;
+  int s_cp = 0;               // first Code-Predictor stage of the program
+  bool cp_pending = false;    // qtts_frame_talker ran; its qtts_frame_cp has not
+  uint32_t cp_tag0 = 0;       // that frame's tag base
+  uint16_t* fb[2] = {nullptr, nullptr};  // qtts_frame_steps: next-frame inputs [max_batch][H]
 
   // staging for qtts_frame_step_host
   qtts_session* st_sess = nullptr;
@@ -389,6 +393,7 @@ int upload_program(qtts_model* m, bool i8) {
   if (!dst) AL(m, dst, P.size());
   CK(m, cudaMemcpy(dst, P.data(), P.size() * sizeof(StageDesc), cudaMemcpyHostToDevice));
   m->n_stages = (int)P.size();
+  m->s_cp = 1 + 5 * m->cfg.n_layers + 2;  // begin, Talker layers, head 0 + projection, sampler 0
   m->g.n_stages = m->n_stages;
   return QTTS_OK;
 }
@@ -519,6 +524,59 @@ int build_tables(qtts_model* m, bool i8) {
 }
 
 size_t trace_words(const qtts_model* m, int ctas) { return (size_t)8 * ctas * m->n_stages + 2 * 4096; }
+
+enum FramePart { PART_ALL = 0, PART_TALKER = 1, PART_CP = 2 };
+
+// Launch all of a frame's stages, or its Talker half (through sampler 0) or
+// its Code-Predictor half (the 15 steps), which reuses the Talker half's tag
+// base: its first stages read words the Talker half wrote.
+int frame_part(qtts_model* m, int part, int B, qtts_session* sess, const int32_t* bt, int bt_stride,
+               const uint16_t* in_embeds, qtts_rng* rng, uint32_t* seen, const int32_t* forced, int32_t* codes_out,
+               uint8_t* eos_out, float* logits_out, void* stream) {
+  if (!m) return fail(m, QTTS_E_INVALID, "null model");
+  if (!m->loaded) return fail(m, QTTS_E_STATE, "load weights first");
+  if (B < 1 || B > m->cfg.max_batch) return fail(m, QTTS_E_BATCH, "B=%d outside 1..%d", B, m->cfg.max_batch);
+  if (!sess || !bt || !rng || !codes_out || !eos_out || bt_stride < 1 || (part != PART_CP && !in_embeds))
+    return fail(m, QTTS_E_INVALID, "null array or bad block-table stride");
+  if (part == PART_CP && !m->cp_pending) return fail(m, QTTS_E_STATE, "qtts_frame_cp needs qtts_frame_talker first");
+  cudaSetDevice(m->device);
+  FrameArgs fa{};
+  fa.B = B;
+  fa.sess = sess;
+  fa.bt = bt;
+  fa.bt_stride = bt_stride;
+  fa.in_embeds = in_embeds;
+  fa.rng = rng;
+  fa.seen = seen;
+  fa.forced = forced;
+  fa.codes_out = codes_out;
+  fa.eos_out = eos_out;
+  fa.logits_out = logits_out;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool i8 = m->use_int8;
+  if (part == PART_CP) {
+    fa.tag0 = m->cp_tag0;
+  } else {
+    // tag base: stage s of this frame writes tag0 + s; tags only grow, so no
+    // word left by an earlier frame matches. Before they would wrap, the
+    // buffers are cleared and the count restarts.
+    if ((uint64_t)(m->frame_seq + 2) * (uint64_t)m->n_stages >= 0xFFFFFFFFull) {
+      CK(m, cudaDeviceSynchronize());
+      CK(m, cudaMemset(m->acts.base, 0, m->acts.words * sizeof(uint64_t)));
+      m->frame_seq = 0;
+    }
+    ++m->frame_seq;
+    fa.tag0 = m->frame_seq * (uint32_t)m->n_stages;
+  }
+  const int s0 = part == PART_CP ? m->s_cp : 0;
+  const int s1 = part == PART_TALKER ? m->s_cp : m->n_stages;
+  const cudaError_t e = launch_frame(m->prog_dev[i8 ? 1 : 0], s0, s1, m->g, fa, m->stepwise, s);
+  m->last_stream = s;
+  if (e != cudaSuccess) return cuda_fail(m, e, "frame launch");
+  m->cp_pending = part == PART_TALKER;
+  m->cp_tag0 = fa.tag0;
+  return QTTS_OK;
+}
 
 // An abandoned frame can leave attention split counters part-way; clear them
 // whenever a device error is reported.
@@ -932,39 +990,56 @@ int qtts_kv_read(qtts_model* m, int layer, int n_tok, const int32_t* pages, uint
 int qtts_frame_step(qtts_model* m, int B, qtts_session* sess, const int32_t* bt, int bt_stride,
                     const uint16_t* in_embeds, qtts_rng* rng, uint32_t* seen, const int32_t* forced,
                     int32_t* codes_out, uint8_t* eos_out, float* logits_out, void* stream) {
+  return frame_part(m, PART_ALL, B, sess, bt, bt_stride, in_embeds, rng, seen, forced, codes_out, eos_out, logits_out,
+                    stream);
+}
+
+int qtts_frame_talker(qtts_model* m, int B, qtts_session* sess, const int32_t* bt, int bt_stride,
+                      const uint16_t* in_embeds, qtts_rng* rng, uint32_t* seen, const int32_t* forced,
+                      int32_t* codes_out, uint8_t* eos_out, float* logits_out, void* stream) {
+  return frame_part(m, PART_TALKER, B, sess, bt, bt_stride, in_embeds, rng, seen, forced, codes_out, eos_out,
+                    logits_out, stream);
+}
+
+int qtts_frame_cp(qtts_model* m, int B, qtts_session* sess, const int32_t* bt, int bt_stride,
+                  const uint16_t* in_embeds, qtts_rng* rng, uint32_t* seen, const int32_t* forced,
+                  int32_t* codes_out, uint8_t* eos_out, float* logits_out, void* stream) {
+  return frame_part(m, PART_CP, B, sess, bt, bt_stride, in_embeds, rng, seen, forced, codes_out, eos_out, logits_out,
+                    stream);
+}
+
+int qtts_frame_steps(qtts_model* m, int n_frames, int B, qtts_session* sess, const int32_t* bt, int bt_stride,
+                     const uint16_t* in_embeds, const uint16_t* text_embeds, qtts_rng* rng, uint32_t* seen,
+                     const int32_t* forced, int32_t* codes_out, uint8_t* eos_out, void* stream) {
   if (!m) return fail(m, QTTS_E_INVALID, "null model");
   if (!m->loaded) return fail(m, QTTS_E_STATE, "load weights first");
+  if (n_frames < 1) return fail(m, QTTS_E_INVALID, "n_frames must be >= 1");
+  if (!text_embeds || !codes_out || !eos_out) return fail(m, QTTS_E_INVALID, "null array");
   if (B < 1 || B > m->cfg.max_batch) return fail(m, QTTS_E_BATCH, "B=%d outside 1..%d", B, m->cfg.max_batch);
-  if (!sess || !bt || !in_embeds || !rng || !codes_out || !eos_out || bt_stride < 1)
-    return fail(m, QTTS_E_INVALID, "null array or bad block-table stride");
   cudaSetDevice(m->device);
-  FrameArgs fa{};
-  fa.B = B;
-  fa.sess = sess;
-  fa.bt = bt;
-  fa.bt_stride = bt_stride;
-  fa.in_embeds = in_embeds;
-  fa.rng = rng;
-  fa.seen = seen;
-  fa.forced = forced;
-  fa.codes_out = codes_out;
-  fa.eos_out = eos_out;
-  fa.logits_out = logits_out;
-  cudaStream_t s = (cudaStream_t)stream;
-  const bool i8 = m->use_int8;
-  // tag base: stage s of this frame writes tag0 + s; tags only grow, so no
-  // word left by an earlier frame matches. Before they would wrap, the
-  // buffers are cleared and the count restarts.
-  if ((uint64_t)(m->frame_seq + 2) * (uint64_t)m->n_stages >= 0xFFFFFFFFull) {
-    CK(m, cudaDeviceSynchronize());
-    CK(m, cudaMemset(m->acts.base, 0, m->acts.words * sizeof(uint64_t)));
-    m->frame_seq = 0;
+  const int H = m->cfg.hidden;
+  if (!m->fb[0]) {
+    AL(m, m->fb[0], (size_t)kMaxBatch * H);
+    AL(m, m->fb[1], (size_t)kMaxBatch * H);
   }
-  ++m->frame_seq;
-  fa.tag0 = m->frame_seq * (uint32_t)m->n_stages;
-  const cudaError_t e = launch_frame(m->prog_dev[i8 ? 1 : 0], m->n_stages, m->g, fa, m->stepwise, s);
-  m->last_stream = s;
-  if (e != cudaSuccess) return cuda_fail(m, e, "frame launch");
+  EmbedTables t{};
+  for (int j = 0; j < kCodebooks; ++j) {
+    t.e[j] = m->embed[j];
+    t.rows[j] = j == 0 ? m->cfg.vocab0 : m->cfg.cp_vocab;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const uint16_t* in = in_embeds;
+  for (int f = 0; f < n_frames; ++f) {
+    int32_t* codes = codes_out + (size_t)f * B * kCodebooks;
+    const int32_t* frc = forced ? forced + (size_t)f * B * kCodebooks : nullptr;
+    int rc = frame_part(m, PART_ALL, B, sess, bt, bt_stride, in, rng, seen, frc, codes, eos_out + (size_t)f * B,
+                        nullptr, stream);
+    if (rc) return rc;
+    if (f + 1 == n_frames) break;
+    // the next frame's input: text + the codes the model consumed (forced ones under teacher forcing)
+    CK(m, launch_feedback(B, H, frc ? frc : codes, text_embeds + (size_t)f * B * H, t, m->fb[f & 1], s));
+    in = m->fb[f & 1];
+  }
   return QTTS_OK;
 }
 

@@ -138,7 +138,8 @@ struct FrameArgs {
 };
 
 // frame_kernel.cu
-cudaError_t launch_frame(const StageDesc* prog, int n_stages, const Globals& g, const FrameArgs& fa,
+// stages [s0, s1) of the program: one cooperative launch, or one launch per stage
+cudaError_t launch_frame(const StageDesc* prog, int s0, int s1, const Globals& g, const FrameArgs& fa,
                          bool stepwise, cudaStream_t stream);
 cudaError_t frame_kernel_setup();
 cudaError_t frame_kernel_occupancy(int* blocks_per_sm);

@@ -82,6 +82,9 @@ SIGNATURES = [
     ("qtts_kv_write_noalloc", C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P, _P]),
     ("qtts_frame_step", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
     ("qtts_frame_step_host", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
+    ("qtts_frame_talker", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
+    ("qtts_frame_cp", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
+    ("qtts_frame_steps", C.c_int, [_P, C.c_int, C.c_int, _P, _P, C.c_int] + [_P] * 8),
     ("qtts_frame_status", C.c_int, [_P, C.POINTER(C.c_int)]),
     ("qtts_feedback_embed", C.c_int, [_P, C.c_int, _P, _P, _P, _P]),
     ("qtts_sample", C.c_int, [_P, C.c_int, C.c_int, _P, C.c_int, _P, _P, _P, _P, _P]),
@@ -211,6 +214,27 @@ def qtts_frame_step_host(m, B, sessions, block_tables, bt_stride, in_embeds, rng
     return _check(m, load_library().qtts_frame_step_host(
         m, B, ptr(sessions), ptr(block_tables), bt_stride, ptr(in_embeds), ptr(rng), ptr(seen), ptr(forced_codes),
         ptr(codes_out), ptr(eos_out), ptr(logits_out), _stream(stream)))
+
+
+def qtts_frame_talker(m, B, sessions, block_tables, bt_stride, in_embeds, rng, seen, forced_codes, codes_out,
+                      eos_out, logits_out=None, stream=None):
+    return _check(m, load_library().qtts_frame_talker(
+        m, B, ptr(sessions), ptr(block_tables), bt_stride, ptr(in_embeds), ptr(rng), ptr(seen), ptr(forced_codes),
+        ptr(codes_out), ptr(eos_out), ptr(logits_out), _stream(stream)))
+
+
+def qtts_frame_cp(m, B, sessions, block_tables, bt_stride, in_embeds, rng, seen, forced_codes, codes_out, eos_out,
+                  logits_out=None, stream=None):
+    return _check(m, load_library().qtts_frame_cp(
+        m, B, ptr(sessions), ptr(block_tables), bt_stride, ptr(in_embeds), ptr(rng), ptr(seen), ptr(forced_codes),
+        ptr(codes_out), ptr(eos_out), ptr(logits_out), _stream(stream)))
+
+
+def qtts_frame_steps(m, n_frames, B, sessions, block_tables, bt_stride, in_embeds, text_embeds, rng, seen,
+                     forced_codes, codes_out, eos_out, stream=None):
+    return _check(m, load_library().qtts_frame_steps(
+        m, n_frames, B, ptr(sessions), ptr(block_tables), bt_stride, ptr(in_embeds), ptr(text_embeds), ptr(rng),
+        ptr(seen), ptr(forced_codes), ptr(codes_out), ptr(eos_out), _stream(stream)))
 
 
 def qtts_frame_status(m, raise_on_error=True):

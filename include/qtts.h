@@ -215,7 +215,7 @@ int qtts_kv_write_noalloc(qtts_model* m, int layer, int n_tok, const int32_t* pa
  *                                      temperature); rows 1..15 fill the first
  *                                      cp_vocab columns only
  * Host-side errors (B, null pointers, state) return at once. Device-side
- * checks (session, page and code ranges, sampling values, barrier time-outs)
+ * checks (session, page and code ranges, sampling values, wait time-outs)
  * skip the frame's work and are reported by qtts_frame_status; a device error
  * stays set (later frames do nothing) until qtts_frame_status clears it. */
 int qtts_frame_step(qtts_model* m, int B, qtts_session* sessions, const int32_t* block_tables, int bt_stride,
@@ -230,6 +230,41 @@ int qtts_frame_step_host(qtts_model* m, int B, qtts_session* sessions, const int
                          int bt_stride, const uint16_t* in_embeds, qtts_rng* rng, uint32_t* seen,
                          const int32_t* forced_codes, int32_t* codes_out, uint8_t* eos_out, float* logits_out,
                          void* stream);
+
+/* The frame in two halves, for a scheduler that interleaves Talker and
+ * Code-Predictor work ("De grens van snelheid en kosten verleggen voor
+ * Qwen3-TTS": the Talker step and the fixed 15-step Code Predictor as separate
+ * scheduled phases). qtts_frame_talker runs the Talker step, the codebook-0
+ * head, the projection of h_t and sampler 0 (codes_out[:,0], eos_out, the
+ * codebook-0 logits row, kv_len and the seen bitmap advance); qtts_frame_cp
+ * then runs the 15 Code-Predictor steps of that same frame (codes_out[:,1..15],
+ * logits rows 1..15, rng frame_ctr advances) and must come next on the same
+ * stream with the same sessions, rng, forced codes and outputs (in_embeds and
+ * seen are not read; pass them or NULL). Together they give exactly
+ * qtts_frame_step's results. qtts_frame_cp without a preceding
+ * qtts_frame_talker returns QTTS_E_STATE. Arguments as in qtts_frame_step. */
+int qtts_frame_talker(qtts_model* m, int B, qtts_session* sessions, const int32_t* block_tables, int bt_stride,
+                      const uint16_t* in_embeds, qtts_rng* rng, uint32_t* seen, const int32_t* forced_codes,
+                      int32_t* codes_out, uint8_t* eos_out, float* logits_out, void* stream);
+int qtts_frame_cp(qtts_model* m, int B, qtts_session* sessions, const int32_t* block_tables, int bt_stride,
+                  const uint16_t* in_embeds, qtts_rng* rng, uint32_t* seen, const int32_t* forced_codes,
+                  int32_t* codes_out, uint8_t* eos_out, float* logits_out, void* stream);
+
+/* n_frames consecutive frames with no host round trip in between
+ * ("Qwen3-TTS PR 5", "Graph": the decode loop feeds talker_input_embeds back):
+ * frame f takes in_embeds (f = 0) or text_embeds[f-1] + sum_j E_j[c_j] of
+ * frame f-1's committed codes (the forced ones under teacher forcing), built
+ * on the device (qtts_feedback_embed). Device arrays: text_embeds
+ * [n_frames][B][hidden] bf16 (row n_frames-1 unused), forced_codes
+ * [n_frames][B][16] or NULL, codes_out [n_frames][B][16], eos_out
+ * [n_frames][B]; sessions, block_tables, rng and seen as in qtts_frame_step
+ * (advanced once per frame; block tables must already cover kv_len +
+ * n_frames positions). Sessions that emit EOS keep running: the caller
+ * compacts finished sessions between calls. Asynchronous on `stream`. */
+int qtts_frame_steps(qtts_model* m, int n_frames, int B, qtts_session* sessions, const int32_t* block_tables,
+                     int bt_stride, const uint16_t* in_embeds, const uint16_t* text_embeds, qtts_rng* rng,
+                     uint32_t* seen, const int32_t* forced_codes, int32_t* codes_out, uint8_t* eos_out,
+                     void* stream);
 
 /* Synchronise the model's last stream and read, then clear, the device error
  * word (QTTS_DEV_*). Returns QTTS_E_DEVICE / QTTS_E_TIMEOUT when it was set. */

@@ -35,6 +35,24 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(n for n, _, _ in qtts.SIGNATURES) == names
 
 
+def declared_arities():
+    """Parameter count of every function the header declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"#define[^\n]*", "", src)
+    out = {}
+    for name, params in re.findall(r"\b(qtts_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", src):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arities_match_header():
+    decl = declared_arities()
+    for name, _, args in qtts.SIGNATURES:
+        assert len(args) == decl[name], (name, len(args), decl[name])
+
+
 def test_exports_with_nm(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", qtts.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r" T (qtts_\w+)", out))
