@@ -186,7 +186,8 @@ def trace_summary(d, stamps):
                        for k, v in out.items()}}
 
 
-def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, trace_file=None):
+def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, trace_file=None, tc_min_rows=None,
+            ksplit_min_rows=None):
     import torch
 
     from codebook_decode_gb300 import qtts
@@ -201,6 +202,10 @@ def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, tra
     eng.setup_sessions(sess, cap, shuffle=wl.shuffle_pages)
     if ring_slots is not None:
         qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_RING_SLOTS, ring_slots)
+    if tc_min_rows is not None:
+        qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_TC_MIN_ROWS, tc_min_rows)
+    if ksplit_min_rows is not None:
+        qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_KSPLIT_MIN_ROWS, ksplit_min_rows)
     dev = eng.dev
     stream = torch.cuda.current_stream()
     sess0 = eng.sess.clone()
@@ -348,6 +353,10 @@ def main():
     ap.add_argument("--trace", action="store_true", help="print a per-stage time breakdown to stderr")
     ap.add_argument("--trace-file", default=None, help="with --trace: save every CTA's raw stage stamps (.npy)")
     ap.add_argument("--ring-slots", type=int, default=None, help="weight-ring depth per SM (library default 8)")
+    ap.add_argument("--tc-min-rows", type=int, default=None,
+                    help="fewest activation rows a GEMV takes on the tensor cores (library default 8; 65: off)")
+    ap.add_argument("--ksplit-min-rows", type=int, default=None,
+                    help="fewest activation rows for the K-split tensor-core GEMV (library default 16; 65: off)")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
     ws, rank, local = (1, 0, 0)
@@ -378,7 +387,8 @@ def main():
     import torch
     w = synth.make_weights(wl.dims, 1000 + wl.seed)
     barrier(ws)
-    r = run_gpu(wl, args.steps, args.warmup, local, w, trace=args.trace, ring_slots=args.ring_slots,
+    r = run_gpu(wl, args.steps, args.warmup, local, w, trace=args.trace, ring_slots=args.ring_slots, tc_min_rows=args.tc_min_rows,
+                ksplit_min_rows=args.ksplit_min_rows,
                 trace_file=args.trace_file)
     if args.trace:
         print(json.dumps(r["trace"]), file=sys.stderr)
@@ -408,7 +418,8 @@ def main():
             sweep = {}
             for name in ("full_b8", "full_b32", "int8_b1", "int8_b32"):
                 o = configs.WORKLOADS[name]
-                rr = run_gpu(o, min(args.steps, 50), 3, local, w, ring_slots=args.ring_slots)  # same weights
+                rr = run_gpu(o, min(args.steps, 50), 3, local, w, ring_slots=args.ring_slots,
+                             tc_min_rows=args.tc_min_rows, ksplit_min_rows=args.ksplit_min_rows)  # same weights
                 sweep[name] = {"frames_per_s": o.batch * min(args.steps, 50) / (rr["total_ms"] / 1e3),
                                "frame_ms": rr["frame_ms"], "achieved_gbs": rr["achieved_gbs"],
                                "frac": rr["achieved_gbs"] / peak, "bytes_per_frame": rr["bytes_per_frame"]}

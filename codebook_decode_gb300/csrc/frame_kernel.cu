@@ -194,6 +194,53 @@ __device__ __forceinline__ bool ll_settle(const uint64_t* const (&ps)[N], const 
   }
 }
 
+// Gather-and-add of tagged words: item i (< nitems) adds the words src(i, 0..nw-1)
+// (nw <= NW, in that order), each once it carries tag(i), to *dst(i); up to
+// NB items per compute thread are in flight at once and every pass re-reads
+// the words still pending. False after the time limit or once an error is
+// set elsewhere (the sums are then incomplete).
+template <int NB, int NW, typename Tag, typename Src, typename Dst>
+__device__ __forceinline__ bool ll_gather_add(int nitems, int nw, const Tag& tag, const Src& src, const Dst& dst,
+                                              int* err) {
+  bool ok = true;
+  for (int base = (int)threadIdx.x; base < nitems; base += kCThreads * NB) {
+    uint64_t w[NB][NW];
+#pragma unroll
+    for (int u = 0; u < NB; ++u)
+#pragma unroll
+      for (int k = 0; k < NW; ++k) w[u][k] = (base + u * kCThreads < nitems && k < nw) ? ld_ll(src(base + u * kCThreads, k)) : 0;
+    const uint64_t t0 = global_timer_ns();
+    unsigned spins = 0;
+    for (;;) {
+      bool all = true;
+#pragma unroll
+      for (int u = 0; u < NB; ++u)
+#pragma unroll
+        for (int k = 0; k < NW; ++k)
+          if (base + u * kCThreads < nitems && k < nw && !ll_ok(w[u][k], tag(base + u * kCThreads))) {
+            w[u][k] = ld_ll(src(base + u * kCThreads, k));
+            all = false;
+          }
+      if (all) break;
+      if ((++spins & 15u) == 0u && (read_err(err) || global_timer_ns() - t0 > kWaitTimeoutNs)) {
+        if (!read_err(err)) set_err(err, QTTS_DEV_TIMEOUT);
+        return false;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < NB; ++u)
+      if (base + u * kCThreads < nitems) {
+        float* o = dst(base + u * kCThreads);
+        float v = *o;
+#pragma unroll
+        for (int k = 0; k < NW; ++k)
+          if (k < nw) v += ll_val(w[u][k]);
+        *o = v;
+      }
+  }
+  return ok;
+}
+
 // deterministic sum over the compute threads (fixed combination order)
 __device__ float block_sum(float v, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -213,7 +260,9 @@ __device__ float block_sum(float v, float* red) {
 // Stage trace: with tracing on, thread 0 of the traced CTAs (the first and
 // the last, or all) stamps %globaltimer at up to 8 points of every stage (0
 // start, 1 after the GEMV prologue, 2 after its phase 1, 3 after its phase 2,
-// 4/5 around the first task's ring wait, 6 after its dot products, 7 end);
+// 4/5 around the first task's ring wait, 6 after its dot products, 7 end;
+// tensor path: 4 when the second activation pass starts loading, 5 when its
+// first words have settled, 6 when it is staged);
 // CTA 0 also stamps its weight-ring slot uses (issue, ready).
 constexpr int kTraceMarks = 8;
 constexpr int kTraceRing = 4096;
@@ -812,33 +861,50 @@ __device__ __forceinline__ int ring_rt(const StageDesc& d, int B) {
 }
 
 // How a GEMV stage runs for batch B: ring path (few rows: CUDA-core dot
-// products from the weight ring), tensor path (8..64 rows, bf16 weights with a
-// tensor-tile copy, K a multiple of 128: tcgen05 MMAs from the weight ring),
+// products from the weight ring), tensor path (from g.tc_min_rows up to 64
+// rows, bf16 weights with a tensor-tile copy, K a multiple of 128: tcgen05
+// MMAs from the weight ring),
 // else direct path (CUDA cores, weights loaded by the lanes). The producer
 // and the compute warps evaluate the same rule.
 enum GemvMode { GM_RING = 0, GM_TC = 1, GM_DIRECT = 2 };
-constexpr int kTcMinRows = 8;
-__device__ __forceinline__ int gemv_mode(const StageDesc& d, int B) {
+// Whether a tensor-path segment takes its K-split partition (tc_ksplit) for
+// `rows` activation rows.
+__device__ __forceinline__ bool tc_split(const Seg& sg, int rows, const Globals& g) {
+  return sg.wtk != nullptr && rows >= g.ksplit_min_rows;
+}
+__device__ __forceinline__ int gemv_mode(const StageDesc& d, int B, const Globals& g) {
   const int rows = B * d.rps;
-  bool tc = rows >= kTcMinRows && rows <= 64 && d.K % kTcK == 0;
-  for (int s = 0; s < d.nseg; ++s) tc = tc && d.seg[s].wt != nullptr;
+  bool tc = rows >= g.tc_min_rows && rows <= kTcMaxActRows && d.K % kTcK == 0;
+  for (int s = 0; s < d.nseg; ++s) tc = tc && (tc_split(d.seg[s], rows, g) || d.seg[s].wt != nullptr);
   if (tc) return GM_TC;
   return ring_rt(d, B) > 0 ? GM_RING : GM_DIRECT;
 }
 
-// This CTA's share of a segment on the tensor path: 16-row groups [g0, g0 + ng);
-// per 128-wide K chunk, slots of up to 4 group tiles (16 KB).
+// This CTA's share of a segment on the tensor path (with `split`, the K-split
+// partition tc_ksplit states, else one K-slice): 16-row groups
+// [g0, g0 + rows / 16) over 128-wide K chunks [kc0, kc0 + nkc); per ring
+// slot, kps 16-wide K steps of the slice; `wt` the packed tiles it reads.
 struct TcShare {
-  int g0, rows;      // rows [8 g0, 8 g0 + rows) of the segment (rows = 0: nothing to do)
+  int S, ks;         // K-slices of the segment, this CTA's slice
+  int g0, rows;      // rows [16 g0, 16 g0 + rows) of the segment (rows = 0: nothing to do)
+  int kc0, nkc;      // this CTA's K chunks
   int kstep_bytes;   // bytes of the slice per 16-wide K step
-  int kps, nslot;    // K steps per ring slot, ring slots of the segment
-  __device__ TcShare(const Seg& sg, int K) {
+  int kps, nslot;    // K steps per ring slot, ring slots of the share
+  const uint16_t* wt;
+  __device__ TcShare(const Seg& sg, int K, bool split) {
+    S = split ? tc_ksplit(sg.N, K, (int)gridDim.x) : 1;
+    wt = split ? sg.wtk : sg.wt;
+    const int C = (int)gridDim.x / max(S, 1);
+    ks = (int)blockIdx.x / C;
+    const int c = (int)blockIdx.x - ks * C;
     const unsigned ngroups = (unsigned)((sg.N + kTcRows - 1) / kTcRows);
-    g0 = (int)(ngroups * blockIdx.x / gridDim.x);
-    rows = ((int)(ngroups * (blockIdx.x + 1) / gridDim.x) - g0) * kTcRows;
+    g0 = (int)(ngroups * c / C);
+    rows = ks < S ? ((int)(ngroups * (c + 1) / C) - g0) * kTcRows : 0;
+    nkc = S ? K / kTcK / S : 0;
+    kc0 = ks * nkc;
     kstep_bytes = rows * 32;
     kps = rows ? kSlotBytes / kstep_bytes : 1;
-    nslot = rows ? (K / 16 + kps - 1) / kps : 0;
+    nslot = rows ? (nkc * (kTcK / 16) + kps - 1) / kps : 0;
   }
 };
 
@@ -1269,7 +1335,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
                               unsigned char* smem, Ring* ring, TcState* ts, uint32_t& q) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rows = fa.B * d.rps;
-  const int K = d.K, nch = K / kTcK, nks = K / 16;
+  const int K = d.K;
   const bool norm = d.xsrc == X_NORM;
   const RowMap rm{d.rps, d.in_rps, d.in_off};
   const uint32_t nsl = (uint32_t)g.ring_slots, nsl_shift = (uint32_t)(__ffs(g.ring_slots) - 1);
@@ -1279,18 +1345,21 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
   const int lbo = meff / 8 * 128;
   const int tile_bytes = meff * kTcK * 2;
   const int cpp = kTcXBytes / tile_bytes;  // K chunks per pass
-  const int npass = (nch + cpp - 1) / cpp;
   const int tpr = kTcStagers * 32 / rows;  // stager threads per activation row
   const int srow = tid / tpr, sub = tid - srow * tpr;
   const uint64_t* xrow = srow < rows ? d.x + (size_t)rm.in_row(srow) * d.x_stride : nullptr;
   const uint32_t row_tag = srow < rows ? fa.tag0 + (uint32_t)d.x_ws[srow % d.rps] : 0u;
   float* ssq = reinterpret_cast<float*>(smem + kWorkBytes);  // [kTcStagers * 32] per-thread partial sums of squares
+  float* rsq = ssq + kTcStagers * 32;                         // [rows] sums of squares per activation row
   bool ok = true;
   uint32_t xuse = ts->xuse, nseg = ts->nseg;
   for (int si = 0; si < d.nseg; ++si) {
     const Seg& sg = d.seg[si];
-    const TcShare sh(sg, K);
+    const TcShare sh(sg, K, tc_split(sg, rows, g));
     if (sh.rows == 0) continue;  // no rows of this segment on this CTA (the same on all its threads)
+    // chunks, K steps and passes below count from the start of the share's K range
+    const int nch = sh.nkc, nks = nch * (kTcK / 16);
+    const int npass = (nch + cpp - 1) / cpp;
     float sq = 0.f;              // this thread's share of its row's sum of squares
     int slot_j = -1, slot = 0;   // issuer: the weight slot in use
     uint32_t wa = 0;
@@ -1303,17 +1372,19 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
       if (warp < kTcStagers) {
         // the MMAs of this buffer's previous fill are done with it
         if (xuse >= 2) ok &= mbar_wait(&ts->xfree[b], ((xuse >> 1) - 1u) & 1u, g.err);
+        if (pass == 1) trace_mark(g, 4);
         const int npair = (c1 - c0) * (kTcK / 2);  // pairs of this row in the pass
         for (int j0 = sub; j0 < npair && srow < rows; j0 += kTcPairs * tpr) {
           uint64_t w[kTcPairs][2];
           const int n = min(kTcPairs, (npair - j0 + tpr - 1) / tpr);  // this thread's pairs j0 + u tpr, u < n
-          const uint64_t* base = xrow + c0 * kTcK + 2 * j0;
+          const uint64_t* base = xrow + (sh.kc0 + c0) * kTcK + 2 * j0;
 #pragma unroll
           for (int u = 0; u < kTcPairs; ++u) {
             w[u][0] = w[u][1] = 0;
             if (u < n) ld_ll2(base + (size_t)u * 2 * tpr, w[u][0], w[u][1]);
           }
           ok &= ll_settle_strided<kTcPairs>(base, 2 * tpr, n, row_tag, w, g.err);
+          if (pass == 1 && j0 == sub) trace_mark(g, 5);
 #pragma unroll
           for (int u = 0; u < kTcPairs; ++u) {
             if (u >= n) continue;
@@ -1323,7 +1394,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
             if (norm) {
               sq = fmaf(x0, x0, sq);
               sq = fmaf(x1, x1, sq);
-              const uint32_t gw = __ldg(reinterpret_cast<const unsigned*>(d.gain + (c0 + cc) * kTcK + kl));
+              const uint32_t gw = __ldg(reinterpret_cast<const unsigned*>(d.gain + (sh.kc0 + c0 + cc) * kTcK + kl));
               x0 *= bf_lo(gw);
               x1 *= bf_hi(gw);
             }
@@ -1340,6 +1411,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
       }
       cbar();
       if (pass == 0) trace_mark(g, 1);
+      if (pass == 1) trace_mark(g, 6);
       if (warp == kTcIssuer && lane == 0) {
         tc_fence_after();
         // activation K step cs of the pass starts at xb + 2 cs lbo (a chunk tile is 16 lbo bytes)
@@ -1391,31 +1463,89 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
     tc_fence_before();
     if (norm && warp < kTcStagers) ssq[tid] = sq;
     if (cbar_or(!ok)) return false;
+    // fold the low lanes into the high ones (the low half is then free), and
+    // each row's sum of squares over the share's K range, in thread order
+    const int nsr = sh.rows, nres = rows * nsr;
+    for (int idx = tid; idx < nres; idx += kCThreads) {
+      res[idx] += res[nres + idx];
+      res[nres + idx] = 0.f;
+    }
+    if (tid < rows) {
+      float t = 0.f;
+      if (norm)
+        for (int i = 0; i < tpr; ++i) t += ssq[tid * tpr + i];
+      rsq[tid] = t;
+    }
+    cbar();
+    // K-split exchange area of this segment: per later slice, [16 n_groups][rows]
+    // partial sums then [rows] partial sums of squares
+    const int npad = (sg.N + kTcRows - 1) / kTcRows * kTcRows;
+    const size_t slice_words = (size_t)npad * rows + rows;
+    uint64_t* kp = nullptr;
+    if (sh.S > 1) {
+      long long off = 0;
+      for (int sp = 0; sp < si; ++sp)
+        if (tc_split(d.seg[sp], rows, g)) off += tc_kpart_words(d.seg[sp].N, K, (int)gridDim.x, kTcMaxActRows);
+      kp = g.kpart + (size_t)((tag - fa.tag0) & 1u) * (size_t)g.kpart_words + (size_t)off;
+    }
+    const int n_base = sh.g0 * kTcRows;
+    if (sh.ks > 0) {
+      // a later K-slice: hand the partial sums to slice 0 and stop here
+      uint64_t* dst = kp + (size_t)(sh.ks - 1) * slice_words;
+      for (int idx = tid; idx < nres; idx += kCThreads) {
+        const int n = idx / rows, r = idx - n * rows;
+        st_ll(dst + (size_t)(n_base + n) * rows + r, res[r * nsr + n], tag);
+      }
+      if (tid < rows) st_ll(dst + (size_t)npad * rows + tid, rsq[tid], tag);
+      cbar();  // res is read before the next share's fills
+      trace_mark(g, 3);
+      continue;
+    }
+    if (sh.S > 1) {
+      // slice 0: add the later slices' partial sums (in slice order) and sums of squares
+      const uint64_t* srcb = kp;
+      ok &= ll_gather_add<4, 7>(
+          nres + rows, sh.S - 1, [&](int) { return tag; },
+          [&](int i, int k) {
+            const uint64_t* b = srcb + (size_t)k * slice_words;
+            if (i >= nres) return b + (size_t)npad * rows + (i - nres);
+            const int n = i / rows, r = i - n * rows;
+            return b + (size_t)(n_base + n) * rows + r;
+          },
+          [&](int i) {
+            if (i >= nres) return rsq + (i - nres);
+            const int n = i / rows, r = i - n * rows;
+            return res + r * nsr + n;
+          },
+          g.err);
+    }
+    if (sg.epi == E_RESID) {
+      // the residual operands of the share's rows, into the free low half
+      ok &= ll_gather_add<4, 1>(
+          nres, 1, [&](int i) { return fa.tag0 + (uint32_t)sg.r_ws[(i % rows) % d.rps]; },
+          [&](int i, int) {
+            const int n = i / rows, r = i - n * rows;
+            const int n0 = min(n_base + n, sg.N - 1);  // padding rows read a real word and never use it
+            return sg.resid + (size_t)out_row_of(sg, d.rps, r) * sg.out_stride + n0;
+          },
+          [&](int i) {
+            const int n = i / rows, r = i - n * rows;
+            return res + nres + r * nsr + n;
+          },
+          g.err);
+    }
+    if (cbar_or(!ok)) return false;
     // epilogue: one thread per (unit, activation row)
     const int U = sg.unit;
-    const int nunits = sh.rows / U;
+    const int nunits = nsr / U;
     for (int idx = tid; idx < nunits * rows; idx += kCThreads) {
       const int ul = idx / rows, r = idx - ul * rows;
-      const int n0 = sh.g0 * kTcRows + ul * U;
+      const int n0 = n_base + ul * U;
       if (n0 >= sg.N) continue;  // padding rows of the last group
-      float f = 1.0f;
-      if (norm) {  // the row's partial sums, in thread order
-        float t = 0.f;
-        for (int i = 0; i < tpr; ++i) t += ssq[r * tpr + i];
-        f = 1.0f / sqrtf(t / (float)K + g.eps);
-      }
+      const float f = norm ? 1.0f / sqrtf(rsq[r] / (float)K + g.eps) : 1.0f;
       float y[2];
-      for (int i = 0; i < U; ++i) {
-        const int col = ul * U + i;
-        y[i] = (res[r * sh.rows + col] + res[(rows + r) * sh.rows + col]) * f;
-      }
-      float resid = 0.f;
-      if (sg.epi == E_RESID) {
-        const uint64_t* p = sg.resid + (size_t)out_row_of(sg, d.rps, r) * sg.out_stride + n0;
-        uint64_t w = ld_ll(p);
-        ok &= ll_get(p, fa.tag0 + (uint32_t)sg.r_ws[r % d.rps], w, g.err);
-        resid = ll_val(w);
-      }
+      for (int i = 0; i < U; ++i) y[i] = res[r * nsr + ul * U + i] * f;
+      const float resid = res[nres + r * nsr + ul * U];
       gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r, r, resid, tag, nullptr);
     }
     cbar();  // the results are read; the next fill may overwrite them
@@ -1434,7 +1564,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
 __device__ __noinline__ bool stage_gemv(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
                            unsigned char* smem, Ring* ring, TcState* ts, uint32_t& q, const StageDesc* next,
                            StageDesc* next_s) {
-  if (gemv_mode(d, fa.B) == GM_TC) {
+  if (gemv_mode(d, fa.B, g) == GM_TC) {
     if (next && (threadIdx.x >> 5) == kCWarps - 2) fetch_desc(next, next_s);
     return stage_gemv_tc(d, tag, g, fa, smem, ring, ts, q);
   }
@@ -1589,14 +1719,16 @@ __device__ void producer(const StageDesc* prog, int s0, int s1, const Globals& g
   for (int s = s0; s < s1 && ok; ++s) {
     const StageDesc& d = prog[s];
     if (d.type != ST_GEMV) continue;
-    const int mode = gemv_mode(d, fa.B);
+    const int mode = gemv_mode(d, fa.B, g);
     if (mode == GM_DIRECT) continue;
     const int K = d.K;
     if (mode == GM_TC) {
       for (int si = 0; si < d.nseg && ok; ++si) {
-        const TcShare sh(d.seg[si], K);
-        const unsigned char* W = (const unsigned char*)d.seg[si].wt + (size_t)sh.g0 * kTcRows * K * 2;
-        const int nks = K / 16;
+        const TcShare sh(d.seg[si], K, tc_split(d.seg[si], fa.B * d.rps, g));
+        // the share's K range is contiguous in its slice of the packed tiles
+        const unsigned char* W = (const unsigned char*)sh.wt + (size_t)sh.g0 * kTcRows * K * 2 +
+                                 (size_t)sh.kc0 * (kTcK / 16) * sh.kstep_bytes;
+        const int nks = sh.nkc * (kTcK / 16);
         for (int j = 0; j < sh.nslot; ++j, ++q) {
           const uint32_t bytes = (uint32_t)(min(nks, (j + 1) * sh.kps) - j * sh.kps) * sh.kstep_bytes;
           const int slot = (int)(q % nsl);

@@ -22,7 +22,8 @@ thread_local std::string g_create_error;
 
 struct LinW {
   uint16_t* w = nullptr;  // bf16 [N][K], GPU row order
-  uint16_t* t = nullptr;  // the same as tensor-core tiles (K % 128 == 0 only)
+  uint16_t* t = nullptr;  // the same as tensor-core tiles, one K-slice (K % 128 == 0 only)
+  uint16_t* tk = nullptr; // the same as tensor-core tiles for the K-split partition (tc_ksplit > 1 only)
   int8_t* q = nullptr;    // int8 [N][K]
   float* s = nullptr;     // [N]
   int N = 0, K = 0;
@@ -205,6 +206,7 @@ Seg make_seg(const LinW& L, bool i8, int unit, int epi, uint64_t* out, int out_s
   Seg s{};
   s.w = i8 ? (const void*)L.q : (const void*)L.w;
   s.wt = i8 ? nullptr : L.t;
+  s.wtk = i8 ? nullptr : L.tk;
   s.scale = i8 ? L.s : nullptr;
   s.N = L.N;
   s.unit = unit;
@@ -380,13 +382,27 @@ int check_gemv_tiles(qtts_model* m, const std::vector<StageDesc>& P) {
 
 int upload_program(qtts_model* m, bool i8) {
   std::vector<StageDesc> P = build_program(m, i8);
-  // the tensor path's MMA covers a CTA's whole row slice: at most kTcMaxRows rows
-  for (StageDesc& d : P)
+  // the tensor path's MMA covers a CTA's whole row slice: at most kTcMaxRows
+  // rows, for some K-split; K-split segments exchange partial sums through
+  // a tagged area (two copies, by stage parity), sized for the largest stage
+  long long kpart = 0;
+  for (StageDesc& d : P) {
+    long long need = 0;
     for (int si = 0; si < d.nseg; ++si) {
       Seg& sg = d.seg[si];
-      const int groups = (sg.N + kTcRows - 1) / kTcRows;
-      if ((groups + m->G - 1) / m->G * kTcRows > kTcMaxRows) sg.wt = nullptr;
+      if (sg.wt && !tc_fits(sg.N, d.K, m->G, 1)) sg.wt = nullptr;
+      if (sg.wtk && tc_ksplit(sg.N, d.K, m->G) < 2) sg.wtk = nullptr;
+      if (sg.wtk) need += tc_kpart_words(sg.N, d.K, m->G, kTcMaxActRows);
     }
+    kpart = std::max(kpart, need);
+  }
+  if (kpart > m->g.kpart_words) {
+    uint64_t* a = nullptr;
+    AL(m, a, (size_t)(2 * kpart));
+    CK(m, cudaMemset(a, 0, (size_t)(2 * kpart) * sizeof(uint64_t)));  // zero tags match no frame
+    m->g.kpart = a;
+    m->g.kpart_words = kpart;
+  }
   int rc;
   if ((rc = check_gemv_tiles(m, P))) return rc;
   StageDesc*& dst = m->prog_dev[i8 ? 1 : 0];
@@ -563,6 +579,7 @@ int frame_part(qtts_model* m, int part, int B, qtts_session* sess, const int32_t
     if ((uint64_t)(m->frame_seq + 2) * (uint64_t)m->n_stages >= 0xFFFFFFFFull) {
       CK(m, cudaDeviceSynchronize());
       CK(m, cudaMemset(m->acts.base, 0, m->acts.words * sizeof(uint64_t)));
+      if (m->g.kpart) CK(m, cudaMemset(m->g.kpart, 0, (size_t)(2 * m->g.kpart_words) * sizeof(uint64_t)));
       m->frame_seq = 0;
     }
     ++m->frame_seq;
@@ -590,8 +607,15 @@ int build_tensor_tiles(qtts_model* m) {
   for (LinW* L : all_lins(m)) {
     if (L->K % kTcK) continue;
     const size_t nr = (size_t)(L->N + kTcRows - 1) / kTcRows * kTcRows;
-    if (!L->t) AL(m, L->t, nr * L->K);
-    CK(m, launch_tile_weights(L->w, L->N, L->K, m->G, L->t, 0));
+    if (tc_fits(L->N, L->K, m->G, 1)) {  // one K-slice over the whole grid
+      if (!L->t) AL(m, L->t, nr * L->K);
+      CK(m, launch_tile_weights(L->w, L->N, L->K, m->G, L->t, 0));
+    }
+    const int S = tc_ksplit(L->N, L->K, m->G);
+    if (S > 1) {  // the K-split partition: G / S CTAs per slice
+      if (!L->tk) AL(m, L->tk, nr * L->K);
+      CK(m, launch_tile_weights(L->w, L->N, L->K, m->G / S, L->tk, 0));
+    }
   }
   CK(m, cudaDeviceSynchronize());
   return QTTS_OK;
@@ -656,6 +680,8 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
   g.Vc = c.cp_vocab; g.eos_id = c.eos_id; g.n_codes = c.n_codes; g.seen_words = seen_words(c);
   g.max_context = c.max_context; g.eps = c.rms_eps; g.G = sms; g.pool_pages = c.kv_pool_pages;
   g.ring_slots = 8;
+  g.tc_min_rows = 8;
+  g.ksplit_min_rows = 16;
 
   const size_t kv_elems = (size_t)c.n_layers * c.kv_pool_pages * 2 * c.n_kv_heads * kPage * c.head_dim;
   if ((rc = dalloc(m, &m->kv_pool, kv_elems))) return bail(rc);
@@ -1162,6 +1188,16 @@ int qtts_set_option(qtts_model* m, int option, int value) {
     if (value != 1 && value != 2 && value != 4 && value != 8)
       return fail(m, QTTS_E_INVALID, "ring slots must be 1, 2, 4 or 8");
     m->g.ring_slots = value;
+    return QTTS_OK;
+  }
+  if (option == QTTS_OPT_TC_MIN_ROWS) {
+    if (value < 1 || value > 65) return fail(m, QTTS_E_INVALID, "tensor-path row threshold must be 1..65");
+    m->g.tc_min_rows = value;
+    return QTTS_OK;
+  }
+  if (option == QTTS_OPT_KSPLIT_MIN_ROWS) {
+    if (value < 1 || value > 65) return fail(m, QTTS_E_INVALID, "K-split row threshold must be 1..65");
+    m->g.ksplit_min_rows = value;
     return QTTS_OK;
   }
   if (option == QTTS_OPT_TRACE) {

@@ -55,18 +55,60 @@ struct Seg {
   uint64_t* out;          // tagged destination rows
   const uint64_t* resid;  // E_RESID: residual rows, laid out like `out`
   const uint16_t* bias;   // E_CPIN: optional bf16 bias [N]
-  const uint16_t* wt;     // bf16 weights as tensor-core tiles (see kTcTile*), or nullptr
+  const uint16_t* wt;     // bf16 weights as tensor-core tiles for one K-slice (see below), or nullptr
+  const uint16_t* wtk;    // the same for the K-split partition (tc_ksplit > 1), or nullptr
 };
 
-// Tensor-core copy of a bf16 weight matrix, packed per CTA of the
-// persistent grid: rows are split into 16-row groups, CTA c of G takes groups
-// [n_groups c / G, n_groups (c+1) / G), i.e. rows [r0, r0 + rows_c), and its
-// slice starts at element r0 * K and is one K-major canonical tile without
-// swizzle: core matrix (k/8, row/8) of 8 rows x 8 bf16 at element
-// ((k/8) * rows_c/8 + row/8) * 64, row-major inside. Rows past N are zero.
+// Tensor-core copy of a bf16 weight matrix, packed per CTA of one K-slice of
+// the persistent grid (C CTAs per slice, see tc_ksplit): rows are split into
+// 16-row groups, CTA c of C takes groups [n_groups c / C, n_groups (c+1) / C),
+// i.e. rows [r0, r0 + rows_c), and its slice starts at element r0 * K and is
+// one K-major canonical tile without swizzle: core matrix (k/8, row/8) of 8
+// rows x 8 bf16 at element ((k/8) * rows_c/8 + row/8) * 64, row-major inside,
+// so a K range of the slice is contiguous. Rows past N are zero.
 constexpr int kTcRows = 16;
 constexpr int kTcK = 128;
 constexpr int kTcMaxRows = 128;  // rows of one CTA's slice (the MMA's N)
+constexpr int kTcMaxActRows = 64;  // activation rows (sessions x rows per session) the tensor path takes
+
+// Whether S K-slices keep every share of the grid within kTcMaxRows rows.
+__host__ __device__ inline bool tc_fits(int N, int K, int G, int S) {
+  const int ngroups = (N + kTcRows - 1) / kTcRows;
+  const int C = G / S;
+  return C >= 1 && (K / kTcK) % S == 0 && (ngroups + C - 1) / C * kTcRows <= kTcMaxRows;
+}
+// K-split of a tensor-path segment (N rows, K) over a grid of G CTAs: the
+// grid's first S C CTAs (C = G / S) form S K-slices; CTA c of slice s takes
+// the 16-row groups [n_groups c / C, n_groups (c + 1) / C) over the 128-wide
+// K chunks [s K / S, (s + 1) K / S). A CTA of slice s > 0 hands its partial
+// sums to CTA c of slice 0, which adds them and runs the epilogue. Among the S
+// in {1, 2, 4, 8} that divide K / kTcK and keep a share within kTcMaxRows
+// rows, S minimises the words a CTA reads per activation row: its K range
+// (K / S) plus the partial sums slice 0 gathers ((S - 1) x its rows); ties
+// take the smaller S. 0: none fits. A second copy of the weight tiles is
+// packed for this partition (C CTAs per slice); a stage takes it from
+// ksplit_min_rows activation rows up, else the one-slice copy (S = 1).
+__host__ __device__ inline int tc_ksplit(int N, int K, int G) {
+  const int ngroups = (N + kTcRows - 1) / kTcRows;
+  int best = 0, best_cost = 0;
+  for (int S = 1; S <= 8; S *= 2) {
+    if (!tc_fits(N, K, G, S)) continue;
+    const int rows = (ngroups + G / S - 1) / (G / S) * kTcRows;
+    const int cost = K / S + (S - 1) * rows;
+    if (!best || cost < best_cost) {
+      best = S;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+// Words of the partial-sum exchange area one K-split segment needs: per slice
+// s > 0, [n_groups * 16][rows] partial sums then [rows] partial sums of squares.
+__host__ __device__ inline long long tc_kpart_words(int N, int K, int G, int rows) {
+  const int S = tc_ksplit(N, K, G);
+  const long long npad = (long long)(N + kTcRows - 1) / kTcRows * kTcRows;
+  return S > 1 ? (long long)(S - 1) * (npad * rows + rows) : 0;
+}
 
 struct alignas(16) StageDesc {
   int type;
@@ -118,6 +160,10 @@ struct Globals {
   int* err;               // device error word (QTTS_DEV_*)
   int n_stages;
   int ring_slots;         // weight-ring slots in use (1..8): how far the producer may run ahead
+  int tc_min_rows;        // fewest activation rows (sessions x rows per session) a GEMV takes on the tensor path
+  int ksplit_min_rows;    // fewest activation rows for which a tensor-path segment takes its K-split partition
+  uint64_t* kpart;        // K-split partial sums: two areas of kpart_words tagged words (by stage parity)
+  long long kpart_words;
   unsigned long long* trace;  // optional [trace_ctas][n_stages][8] %globaltimer stamps, then ring events
   int trace_ctas;         // 2: the first and the last CTA; G: every CTA
 };

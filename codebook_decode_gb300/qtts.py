@@ -28,6 +28,8 @@ QTTS_E_TIMEOUT = -11
 QTTS_OPT_STEPWISE = 1
 QTTS_OPT_TRACE = 3
 QTTS_OPT_RING_SLOTS = 4
+QTTS_OPT_TC_MIN_ROWS = 5
+QTTS_OPT_KSPLIT_MIN_ROWS = 6
 
 
 class QttsError(RuntimeError):

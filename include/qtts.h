@@ -293,10 +293,22 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
  *                      the first and last CTA (qtts_frame_trace); 2: on
  *                      every CTA. 0 (default): off.
  *   QTTS_OPT_RING_SLOTS 1, 2, 4 or 8: 16 KB weight slots per SM the producer
- *                      warp may fill ahead of the compute warps. Default 8. */
+ *                      warp may fill ahead of the compute warps. Default 8.
+ *   QTTS_OPT_TC_MIN_ROWS 1..65: a GEMV stage whose activation rows (sessions
+ *                      x rows per session) number at least this and at most
+ *                      64 runs on the tensor cores (bf16 weights, K a
+ *                      multiple of 128); 65 turns the tensor path off.
+ *                      Default 8.
+ *   QTTS_OPT_KSPLIT_MIN_ROWS 1..65: from this many activation rows up, a
+ *                      tensor-path GEMV splits K across groups of CTAs
+ *                      whose partial sums one CTA per group adds (fewer
+ *                      activation words per CTA, one more exchange);
+ *                      65: never. Default 16. */
 #define QTTS_OPT_STEPWISE 1
 #define QTTS_OPT_TRACE 3
 #define QTTS_OPT_RING_SLOTS 4
+#define QTTS_OPT_TC_MIN_ROWS 5
+#define QTTS_OPT_KSPLIT_MIN_ROWS 6
 int qtts_set_option(qtts_model* m, int option, int value);
 
 /* Stage timestamps of the last frame run with QTTS_OPT_TRACE on: 8 values
