@@ -260,7 +260,9 @@ __device__ float block_sum(float v, float* red) {
 // Stage trace: with tracing on, thread 0 of the traced CTAs (the first and
 // the last, or all) stamps %globaltimer at up to 8 points of every stage (0
 // start, 1 after the GEMV prologue, 2 after its phase 1, 3 after its phase 2,
-// 4/5 around the first task's ring wait, 6 after its dot products, 7 end;
+// 7 end; ring path: 4 before warp 0's first ring wait, 5 after that unit's
+// dot products, 6 after its epilogue, 3 after the dot products of warp 0's
+// second unit;
 // tensor path: 4 when the second activation pass starts loading, 5 when its
 // first words have settled, 6 when it is staged);
 // CTA 0 also stamps its weight-ring slot uses (issue, ready).
@@ -890,10 +892,12 @@ struct TcShare {
   int kc0, nkc;      // this CTA's K chunks
   int kstep_bytes;   // bytes of the slice per 16-wide K step
   int kps, nslot;    // K steps per ring slot, ring slots of the share
-  const uint16_t* wt;
+  int es;            // bytes per weight element in the tiles: 2 (bf16) or 1 (int8, widened in the slot)
+  const unsigned char* wt;
   __device__ TcShare(const Seg& sg, int K, bool split) {
     S = split ? tc_ksplit(sg.N, K, (int)gridDim.x) : 1;
-    wt = split ? sg.wtk : sg.wt;
+    wt = (const unsigned char*)(split ? sg.wtk : sg.wt);
+    es = sg.scale ? 1 : 2;
     const int C = (int)gridDim.x / max(S, 1);
     ks = (int)blockIdx.x / C;
     const int c = (int)blockIdx.x - ks * C;
@@ -902,7 +906,7 @@ struct TcShare {
     rows = ks < S ? ((int)(ngroups * (c + 1) / C) - g0) * kTcRows : 0;
     nkc = S ? K / kTcK / S : 0;
     kc0 = ks * nkc;
-    kstep_bytes = rows * 32;
+    kstep_bytes = rows * 32;  // in the slot (bf16)
     kps = rows ? kSlotBytes / kstep_bytes : 1;
     nslot = rows ? (nkc * (kTcK / 16) + kps - 1) / kps : 0;
   }
@@ -1137,7 +1141,6 @@ __device__ void gemv_ring(const StageDesc& d, const Seg& sg, int si, const SegSh
     // the stage
     if (ul == 0) trace_mark(g, 4);
     const bool got = ring_wait_full(ring, slot, qq >> nsl_shift, g.err);
-    if (ul == 0) trace_mark(g, 5);
     if (lane == 0 && ul == ua) trace_ring(g, qq, 1);
     const WT* rowp = (const WT*)ring_slot(smem, slot) + (size_t)(ul - ua) * U * K;
     float acc[U][RT];
@@ -1153,7 +1156,8 @@ __device__ void gemv_ring(const StageDesc& d, const Seg& sg, int si, const SegSh
       task_fma<WT, U, RT>(raw, xs, K, kb, nr, acc);
     }
     __syncwarp();
-    if (ul == 0) trace_mark(g, 6);
+    if (ul == 0) trace_mark(g, 5);
+    if (ul == kCWarps) trace_mark(g, 3);
     if (lane == 0 && got) {
       const int slot_units = min(sh.nu, ua + sh.upslot) - ua;
       if (atomicAdd(&ring->done[slot], 1u) + 1u == (uint32_t)slot_units) {
@@ -1180,6 +1184,7 @@ __device__ void gemv_ring(const StageDesc& d, const Seg& sg, int si, const SegSh
       }
       gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r0 + lane, lane, tail->resid[ul * RT + lane], tag, &tail->ec);
     }
+    if (ul == 0) trace_mark(g, 6);
   }
 }
 
@@ -1303,6 +1308,34 @@ __device__ void fill_epi_cache(const StageDesc& d, const Globals& g, const Frame
   }
 }
 
+// Widen the int8 weight tiles a bulk copy left in a ring slot's upper half
+// (nraw bytes) to bf16 over the whole slot, element for element (exact: an
+// int8 value is a bf16 with its low 16 float bits zero). One warp, in
+// 512-byte steps whose reads all precede their writes: step c writes bytes
+// [1024 c, 1024 c + 1024), which hold only the raw bytes of steps <= c.
+__device__ __forceinline__ void widen_i8_slot(unsigned char* slot, int nraw, int lane) {
+  const unsigned char* raw = slot + kSlotBytes / 2;
+  for (int c0 = 0; c0 < nraw; c0 += 512) {
+    const int o = c0 + lane * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (o < nraw) v = *reinterpret_cast<const uint4*>(raw + o);
+    __syncwarp();
+    if (o < nraw) {
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t out[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t word = in[i >> 1], sh = (i & 1) * 16;
+        const float a = (float)(int8_t)((word >> sh) & 0xFFu), b = (float)(int8_t)((word >> (sh + 8)) & 0xFFu);
+        out[i] = (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u);
+      }
+      *reinterpret_cast<uint4*>(slot + 2 * o) = make_uint4(out[0], out[1], out[2], out[3]);
+      *reinterpret_cast<uint4*>(slot + 2 * o + 16) = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+    __syncwarp();
+  }
+}
+
 // Tensor-path state kept across stages in shared memory.
 struct TcState {
   uint64_t xfree[2];  // MMAs reading X buffer b have completed
@@ -1412,34 +1445,45 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
       cbar();
       if (pass == 0) trace_mark(g, 1);
       if (pass == 1) trace_mark(g, 6);
-      if (warp == kTcIssuer && lane == 0) {
+      if (warp == kTcIssuer) {
         tc_fence_after();
         // activation K step cs of the pass starts at xb + 2 cs lbo (a chunk tile is 16 lbo bytes)
         const int s_end = c1 * (kTcK / 16);
         for (int s = c0 * (kTcK / 16); s < s_end;) {
           const int j = s / sh.kps;
-          if (j != slot_j) {  // next weight slot
+          const int slot_end = min(nks, (j + 1) * sh.kps);
+          if (j != slot_j) {  // next weight slot: the whole warp waits (and widens int8 tiles)
             slot_j = j;
             const uint32_t qq = q + (uint32_t)j;
             slot = (int)(qq & (nsl - 1u));
             ok &= ring_wait_full(ring, slot, qq >> nsl_shift, g.err);
-            trace_ring(g, qq, 1);
-            wa = smem_addr(ring_slot(smem, slot));
+            if (lane == 0) trace_ring(g, qq, 1);
+            unsigned char* sp = ring_slot(smem, slot);
+            if (sh.es == 1) {
+              widen_i8_slot(sp, (slot_end - j * sh.kps) * sh.rows * 16, lane);
+              fence_proxy_async_smem();  // read by the tensor cores next
+              __syncwarp();
+            }
+            wa = smem_addr(sp);
           }
-          const int slot_end = min(nks, (j + 1) * sh.kps);
           const int e = min(s_end, slot_end);
-          uint64_t da = tc_smem_desc(smem_addr(xb) + (uint32_t)((s - c0 * (kTcK / 16)) * 2 * lbo), lbo, 128);
-          uint64_t db = tc_smem_desc(wa + (uint32_t)((s - j * sh.kps) * sh.kstep_bytes), sh.rows * 16, 128);
-          const uint64_t da_step = (uint64_t)((2 * lbo) >> 4), db_step = (uint64_t)(sh.kstep_bytes >> 4);
-          for (; s < e; ++s) {  // descriptors advance in their 16-byte address field
-            tc_mma(ts->tmem, da, db, idesc, s > 0);
-            da += da_step;
-            db += db_step;
+          if (lane == 0) {
+            uint64_t da = tc_smem_desc(smem_addr(xb) + (uint32_t)((s - c0 * (kTcK / 16)) * 2 * lbo), lbo, 128);
+            uint64_t db = tc_smem_desc(wa + (uint32_t)((s - j * sh.kps) * sh.kstep_bytes), sh.rows * 16, 128);
+            const uint64_t da_step = (uint64_t)((2 * lbo) >> 4), db_step = (uint64_t)(sh.kstep_bytes >> 4);
+            for (int t = s; t < e; ++t) {  // descriptors advance in their 16-byte address field
+              tc_mma(ts->tmem, da, db, idesc, t > 0);
+              da += da_step;
+              db += db_step;
+            }
+            if (e == slot_end) tc_commit(&ring->empty[slot]);  // the slot is free once these MMAs are done
           }
-          if (s == slot_end) tc_commit(&ring->empty[slot]);  // the slot is free once these MMAs are done
+          s = e;
         }
-        tc_commit(&ts->xfree[b]);
-        if (pass == npass - 1) tc_commit(&ts->done);
+        if (lane == 0) {
+          tc_commit(&ts->xfree[b]);
+          if (pass == npass - 1) tc_commit(&ts->done);
+        }
       }
       __syncwarp();
     }
@@ -1544,7 +1588,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
       if (n0 >= sg.N) continue;  // padding rows of the last group
       const float f = norm ? 1.0f / sqrtf(rsq[r] / (float)K + g.eps) : 1.0f;
       float y[2];
-      for (int i = 0; i < U; ++i) y[i] = res[r * nsr + ul * U + i] * f;
+      for (int i = 0; i < U; ++i) y[i] = res[r * nsr + ul * U + i] * f * (sg.scale ? __ldg(sg.scale + n0 + i) : 1.0f);
       const float resid = res[nres + r * nsr + ul * U];
       gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r, r, resid, tag, nullptr);
     }
@@ -1690,7 +1734,6 @@ __device__ __noinline__ bool stage_gemv(const StageDesc& d, uint32_t tag, const 
         q += (uint32_t)sh.nslot;
         cbar();
         trace_mark(g, 2);
-        trace_mark(g, 3);
       } else {
         gemv_p1(sg, K, RT, xs, nr, tail);
         cbar();
@@ -1725,12 +1768,15 @@ __device__ void producer(const StageDesc* prog, int s0, int s1, const Globals& g
     if (mode == GM_TC) {
       for (int si = 0; si < d.nseg && ok; ++si) {
         const TcShare sh(d.seg[si], K, tc_split(d.seg[si], fa.B * d.rps, g));
-        // the share's K range is contiguous in its slice of the packed tiles
-        const unsigned char* W = (const unsigned char*)sh.wt + (size_t)sh.g0 * kTcRows * K * 2 +
-                                 (size_t)sh.kc0 * (kTcK / 16) * sh.kstep_bytes;
+        // the share's K range is contiguous in its slice of the packed tiles;
+        // int8 tiles land in the slot's upper half (the compute side widens them)
+        const int gstep = sh.rows * 16 * sh.es;  // tile bytes per 16-wide K step
+        const unsigned char* W =
+            sh.wt + ((size_t)sh.g0 * kTcRows * K + (size_t)sh.kc0 * (kTcK / 16) * sh.rows * 16) * sh.es;
         const int nks = sh.nkc * (kTcK / 16);
+        const int dst_off = sh.es == 1 ? kSlotBytes / 2 : 0;
         for (int j = 0; j < sh.nslot; ++j, ++q) {
-          const uint32_t bytes = (uint32_t)(min(nks, (j + 1) * sh.kps) - j * sh.kps) * sh.kstep_bytes;
+          const uint32_t bytes = (uint32_t)(min(nks, (j + 1) * sh.kps) - j * sh.kps) * gstep;
           const int slot = (int)(q % nsl);
           if (!mbar_wait(&ring->empty[slot], ((q / nsl) & 1u) ^ 1u, g.err)) {
             ok = false;
@@ -1739,7 +1785,7 @@ __device__ void producer(const StageDesc* prog, int s0, int s1, const Globals& g
           trace_ring(g, q, 0);
           *(volatile uint32_t*)&ring->seq[slot] = q / nsl;
           mbar_arrive_expect_tx(&ring->full[slot], bytes);
-          bulk_load(ring_slot(smem, slot), W + (size_t)j * sh.kps * sh.kstep_bytes, bytes, &ring->full[slot], policy);
+          bulk_load(ring_slot(smem, slot) + dst_off, W + (size_t)j * sh.kps * gstep, bytes, &ring->full[slot], policy);
         }
       }
       continue;

@@ -24,6 +24,8 @@ struct LinW {
   uint16_t* w = nullptr;  // bf16 [N][K], GPU row order
   uint16_t* t = nullptr;  // the same as tensor-core tiles, one K-slice (K % 128 == 0 only)
   uint16_t* tk = nullptr; // the same as tensor-core tiles for the K-split partition (tc_ksplit > 1 only)
+  int8_t* tq = nullptr;   // q as tensor-core tiles, one K-slice
+  int8_t* tqk = nullptr;  // q as tensor-core tiles for the K-split partition
   int8_t* q = nullptr;    // int8 [N][K]
   float* s = nullptr;     // [N]
   int N = 0, K = 0;
@@ -205,8 +207,8 @@ Seg make_seg(const LinW& L, bool i8, int unit, int epi, uint64_t* out, int out_s
              const uint64_t* resid, int r_ws0, int r_ws1, const uint16_t* bias) {
   Seg s{};
   s.w = i8 ? (const void*)L.q : (const void*)L.w;
-  s.wt = i8 ? nullptr : L.t;
-  s.wtk = i8 ? nullptr : L.tk;
+  s.wt = i8 ? (const void*)L.tq : (const void*)L.t;
+  s.wtk = i8 ? (const void*)L.tqk : (const void*)L.tk;
   s.scale = i8 ? L.s : nullptr;
   s.N = L.N;
   s.unit = unit;
@@ -603,18 +605,25 @@ cudaError_t reset_split_counters(qtts_model* m) {
 
 // Tensor-core tile copies of every bf16 GEMM weight whose K is a multiple of
 // 128 (the layout the large-batch GEMV stages stream).
-int build_tensor_tiles(qtts_model* m) {
+// i8: tiles of the int8 weights (after qtts_quantize_int8), else of the bf16 ones.
+int build_tensor_tiles(qtts_model* m, bool i8) {
   for (LinW* L : all_lins(m)) {
     if (L->K % kTcK) continue;
     const size_t nr = (size_t)(L->N + kTcRows - 1) / kTcRows * kTcRows;
-    if (tc_fits(L->N, L->K, m->G, 1)) {  // one K-slice over the whole grid
-      if (!L->t) AL(m, L->t, nr * L->K);
-      CK(m, launch_tile_weights(L->w, L->N, L->K, m->G, L->t, 0));
-    }
     const int S = tc_ksplit(L->N, L->K, m->G);
-    if (S > 1) {  // the K-split partition: G / S CTAs per slice
-      if (!L->tk) AL(m, L->tk, nr * L->K);
-      CK(m, launch_tile_weights(L->w, L->N, L->K, m->G / S, L->tk, 0));
+    for (int split = 0; split < 2; ++split) {
+      // one K-slice over the whole grid, then the K-split partition (G / S CTAs per slice)
+      if (split ? S < 2 : !tc_fits(L->N, L->K, m->G, 1)) continue;
+      const int C = split ? m->G / S : m->G;
+      if (i8) {
+        int8_t*& t = split ? L->tqk : L->tq;
+        if (!t) AL(m, t, nr * L->K);
+        CK(m, launch_tile_weights_i8(L->q, L->N, L->K, C, t, 0));
+      } else {
+        uint16_t*& t = split ? L->tk : L->t;
+        if (!t) AL(m, t, nr * L->K);
+        CK(m, launch_tile_weights(L->w, L->N, L->K, C, t, 0));
+      }
     }
   }
   CK(m, cudaDeviceSynchronize());
@@ -842,7 +851,7 @@ int qtts_load_weights(qtts_model* m, const qtts_tensor* t, int n) {
   cudaFree(dmap);
   if (rc) return rc;
   if ((rc = build_tables(m, false))) return rc;
-  if ((rc = build_tensor_tiles(m))) return rc;
+  if ((rc = build_tensor_tiles(m, false))) return rc;
   if ((rc = upload_program(m, false))) return rc;
   m->loaded = true;
   return QTTS_OK;
@@ -863,6 +872,7 @@ int qtts_quantize_int8(qtts_model* m) {
     CK(m, cudaDeviceSynchronize());
     int rc;
     if ((rc = build_tables(m, true))) return rc;
+    if ((rc = build_tensor_tiles(m, true))) return rc;
     if ((rc = upload_program(m, true))) return rc;
     m->quantized = true;
   }

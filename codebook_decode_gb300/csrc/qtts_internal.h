@@ -55,8 +55,9 @@ struct Seg {
   uint64_t* out;          // tagged destination rows
   const uint64_t* resid;  // E_RESID: residual rows, laid out like `out`
   const uint16_t* bias;   // E_CPIN: optional bf16 bias [N]
-  const uint16_t* wt;     // bf16 weights as tensor-core tiles for one K-slice (see below), or nullptr
-  const uint16_t* wtk;    // the same for the K-split partition (tc_ksplit > 1), or nullptr
+  const void* wt;         // the weights (bf16, or int8 with `scale`) as tensor-core tiles for one K-slice
+                          // (see below), or nullptr
+  const void* wtk;        // the same for the K-split partition (tc_ksplit > 1), or nullptr
 };
 
 // Tensor-core copy of a bf16 weight matrix, packed per CTA of one K-slice of
@@ -202,6 +203,7 @@ cudaError_t launch_kv_scatter(uint16_t* pool, int pool_pages, int nkv, int d, in
                               const int32_t* pages, uint16_t* k, uint16_t* v, int to_pool, cudaStream_t s);
 // Requires K % kTcK == 0; t holds ceil(N / 16) * 16 * K bf16; G: the grid the slices are cut for.
 cudaError_t launch_tile_weights(const uint16_t* w, int N, int K, int G, uint16_t* t, cudaStream_t s);
+cudaError_t launch_tile_weights_i8(const int8_t* w, int N, int K, int G, int8_t* t, cudaStream_t s);
 struct EmbedTables {
   const uint16_t* e[kCodebooks];
   int rows[kCodebooks];

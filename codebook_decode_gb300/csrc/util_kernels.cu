@@ -158,10 +158,11 @@ cudaError_t launch_feedback(int B, int H, const int32_t* codes, const uint16_t* 
   return cudaGetLastError();
 }
 
-// Row-major bf16 W [N][K] -> the per-CTA tensor-core slices (layout in
-// qtts_internal.h): one thread per 8-element run (one 16-byte core-matrix
-// row).
-__global__ void tile_weights_kernel(const uint16_t* w, int N, int K, int n_groups, int G, uint16_t* t) {
+// Row-major W [N][K] (bf16, or int8 for the weight-only INT8 path) -> the
+// per-CTA tensor-core slices (layout in qtts_internal.h, by element): one
+// thread per 8-element run (one core-matrix row: 16 bytes of bf16, 8 of int8).
+template <typename T, typename Run>
+__global__ void tile_weights_kernel(const T* w, int N, int K, int n_groups, int G, T* t) {
   const size_t runs = (size_t)n_groups * kTcRows * (K / 8);
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < runs; i += (size_t)gridDim.x * blockDim.x) {
     const int n = (int)(i / (K / 8)), k = (int)(i % (K / 8)) * 8;
@@ -173,15 +174,21 @@ __global__ void tile_weights_kernel(const uint16_t* w, int N, int K, int n_group
     const int g0 = (int)((long long)n_groups * c / G), g1 = (int)((long long)n_groups * (c + 1) / G);
     const int rows_c = (g1 - g0) * kTcRows, nl = n - g0 * kTcRows;
     const size_t off = (size_t)g0 * kTcRows * K + ((size_t)(k / 8) * (rows_c / 8) + nl / 8) * 64 + (nl % 8) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (n < N) v = *reinterpret_cast<const uint4*>(w + (size_t)n * K + k);
-    *reinterpret_cast<uint4*>(t + off) = v;
+    Run v{};
+    if (n < N) v = *reinterpret_cast<const Run*>(w + (size_t)n * K + k);
+    *reinterpret_cast<Run*>(t + off) = v;
   }
 }
 
 cudaError_t launch_tile_weights(const uint16_t* w, int N, int K, int G, uint16_t* t, cudaStream_t s) {
   const int n_groups = (N + kTcRows - 1) / kTcRows;
-  tile_weights_kernel<<<1024, 256, 0, s>>>(w, N, K, n_groups, G, t);
+  tile_weights_kernel<uint16_t, uint4><<<1024, 256, 0, s>>>(w, N, K, n_groups, G, t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_weights_i8(const int8_t* w, int N, int K, int G, int8_t* t, cudaStream_t s) {
+  const int n_groups = (N + kTcRows - 1) / kTcRows;
+  tile_weights_kernel<int8_t, uint2><<<1024, 256, 0, s>>>(w, N, K, n_groups, G, t);
   return cudaGetLastError();
 }
 

@@ -76,15 +76,18 @@ def test_tiny_max_batch_long_context(tiny_w):
         free(run)
 
 
-@pytest.mark.parametrize("B,tc_min,ks_min", [(1, 1, 65), (3, 1, 1), (9, 65, 65), (9, 8, 65), (9, 8, 8)])
-def test_gemv_path_choice(tiny_w, B, tc_min, ks_min):
-    """Every GEMV path matches the oracle: tensor cores from one activation
-    row up (tc_min 1) with one K-slice (ks_min 65) or K split across CTAs
-    (ks_min <= rows), and the CUDA-core paths alone (tc_min 65)."""
+@pytest.mark.parametrize("B,tc_min,ks_min,int8", [(1, 1, 65, False), (3, 1, 1, False), (9, 65, 65, False),
+                                                  (9, 8, 65, False), (9, 8, 8, False), (9, 8, 65, True),
+                                                  (9, 8, 8, True), (2, 1, 1, True)])
+def test_gemv_path_choice(tiny_w, B, tc_min, ks_min, int8):
+    """Every GEMV path matches the oracle, BF16 and INT8 weights: tensor
+    cores from one activation row up (tc_min 1) with one K-slice (ks_min 65)
+    or K split across CTAs (ks_min <= rows), and the CUDA-core paths alone
+    (tc_min 65)."""
     s = tiny_sessions(B, [7, 33, 16, 2, 40, 1, 15, 64, 30][:B], [0, 2, 5, 1, 3, 0, 4, 6, 2][:B], T=0.9, k=50, r=1.05)
-    run = ParityRun(TINY, tiny_w, s, 3, shuffle=True, tc_min_rows=tc_min, ksplit_min_rows=ks_min).run()
+    run = ParityRun(TINY, tiny_w, s, 3, shuffle=True, int8=int8, tc_min_rows=tc_min, ksplit_min_rows=ks_min).run()
     try:
-        assert run.max_rel() < TOL_BF16, run.max_rel()
+        assert run.max_rel() < (TOL_INT8 if int8 else TOL_BF16), run.max_rel()
         assert run.confident_agree == run.confident
         run.check_state()
     finally:
