@@ -1043,6 +1043,14 @@ __device__ __forceinline__ void gemv_epilogue(const StageDesc& d, const Seg& sg,
   }
 }
 
+// The same as one out-of-line copy, for the stages that run it once per
+// thread per unit (the tensor path): their code stays small.
+__device__ __noinline__ void gemv_epilogue_call(const StageDesc& d, const Seg& sg, const Globals& g,
+                                                const FrameArgs& fa, int n0, float y0, float y1, int r, float resid,
+                                                uint32_t tag) {
+  gemv_epilogue(d, sg, g, fa, n0, y0, y1, r, r, resid, tag, nullptr);
+}
+
 template <typename WT>
 struct Raw8 {
   using T = uint4;  // 8 bf16
@@ -1548,7 +1556,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
     if (sh.S > 1) {
       // slice 0: add the later slices' partial sums (in slice order) and sums of squares
       const uint64_t* srcb = kp;
-      ok &= ll_gather_add<4, 7>(
+      ok &= ll_gather_add<4, kTcMaxSplit - 1>(
           nres + rows, sh.S - 1, [&](int) { return tag; },
           [&](int i, int k) {
             const uint64_t* b = srcb + (size_t)k * slice_words;
@@ -1565,7 +1573,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
     }
     if (sg.epi == E_RESID) {
       // the residual operands of the share's rows, into the free low half
-      ok &= ll_gather_add<4, 1>(
+      ok &= ll_gather_add<2, 1>(
           nres, 1, [&](int i) { return fa.tag0 + (uint32_t)sg.r_ws[(i % rows) % d.rps]; },
           [&](int i, int) {
             const int n = i / rows, r = i - n * rows;
@@ -1590,7 +1598,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
       float y[2];
       for (int i = 0; i < U; ++i) y[i] = res[r * nsr + ul * U + i] * f * (sg.scale ? __ldg(sg.scale + n0 + i) : 1.0f);
       const float resid = res[nres + r * nsr + ul * U];
-      gemv_epilogue(d, sg, g, fa, n0, y[0], y[U - 1], r, r, resid, tag, nullptr);
+      gemv_epilogue_call(d, sg, g, fa, n0, y[0], y[U - 1], r, resid, tag);
     }
     cbar();  // the results are read; the next fill may overwrite them
     trace_mark(g, 3);

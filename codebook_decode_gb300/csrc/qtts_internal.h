@@ -82,17 +82,18 @@ __host__ __device__ inline bool tc_fits(int N, int K, int G, int S) {
 // grid's first S C CTAs (C = G / S) form S K-slices; CTA c of slice s takes
 // the 16-row groups [n_groups c / C, n_groups (c + 1) / C) over the 128-wide
 // K chunks [s K / S, (s + 1) K / S). A CTA of slice s > 0 hands its partial
-// sums to CTA c of slice 0, which adds them and runs the epilogue. Among the S
-// in {1, 2, 4, 8} that divide K / kTcK and keep a share within kTcMaxRows
-// rows, S minimises the words a CTA reads per activation row: its K range
+// sums to CTA c of slice 0, which adds them and runs the epilogue. Among the
+// powers of two S <= kTcMaxSplit that divide K / kTcK and keep a share within
+// kTcMaxRows rows, S minimises the words a CTA reads per activation row: its K range
 // (K / S) plus the partial sums slice 0 gathers ((S - 1) x its rows); ties
 // take the smaller S. 0: none fits. A second copy of the weight tiles is
 // packed for this partition (C CTAs per slice); a stage takes it from
 // ksplit_min_rows activation rows up, else the one-slice copy (S = 1).
+constexpr int kTcMaxSplit = 4;
 __host__ __device__ inline int tc_ksplit(int N, int K, int G) {
   const int ngroups = (N + kTcRows - 1) / kTcRows;
   int best = 0, best_cost = 0;
-  for (int S = 1; S <= 8; S *= 2) {
+  for (int S = 1; S <= kTcMaxSplit; S *= 2) {
     if (!tc_fits(N, K, G, S)) continue;
     const int rows = (ngroups + G / S - 1) / (G / S) * kTcRows;
     const int cost = K / S + (S - 1) * rows;
