@@ -1417,12 +1417,18 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
         const int npair = (c1 - c0) * (kTcK / 2);  // pairs of this row in the pass
         for (int j0 = sub; j0 < npair && srow < rows; j0 += kTcPairs * tpr) {
           uint64_t w[kTcPairs][2];
+          uint32_t gw[kTcPairs];  // RMSNorm gains of the pairs, loaded with them
           const int n = min(kTcPairs, (npair - j0 + tpr - 1) / tpr);  // this thread's pairs j0 + u tpr, u < n
           const uint64_t* base = xrow + (sh.kc0 + c0) * kTcK + 2 * j0;
+          const unsigned* gbase = reinterpret_cast<const unsigned*>(d.gain + (sh.kc0 + c0) * kTcK + 2 * j0);
 #pragma unroll
           for (int u = 0; u < kTcPairs; ++u) {
             w[u][0] = w[u][1] = 0;
-            if (u < n) ld_ll2(base + (size_t)u * 2 * tpr, w[u][0], w[u][1]);
+            gw[u] = 0u;
+            if (u < n) {
+              ld_ll2(base + (size_t)u * 2 * tpr, w[u][0], w[u][1]);
+              if (norm) gw[u] = __ldg(gbase + u * tpr);
+            }
           }
           ok &= ll_settle_strided<kTcPairs>(base, 2 * tpr, n, row_tag, w, g.err);
           if (pass == 1 && j0 == sub) trace_mark(g, 5);
@@ -1435,9 +1441,8 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
             if (norm) {
               sq = fmaf(x0, x0, sq);
               sq = fmaf(x1, x1, sq);
-              const uint32_t gw = __ldg(reinterpret_cast<const unsigned*>(d.gain + (sh.kc0 + c0 + cc) * kTcK + kl));
-              x0 *= bf_lo(gw);
-              x1 *= bf_hi(gw);
+              x0 *= bf_lo(gw[u]);
+              x1 *= bf_hi(gw[u]);
             }
             const uint16_t h0 = f2bf(x0), h1 = f2bf(x1);
             const uint16_t l0 = f2bf(x0 - bf2f(h0)), l1 = f2bf(x1 - bf2f(h1));
