@@ -1996,8 +1996,9 @@ __device__ __noinline__ bool stage_attn_talker(const StageDesc& d, uint32_t tag,
   uint32_t parity = 0;
   bool ok = true;
   const uint32_t tag_in = fa.tag0 + (uint32_t)d.q_ws;
-  // split plan, identical on every CTA (same inputs, same arithmetic): about
-  // one page-aligned split per warp of the grid
+  // split plan, identical on every CTA (same inputs, same arithmetic): the
+  // smallest page-aligned split length whose splits (each session's rounded
+  // up) number at most one per warp of the grid, so no warp runs two in turn
   const int len = lane < fa.B ? s_kv_len[lane] + 1 : 0;
   int total = len;
 #pragma unroll
@@ -2006,6 +2007,13 @@ __device__ __noinline__ bool stage_attn_talker(const StageDesc& d, uint32_t tag,
   int chunk = (total * nkv + target - 1) / target;
   chunk = ((chunk + kPage - 1) / kPage) * kPage;
   if (chunk < kMinChunk) chunk = kMinChunk;
+  for (;;) {  // ends by kMaxContext at the latest (one split per session)
+    int cnt = (len + chunk - 1) / chunk * nkv;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (cnt <= target || chunk >= kMaxContext) break;
+    chunk += kPage;
+  }
   const int nsp = (len + chunk - 1) / chunk;
   int incl = nsp * nkv;
 #pragma unroll
