@@ -173,7 +173,7 @@ def trace_summary(d, stamps):
             o["w"] += (t[i, 2] - t[i, 1]) / 1e3
             o["epi"] += (t[i, 3] - t[i, 2]) / 1e3
     total = (t[-1, 7] - t[0, 0]) / 1e3
-    ring = stamps[16 * n: 16 * n + 8192].reshape(4096, 2).astype(np.int64)
+    ring = stamps[16 * n: 16 * n + 4 * 4096].reshape(4096, 4)[:, :2].astype(np.int64)
     used = int((ring[:, 1] > 0).sum())
     rq = ring[:used]
     lead = (t[:, 0].min(), rq)
@@ -302,7 +302,7 @@ def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, tra
         eng.sess.copy_(sess0)
         for _ in range(2):
             eng.step(emb, None, want_logits=False, stream=stream)
-        stamps = np.zeros(16 * len(stage_names(d)) + 2 * 4096, dtype=np.uint64)
+        stamps = np.zeros(16 * len(stage_names(d)) + 4 * 4096, dtype=np.uint64)
         qtts.qtts_frame_trace(eng.m, stamps)
         res["trace"] = trace_summary(d, stamps)
         if trace_file:  # every CTA's stage stamps, raw
@@ -311,7 +311,7 @@ def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, tra
             for _ in range(2):
                 eng.step(emb, None, want_logits=False, stream=stream)
             G = torch.cuda.get_device_properties(local).multi_processor_count
-            raw = np.zeros(8 * G * len(stage_names(d)) + 2 * 4096, dtype=np.uint64)
+            raw = np.zeros(8 * G * len(stage_names(d)) + 4 * 4096, dtype=np.uint64)
             qtts.qtts_frame_trace(eng.m, raw)
             np.save(trace_file, raw)
     eng.release_pages()

@@ -541,7 +541,7 @@ int build_tables(qtts_model* m, bool i8) {
   return QTTS_OK;
 }
 
-size_t trace_words(const qtts_model* m, int ctas) { return (size_t)8 * ctas * m->n_stages + 2 * 4096; }
+size_t trace_words(const qtts_model* m, int ctas) { return (size_t)8 * ctas * m->n_stages + 4 * 4096; }
 
 enum FramePart { PART_ALL = 0, PART_TALKER = 1, PART_CP = 2 };
 

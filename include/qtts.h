@@ -314,12 +314,16 @@ int qtts_set_option(qtts_model* m, int option, int value);
 /* Stage timestamps of the last frame run with QTTS_OPT_TRACE on: 8 values
  * per stage for CTA 0 (every stage in order), then the same for the last CTA
  * (trace 1) or for CTAs 1, 2, ... in order (trace 2) (nanoseconds,
- * %globaltimer; 0 = stage start, 1 after the GEMV prologue, 2 after its
- * weight pass, 3 after its epilogues, 4 and 5 around the first weight task's
- * ring wait, 6 after that task's dot products, 7 = stage end; unused marks
- * keep older values); then, for CTA 0, 4096 pairs (issue, ready) of the weight ring's
- * slot uses in order. Synchronises the model's last stream. Returns the
- * number of values written (<= capacity) or a negative error. */
+ * %globaltimer; 0 = stage start, 1 after the GEMV prologue (tensor path:
+ * its first activation pass), 2 after its weight pass, 3 after its
+ * epilogues, 7 = stage end; 4-6 ring path: before warp 0's first ring wait,
+ * after that unit's dot products, after its epilogue, and 3 then marks warp
+ * 0's second unit's dot products; 4-6 tensor path: the second activation
+ * pass starts loading, its first words settle, it is staged; unused marks
+ * keep older values); then, for CTA 0, 4096 quadruples (issue, ready, MMAs
+ * issued on the tensor path, unused) of the weight ring's slot uses in
+ * order. Synchronises the model's last stream. Returns the number of values
+ * written (<= capacity) or a negative error. */
 int qtts_frame_trace(qtts_model* m, uint64_t* host, int capacity);
 
 /* Bytes of weights one frame streams (the roofline's numerator, without KV):
