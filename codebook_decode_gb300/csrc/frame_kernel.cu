@@ -265,13 +265,14 @@ __device__ float block_sum(float v, float* red) {
 // second unit;
 // tensor path: 4 when the second activation pass starts loading, 5 when its
 // first words have settled, 6 when it is staged);
-// CTA 0 also stamps its weight-ring slot uses (issue, ready).
+// CTA 0 also stamps its weight-ring slot uses (issue, ready, and on the
+// tensor path the end of the slot's MMA issue).
 constexpr int kTraceMarks = 8;
 constexpr int kTraceRing = 4096;
 __shared__ int g_trace_stage;
 __device__ __forceinline__ void trace_ring(const Globals& g, uint32_t q, int which) {
   if (g.trace && blockIdx.x == 0 && q < (uint32_t)kTraceRing)
-    g.trace[(size_t)g.trace_ctas * g.n_stages * kTraceMarks + (size_t)q * 2 + which] = global_timer_ns();
+    g.trace[(size_t)g.trace_ctas * g.n_stages * kTraceMarks + (size_t)q * 4 + which] = global_timer_ns();
 }
 __device__ __forceinline__ void trace_mark(const Globals& g, int which) {
   if (g.trace && threadIdx.x == 0) {
@@ -1489,7 +1490,10 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
               da += da_step;
               db += db_step;
             }
-            if (e == slot_end) tc_commit(&ring->empty[slot]);  // the slot is free once these MMAs are done
+            if (e == slot_end) {
+            tc_commit(&ring->empty[slot]);  // the slot is free once these MMAs are done
+            trace_ring(g, q + (uint32_t)j, 2);
+          }
           }
           s = e;
         }
