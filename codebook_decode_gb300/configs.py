@@ -76,6 +76,9 @@ WORKLOADS = {
                         False, 2),
     "full_b32": Workload("full_b32", FULL, 32, ("uniform", 100, 1000), ("uniform", 0, 200), 256, 0.9, 50, 1.05,
                          True, False, 3),
+    # full widths with 2 Talker layers at B = 32: the tensor-path small case for profiler captures
+    "full2l_b32": Workload("full2l_b32", Dims(**{**FULL.as_dict(), "n_layers": 2}), 32, ("uniform", 100, 1000),
+                           ("uniform", 0, 200), 256, 0.9, 50, 1.05, True, False, 3),
     "int8_b1": Workload("int8_b1", FULL, 1, ("uniform", 64, 512), ("fixed", 0), 128, 0.9, 50, 1.05, True, True, 4),
     "int8_b32": Workload("int8_b32", FULL, 32, ("uniform", 64, 512), ("fixed", 0), 128, 0.9, 50, 1.05, True,
                          True, 4),
