@@ -136,6 +136,15 @@ class Sessions:
         a = r.standard_normal(size=(self.B, d.hidden), dtype=np.float32) * np.float32(0.08)
         return bf16_bits(a)
 
+    def prompt_embeds(self, n_tok, chunk=0):
+        """Prompt embeddings for a Talker prefill: [n_tok][B][hidden] bf16
+        bits, like the frame inputs (chunk: which prompt chunk, for distinct
+        draws)."""
+        d = self.d
+        r = _rng(self.seed, f"prompt_embeds.{chunk}")
+        a = r.standard_normal(size=(n_tok, self.B, d.hidden), dtype=np.float32) * np.float32(0.08)
+        return bf16_bits(a)
+
     def text_embeds(self, frame):
         d = self.d
         r = _rng(self.seed, f"text_embeds.{frame}")

@@ -96,6 +96,8 @@ def _declare(L):
     L.orc_frame_step.argtypes = [C.POINTER(Model), i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
     L.orc_frame_step.restype = i32
     L.orc_feedback.argtypes = [C.POINTER(Model), i32, vp, vp, vp]
+    L.orc_talker_prefill.argtypes = [C.POINTER(Model), i32, vp, vp, i32, vp, i32]
+    L.orc_talker_prefill.restype = i32
 
 
 def _p(a):
@@ -192,6 +194,22 @@ class Oracle:
         for b in range(B):
             sess_rows[b, 0] = sess[b].kv_len
         return codes, eos, logits
+
+    def talker_prefill(self, sess_rows, kv_list, kv_cap, embeds):
+        """Prompt tokens through the Talker layers (no head, no sampling):
+        embeds [n_tok][B][hidden] bf16 bits; token t of session b at position
+        kv_len_b + t, its K/V written into kv_list[b]; kv_len advanced in
+        place by n_tok."""
+        B = sess_rows.shape[0]
+        n_tok = embeds.shape[0]
+        sess = (Session * B)(*[session_struct(sess_rows[b]) for b in range(B)])
+        ptrs = (C.c_void_p * B)(*[k.ctypes.data for k in kv_list])
+        e = np.ascontiguousarray(embeds, dtype=np.uint16)
+        rc = self.L.orc_talker_prefill(C.byref(self.m), B, C.addressof(sess), C.addressof(ptrs), kv_cap, _p(e), n_tok)
+        if rc != 0:
+            raise RuntimeError(f"orc_talker_prefill failed: {rc}")
+        for b in range(B):
+            sess_rows[b, 0] = sess[b].kv_len
 
     def feedback(self, codes, text):
         B = codes.shape[0]

@@ -475,6 +475,33 @@ int orc_frame_step(const orc_model* m, int B, orc_session* sess, uint16_t* const
   return 0;
 }
 
+/* Talker prefill (header): the decode step's Talker layers, one prompt token
+ * after another, which is the causal prompt pass the pages describe the
+ * serving stacks running before the first frame. */
+int orc_talker_prefill(const orc_model* m, int B, orc_session* sess, uint16_t* const* kv, int kv_cap,
+                       const uint16_t* embeds, int n_tok) {
+  const orc_dims* D = &m->d;
+  const int H = D->hidden;
+  layer_dims tl = {H, D->n_q_heads, D->n_kv_heads, D->head_dim, D->ffn, D->rms_eps, D->rope_theta};
+  const size_t t_tok = (size_t)D->n_kv_heads * D->head_dim;
+  for (int b = 0; b < B; b++)
+    if (sess[b].kv_len < 0 || sess[b].kv_len + n_tok > kv_cap) return -1;
+  double* x = (double*)malloc(sizeof(double) * (size_t)H);
+  for (int b = 0; b < B; b++) {
+    for (int t = 0; t < n_tok; t++) {
+      const int pos = sess[b].kv_len + t;
+      for (int i = 0; i < H; i++) x[i] = orc_from_bf16(embeds[((size_t)t * B + b) * H + i]);
+      for (int l = 0; l < D->n_layers; l++) {
+        uint16_t* kc = kv[b] + (size_t)l * 2 * kv_cap * t_tok;
+        run_layer(&m->talker[l], &tl, m->use_int8, x, pos, kc, kc + (size_t)kv_cap * t_tok);
+      }
+    }
+    sess[b].kv_len += n_tok;
+  }
+  free(x);
+  return 0;
+}
+
 void orc_feedback(const orc_model* m, int B, const int32_t* codes, const uint16_t* text, double* out) {
   const int H = m->d.hidden, NCB = m->d.n_codebooks;
   for (int b = 0; b < B; b++) {

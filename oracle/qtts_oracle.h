@@ -110,6 +110,14 @@ int orc_frame_step(const orc_model* m, int B, orc_session* sess, uint16_t* const
 /* next_in[b] = text[b] + sum_j E_j[codes[b][j]]  (free-running feedback) */
 void orc_feedback(const orc_model* m, int B, const int32_t* codes, const uint16_t* text, double* out);
 
+/* ---- Talker prefill: a prompt's tokens through the Talker layers ----
+ * For each session b and prompt token t = 0..n_tok-1 (in order): the Talker
+ * layers at position kv_len_b + t on input embeds[t][b] (bf16 [n_tok][B]
+ * [hidden]), writing that position's K/V into kv[b] as the decode step does;
+ * no head, no sampling. kv_len advanced by n_tok. -1 if a session lacks room. */
+int orc_talker_prefill(const orc_model* m, int B, orc_session* sess, uint16_t* const* kv, int kv_cap,
+                       const uint16_t* embeds, int n_tok);
+
 #ifdef __cplusplus
 }
 #endif
