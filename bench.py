@@ -186,6 +186,53 @@ def trace_summary(d, stamps):
                        for k, v in out.items()}}
 
 
+def talker_pass_weight_bytes(d, int8):
+    """Weight bytes one Talker pass streams (QKV, O, gate/up, down of every
+    layer; int8 per-row scales are negligible)."""
+    per_layer = ((d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim * d.hidden + d.hidden * d.n_q_heads * d.head_dim
+                 + 2 * d.ffn * d.hidden + d.hidden * d.ffn)
+    return d.n_layers * per_layer * (1 if int8 else 2)
+
+
+def run_prefill(wl, n_tok, reps, local, weights):
+    """Talker prefill throughput: every session of the workload takes an
+    n_tok-token prompt after its prefix (kv_len rewound between repetitions,
+    median of reps timed with CUDA events on the launching stream)."""
+    import torch
+
+    from codebook_decode_gb300 import qtts
+    from codebook_decode_gb300.engine import Engine, to_dev_u16
+
+    d = wl.dims
+    sess = synth.make_sessions(wl)
+    cap = int(sess.kv_len0.max()) + n_tok + 4
+    pool = wl.batch * ((cap + 15) // 16) + 8
+    eng = Engine(d, weights, max_batch=wl.batch, max_context=cap, pool_pages=pool, device=local, int8=wl.int8)
+    eng.setup_sessions(sess, cap, shuffle=wl.shuffle_pages)
+    sess0 = eng.sess.clone()
+    e = to_dev_u16(sess.prompt_embeds(n_tok), eng.dev)
+    stream = torch.cuda.current_stream()
+    eng.prefill(e, stream)  # warm-up
+    times = []
+    for _ in range(reps):
+        eng.sess.copy_(sess0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        eng.prefill(e, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    rc, derr = qtts.qtts_frame_status(eng.m, raise_on_error=False)
+    assert rc == 0 and derr == 0, (rc, derr)
+    ms = statistics.median(times)
+    t_tok = d.n_layers * 2 * d.n_kv_heads * d.head_dim * 2  # K and V of one token, all layers
+    kv = sum(sum(int(n0) + t + 1 for t in range(n_tok)) for n0 in sess.kv_len0) * t_tok + wl.batch * n_tok * t_tok
+    nbytes = n_tok * talker_pass_weight_bytes(d, wl.int8) + kv
+    eng.release_pages()
+    eng.close()
+    return dict(tokens_per_s=wl.batch * n_tok / (ms / 1e3), ms=ms, bytes=nbytes, achieved_gbs=nbytes / (ms / 1e3) / 1e9)
+
+
 def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, trace_file=None, tc_min_rows=None,
             ksplit_min_rows=None):
     import torch
@@ -423,6 +470,13 @@ def main():
                 sweep[name] = {"frames_per_s": o.batch * min(args.steps, 50) / (rr["total_ms"] / 1e3),
                                "frame_ms": rr["frame_ms"], "achieved_gbs": rr["achieved_gbs"],
                                "frac": rr["achieved_gbs"] / peak, "bytes_per_frame": rr["bytes_per_frame"]}
+            for name, n_tok in (("full_b1", 64), ("full_b8", 64)):
+                o = configs.WORKLOADS[name]
+                rp = run_prefill(o, n_tok, 3, local, w)
+                sweep[f"prefill_{name}_{n_tok}tok"] = {
+                    "tokens_per_s": rp["tokens_per_s"], "ms": rp["ms"], "achieved_gbs": rp["achieved_gbs"],
+                    "frac": rp["achieved_gbs"] / peak, "bytes": rp["bytes"],
+                    "what": f"Talker prefill of {n_tok} prompt tokens for each of {o.batch} session(s), one pass per token"}
             line["sweep"] = sweep
         print(json.dumps(line))
     barrier(ws)

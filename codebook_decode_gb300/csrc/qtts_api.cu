@@ -548,6 +548,21 @@ enum FramePart { PART_ALL = 0, PART_TALKER = 1, PART_CP = 2 };
 // Launch all of a frame's stages, or its Talker half (through sampler 0) or
 // its Code-Predictor half (the 15 steps), which reuses the Talker half's tag
 // base: its first stages read words the Talker half wrote.
+// Tag base of the next launch over the program: stage s writes tag0 + s;
+// tags only grow, so no word left by an earlier launch matches. Before they
+// would wrap, the tagged buffers are cleared and the count restarts.
+int take_tag0(qtts_model* m, uint32_t* tag0) {
+  if ((uint64_t)(m->frame_seq + 2) * (uint64_t)m->n_stages >= 0xFFFFFFFFull) {
+    CK(m, cudaDeviceSynchronize());
+    CK(m, cudaMemset(m->acts.base, 0, m->acts.words * sizeof(uint64_t)));
+    if (m->g.kpart) CK(m, cudaMemset(m->g.kpart, 0, (size_t)(2 * m->g.kpart_words) * sizeof(uint64_t)));
+    m->frame_seq = 0;
+  }
+  ++m->frame_seq;
+  *tag0 = m->frame_seq * (uint32_t)m->n_stages;
+  return QTTS_OK;
+}
+
 int frame_part(qtts_model* m, int part, int B, qtts_session* sess, const int32_t* bt, int bt_stride,
                const uint16_t* in_embeds, qtts_rng* rng, uint32_t* seen, const int32_t* forced, int32_t* codes_out,
                uint8_t* eos_out, float* logits_out, void* stream) {
@@ -575,17 +590,8 @@ int frame_part(qtts_model* m, int part, int B, qtts_session* sess, const int32_t
   if (part == PART_CP) {
     fa.tag0 = m->cp_tag0;
   } else {
-    // tag base: stage s of this frame writes tag0 + s; tags only grow, so no
-    // word left by an earlier frame matches. Before they would wrap, the
-    // buffers are cleared and the count restarts.
-    if ((uint64_t)(m->frame_seq + 2) * (uint64_t)m->n_stages >= 0xFFFFFFFFull) {
-      CK(m, cudaDeviceSynchronize());
-      CK(m, cudaMemset(m->acts.base, 0, m->acts.words * sizeof(uint64_t)));
-      if (m->g.kpart) CK(m, cudaMemset(m->g.kpart, 0, (size_t)(2 * m->g.kpart_words) * sizeof(uint64_t)));
-      m->frame_seq = 0;
-    }
-    ++m->frame_seq;
-    fa.tag0 = m->frame_seq * (uint32_t)m->n_stages;
+    int rc = take_tag0(m, &fa.tag0);
+    if (rc) return rc;
   }
   const int s0 = part == PART_CP ? m->s_cp : 0;
   const int s1 = part == PART_TALKER ? m->s_cp : m->n_stages;
@@ -1042,6 +1048,35 @@ int qtts_frame_cp(qtts_model* m, int B, qtts_session* sess, const int32_t* bt, i
                   int32_t* codes_out, uint8_t* eos_out, float* logits_out, void* stream) {
   return frame_part(m, PART_CP, B, sess, bt, bt_stride, in_embeds, rng, seen, forced, codes_out, eos_out, logits_out,
                     stream);
+}
+
+int qtts_talker_prefill(qtts_model* m, int B, qtts_session* sess, const int32_t* bt, int bt_stride,
+                        const uint16_t* embeds, int n_tok, void* stream) {
+  if (!m) return fail(m, QTTS_E_INVALID, "null model");
+  if (!m->loaded) return fail(m, QTTS_E_STATE, "load weights first");
+  if (B < 1 || B > m->cfg.max_batch) return fail(m, QTTS_E_BATCH, "B=%d outside 1..%d", B, m->cfg.max_batch);
+  if (!sess || !bt || bt_stride < 1 || (n_tok > 0 && !embeds) || n_tok < 0)
+    return fail(m, QTTS_E_INVALID, "null array, bad block-table stride or negative token count");
+  if (m->cp_pending) return fail(m, QTTS_E_STATE, "a split frame waits for qtts_frame_cp");
+  cudaSetDevice(m->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int s1 = 1 + 5 * m->cfg.n_layers;  // the begin stage and the Talker layers
+  for (int t = 0; t < n_tok; ++t) {
+    FrameArgs fa{};
+    fa.B = B;
+    fa.sess = sess;
+    fa.bt = bt;
+    fa.bt_stride = bt_stride;
+    fa.in_embeds = embeds + (size_t)t * B * m->cfg.hidden;
+    int rc = take_tag0(m, &fa.tag0);
+    if (rc) return rc;
+    cudaError_t e = launch_frame(m->prog_dev[m->use_int8 ? 1 : 0], 0, s1, m->g, fa, m->stepwise, s);
+    if (e != cudaSuccess) return cuda_fail(m, e, "prefill launch");
+    e = launch_advance_kv(sess, B, m->g.err, s);
+    if (e != cudaSuccess) return cuda_fail(m, e, "prefill kv_len advance");
+  }
+  m->last_stream = s;
+  return QTTS_OK;
 }
 
 int qtts_frame_steps(qtts_model* m, int n_frames, int B, qtts_session* sess, const int32_t* bt, int bt_stride,

@@ -192,4 +192,16 @@ cudaError_t launch_tile_weights_i8(const int8_t* w, int N, int K, int G, int8_t*
   return cudaGetLastError();
 }
 
+// After a prefill pass: every session's kv_len advances by one, unless the
+// pass set the device error word (then nothing was appended consistently).
+__global__ void advance_kv_kernel(qtts_session* sess, int B, const int* err) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B && *(const volatile int*)err == 0) sess[b].kv_len += 1;
+}
+
+cudaError_t launch_advance_kv(qtts_session* sess, int B, const int* err, cudaStream_t s) {
+  advance_kv_kernel<<<1, 32, 0, s>>>(sess, B, err);
+  return cudaGetLastError();
+}
+
 }  // namespace qtts

@@ -103,6 +103,12 @@ class Engine:
         qtts.qtts_frame_step(self.m, self.B, self.sess, self.bt, self.bt_stride, in_embeds, self.rng, self.seen,
                              forced, self.codes, self.eos, self.logits if want_logits else None, stream)
 
+    def prefill(self, embeds, stream=None):
+        """embeds: device int16 tensor [n_tok][B][H] of bf16 bits: the prompt
+        through the Talker, K/V appended, kv_len advanced."""
+        qtts.qtts_talker_prefill(self.m, self.B, self.sess, self.bt, self.bt_stride, embeds, int(embeds.shape[0]),
+                                 stream)
+
     def read_kv(self, b, layer, n_tok):
         d = self.d
         k = np.zeros((n_tok, d.n_kv_heads, d.head_dim), dtype=np.uint16)

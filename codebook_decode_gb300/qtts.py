@@ -87,6 +87,7 @@ SIGNATURES = [
     ("qtts_frame_talker", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
     ("qtts_frame_cp", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
     ("qtts_frame_steps", C.c_int, [_P, C.c_int, C.c_int, _P, _P, C.c_int] + [_P] * 8),
+    ("qtts_talker_prefill", C.c_int, [_P, C.c_int, _P, _P, C.c_int, _P, C.c_int, _P]),
     ("qtts_frame_status", C.c_int, [_P, C.POINTER(C.c_int)]),
     ("qtts_feedback_embed", C.c_int, [_P, C.c_int, _P, _P, _P, _P]),
     ("qtts_sample", C.c_int, [_P, C.c_int, C.c_int, _P, C.c_int, _P, _P, _P, _P, _P]),
@@ -237,6 +238,11 @@ def qtts_frame_steps(m, n_frames, B, sessions, block_tables, bt_stride, in_embed
     return _check(m, load_library().qtts_frame_steps(
         m, n_frames, B, ptr(sessions), ptr(block_tables), bt_stride, ptr(in_embeds), ptr(text_embeds), ptr(rng),
         ptr(seen), ptr(forced_codes), ptr(codes_out), ptr(eos_out), _stream(stream)))
+
+
+def qtts_talker_prefill(m, B, sessions, block_tables, bt_stride, embeds, n_tok, stream=None):
+    return _check(m, load_library().qtts_talker_prefill(
+        m, B, ptr(sessions), ptr(block_tables), bt_stride, ptr(embeds), n_tok, _stream(stream)))
 
 
 def qtts_frame_status(m, raise_on_error=True):

@@ -1,0 +1,112 @@
+"""GPU parity of the Talker prefill (qtts_talker_prefill) against the oracle's
+prompt pass: appended K/V to bf16 rounding at every layer and position,
+kv_len advanced by the prompt length, and the first decode frames after the
+prompt within the logit tolerance; on the CUDA-core and tensor-core GEMV
+paths, BF16 and INT8, with ragged prefixes across page boundaries."""
+import numpy as np
+import pytest
+import torch
+
+from codebook_decode_gb300 import configs, qtts, synth
+from codebook_decode_gb300.engine import to_dev_u16
+from gpu_helpers import TOL_BF16, TOL_INT8, ParityRun, free
+
+pytestmark = pytest.mark.gpu
+
+TINY = configs.TINY
+
+
+@pytest.fixture(scope="module")
+def tiny_w():
+    return synth.make_weights(TINY, 1000)
+
+
+def sessions(d, B, prefixes, frames):
+    return synth.Sessions(d, B, prefixes[:B], [0] * B, frames, 2100 + B, temperature=0.9, top_k=50,
+                          rep_penalty=1.05)
+
+
+@pytest.mark.parametrize("B,n_tok,tc_min,int8", [(1, 20, None, False), (3, 37, None, False), (9, 18, None, False),
+                                                 (3, 21, 1, False), (9, 17, None, True), (2, 19, None, True)])
+def test_prefill_matches_oracle(tiny_w, B, n_tok, tc_min, int8):
+    prefixes = [5, 16, 31, 0, 44, 9, 15, 33, 2]
+    s = sessions(TINY, B, prefixes, n_tok + 3)
+    run = ParityRun(TINY, tiny_w, s, n_tok + 2, shuffle=True, int8=int8, tc_min_rows=tc_min)  # room for prompt + 2 frames
+    try:
+        e = s.prompt_embeds(n_tok)
+        run.eng.prefill(to_dev_u16(e, run.eng.dev))
+        rc, derr = run.eng.status()
+        assert rc == 0 and derr == 0, (rc, derr)
+        run.O.talker_prefill(run.rows, run.kv, run.cap, e)
+        run.check_state()
+        run.check_kv()
+        # the frames after the prompt read its cache
+        run.run(frames=2)
+        assert run.max_rel() < (TOL_INT8 if int8 else TOL_BF16), run.max_rel()
+        assert run.confident_agree == run.confident
+        run.check_state()
+        run.check_kv()
+    finally:
+        free(run)
+
+
+def test_prefill_in_chunks_equals_one_call(tiny_w):
+    """Two calls of 7 and 12 tokens leave the same bits as one call of 19."""
+    s = sessions(TINY, 3, [4, 17, 30], 22)
+    e = s.prompt_embeds(19)
+    caches = []
+    for split in (None, 7):
+        run = ParityRun(TINY, tiny_w, s, 20, shuffle=True)
+        try:
+            if split is None:
+                run.eng.prefill(to_dev_u16(e, run.eng.dev))
+            else:
+                run.eng.prefill(to_dev_u16(e[:split], run.eng.dev))
+                run.eng.prefill(to_dev_u16(e[split:], run.eng.dev))
+            assert run.eng.status() == (0, 0)
+            n = run.eng.sess.cpu().numpy()[:, 0]
+            assert np.array_equal(n, s.kv_len0 + 19)
+            caches.append([run.eng.read_kv(b, l, int(n[b])) for b in range(3) for l in range(TINY.n_layers)])
+        finally:
+            free(run)
+    for (k0, v0), (k1, v1) in zip(*caches):
+        assert np.array_equal(k0, k1) and np.array_equal(v0, v1)
+
+
+def test_prefill_refused_inside_a_split_frame(tiny_w):
+    s = sessions(TINY, 1, [8], 4)
+    run = ParityRun(TINY, tiny_w, s, 1, shuffle=False)
+    try:
+        eng = run.eng
+        emb = to_dev_u16(s.in_embeds(0), eng.dev)
+        qtts.qtts_frame_talker(eng.m, eng.B, eng.sess, eng.bt, eng.bt_stride, emb, eng.rng, eng.seen, None,
+                               eng.codes, eng.eos, None)
+        e = to_dev_u16(s.prompt_embeds(2), eng.dev)
+        with pytest.raises(RuntimeError):
+            eng.prefill(e)
+        qtts.qtts_frame_cp(eng.m, eng.B, eng.sess, eng.bt, eng.bt_stride, emb, eng.rng, eng.seen, None, eng.codes,
+                           eng.eos, None)
+        torch.cuda.synchronize()
+        assert eng.status() == (0, 0)
+    finally:
+        free(run)
+
+
+def test_full_size_prefill(tiny_w):
+    """Full widths and depth, B = 2, a 40-token prompt: the cache of the first
+    and last layers against the oracle, then one frame's logits."""
+    d = configs.FULL
+    w = synth.make_weights(d, 1001)
+    s = sessions(d, 2, [128, 77], 44)
+    run = ParityRun(d, w, s, 42, shuffle=True)
+    try:
+        e = s.prompt_embeds(40)
+        run.eng.prefill(to_dev_u16(e, run.eng.dev))
+        assert run.eng.status() == (0, 0)
+        run.O.talker_prefill(run.rows, run.kv, run.cap, e)
+        run.check_state()
+        run.check_kv(layers=[0, d.n_layers - 1])
+        run.run(frames=1)
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+    finally:
+        free(run)
