@@ -871,14 +871,18 @@ __device__ __forceinline__ int ring_rt(const StageDesc& d, int B) {
 // and the compute warps evaluate the same rule.
 enum GemvMode { GM_RING = 0, GM_TC = 1, GM_DIRECT = 2 };
 // Whether a tensor-path segment takes its K-split partition (tc_ksplit) for
-// `rows` activation rows.
-__device__ __forceinline__ bool tc_split(const Seg& sg, int rows, const Globals& g) {
-  return sg.wtk != nullptr && rows >= g.ksplit_min_rows;
+// `rows` activation rows of K: from ksplit_min_rows rows up, or when the
+// activation words one CTA would stage alone (rows x K) reach kTcSplitWords
+// (at B = 8 only the 6144-deep down projection: its one-slice staging costs
+// more than the partial-sum exchange).
+constexpr int kTcSplitWords = 8 * 6144;
+__device__ __forceinline__ bool tc_split(const Seg& sg, int rows, int K, const Globals& g) {
+  return sg.wtk != nullptr && (rows >= g.ksplit_min_rows || rows * K >= kTcSplitWords);
 }
 __device__ __forceinline__ int gemv_mode(const StageDesc& d, int B, const Globals& g) {
   const int rows = B * d.rps;
   bool tc = rows >= g.tc_min_rows && rows <= kTcMaxActRows && d.K % kTcK == 0;
-  for (int s = 0; s < d.nseg; ++s) tc = tc && (tc_split(d.seg[s], rows, g) || d.seg[s].wt != nullptr);
+  for (int s = 0; s < d.nseg; ++s) tc = tc && (tc_split(d.seg[s], rows, d.K, g) || d.seg[s].wt != nullptr);
   if (tc) return GM_TC;
   return ring_rt(d, B) > 0 ? GM_RING : GM_DIRECT;
 }
@@ -1397,7 +1401,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
   uint32_t xuse = ts->xuse, nseg = ts->nseg;
   for (int si = 0; si < d.nseg; ++si) {
     const Seg& sg = d.seg[si];
-    const TcShare sh(sg, K, tc_split(sg, rows, g));
+    const TcShare sh(sg, K, tc_split(sg, rows, K, g));
     if (sh.rows == 0) continue;  // no rows of this segment on this CTA (the same on all its threads)
     // chunks, K steps and passes below count from the start of the share's K range
     const int nch = sh.nkc, nks = nch * (kTcK / 16);
@@ -1546,7 +1550,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
     if (sh.S > 1) {
       long long off = 0;
       for (int sp = 0; sp < si; ++sp)
-        if (tc_split(d.seg[sp], rows, g)) off += tc_kpart_words(d.seg[sp].N, K, (int)gridDim.x, kTcMaxActRows);
+        if (tc_split(d.seg[sp], rows, K, g)) off += tc_kpart_words(d.seg[sp].N, K, (int)gridDim.x, kTcMaxActRows);
       kp = g.kpart + (size_t)((tag - fa.tag0) & 1u) * (size_t)g.kpart_words + (size_t)off;
     }
     const int n_base = sh.g0 * kTcRows;
@@ -1784,7 +1788,7 @@ __device__ void producer(const StageDesc* prog, int s0, int s1, const Globals& g
     const int K = d.K;
     if (mode == GM_TC) {
       for (int si = 0; si < d.nseg && ok; ++si) {
-        const TcShare sh(d.seg[si], K, tc_split(d.seg[si], fa.B * d.rps, g));
+        const TcShare sh(d.seg[si], K, tc_split(d.seg[si], fa.B * d.rps, K, g));
         // the share's K range is contiguous in its slice of the packed tiles;
         // int8 tiles land in the slot's upper half (the compute side widens them)
         const int gstep = sh.rows * 16 * sh.es;  // tile bytes per 16-wide K step

@@ -319,8 +319,9 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
  *   QTTS_OPT_KSPLIT_MIN_ROWS 1..65: from this many activation rows up, a
  *                      tensor-path GEMV splits K across groups of CTAs
  *                      whose partial sums one CTA per group adds (fewer
- *                      activation words per CTA, one more exchange);
- *                      65: never. Default 16. */
+ *                      activation words per CTA, one more exchange); below
+ *                      it only GEMVs of at least 8 x 6144 activation values
+ *                      (rows x K) split. Default 16. */
 #define QTTS_OPT_STEPWISE 1
 #define QTTS_OPT_TRACE 3
 #define QTTS_OPT_RING_SLOTS 4
