@@ -403,7 +403,7 @@ def main():
     ap.add_argument("--tc-min-rows", type=int, default=None,
                     help="fewest activation rows a GEMV takes on the tensor cores (library default 8; 65: off)")
     ap.add_argument("--ksplit-min-rows", type=int, default=None,
-                    help="fewest activation rows for the K-split tensor-core GEMV (library default 16; below it only the deepest GEMVs split)")
+                    help="fewest activation rows for the K-split tensor-core GEMV (library default 8; below it only the deepest GEMVs split)")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
     ws, rank, local = (1, 0, 0)

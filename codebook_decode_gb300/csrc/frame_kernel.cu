@@ -865,10 +865,9 @@ __device__ __forceinline__ int ring_rt(const StageDesc& d, int B) {
 
 // How a GEMV stage runs for batch B: ring path (few rows: CUDA-core dot
 // products from the weight ring), tensor path (from g.tc_min_rows up to 64
-// rows, bf16 weights with a tensor-tile copy, K a multiple of 128: tcgen05
-// MMAs from the weight ring),
-// else direct path (CUDA cores, weights loaded by the lanes). The producer
-// and the compute warps evaluate the same rule.
+// rows, weights with a tensor-tile copy, K a multiple of 128: tcgen05 MMAs
+// from the weight ring), else direct path (CUDA cores, weights loaded by the
+// lanes). The producer and the compute warps evaluate the same rule.
 enum GemvMode { GM_RING = 0, GM_TC = 1, GM_DIRECT = 2 };
 // Whether a tensor-path segment takes its K-split partition (tc_ksplit) for
 // `rows` activation rows of K: from ksplit_min_rows rows up, or when the
@@ -1365,8 +1364,10 @@ constexpr int kTcIssuer = kCWarps - 1;    // the warp whose lane 0 issues the MM
 constexpr int kTcStagers = kCWarps - 1;   // warps 0.. that stage activations
 constexpr int kTcPairs = (kTcXBytes / 4 / 2 + kTcStagers * 32 - 1) / (kTcStagers * 32);  // word pairs per stager thread per pass
 
-// Tensor path of a GEMV stage (8..64 activation rows, bf16 weights): one
-// tcgen05 MMA per 16-wide K step, M = 128 lanes holding the activation rows
+// Tensor path of a GEMV stage (from g.tc_min_rows up to 64 activation rows;
+// bf16 weights, or int8 ones widened to bf16 in the ring slot and scaled per
+// row in the epilogue): one tcgen05 MMA per 16-wide K step of this CTA's K
+// range (all of K, or its K-slice, tc_ksplit), M = 128 lanes holding the activation rows
 // twice, bf16 high parts (times the RMSNorm gain) in lanes 0..rows-1 and the
 // bf16 low parts x - hi in lanes rows..2 rows-1, so hi + lo carries about 16
 // mantissa bits of each fp32 activation (the other lanes read whatever follows
@@ -1375,8 +1376,9 @@ constexpr int kTcPairs = (kTcXBytes / 4 / 2 + kTcStagers * 32 - 1) / (kTcStagers
 // TMEM over all of K. Stager warps fill 32 KB activation tiles (several
 // 128-wide K chunks per pass, two buffers) while the issuer's MMAs read the
 // other buffer; a commit frees each weight slot and activation buffer when its
-// MMAs are done. The epilogue adds the hi and lo lanes, applies 1/rms and runs
-// the stage's epilogue.
+// MMAs are done. The epilogue adds the hi and lo lanes; a CTA of a later
+// K-slice then hands its partial sums to slice 0, which adds them, applies
+// 1/rms and runs the stage's epilogue.
 __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
                               unsigned char* smem, Ring* ring, TcState* ts, uint32_t& q) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1495,9 +1497,9 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
               db += db_step;
             }
             if (e == slot_end) {
-            tc_commit(&ring->empty[slot]);  // the slot is free once these MMAs are done
-            trace_ring(g, q + (uint32_t)j, 2);
-          }
+              tc_commit(&ring->empty[slot]);  // the slot is free once these MMAs are done
+              trace_ring(g, q + (uint32_t)j, 2);
+            }
           }
           s = e;
         }

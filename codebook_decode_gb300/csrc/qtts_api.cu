@@ -696,7 +696,7 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
   g.max_context = c.max_context; g.eps = c.rms_eps; g.G = sms; g.pool_pages = c.kv_pool_pages;
   g.ring_slots = 8;
   g.tc_min_rows = 8;
-  g.ksplit_min_rows = 16;
+  g.ksplit_min_rows = 8;
 
   const size_t kv_elems = (size_t)c.n_layers * c.kv_pool_pages * 2 * c.n_kv_heads * kPage * c.head_dim;
   if ((rc = dalloc(m, &m->kv_pool, kv_elems))) return bail(rc);

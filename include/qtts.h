@@ -321,7 +321,7 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
  *                      whose partial sums one CTA per group adds (fewer
  *                      activation words per CTA, one more exchange); below
  *                      it only GEMVs of at least 8 x 6144 activation values
- *                      (rows x K) split. Default 16. */
+ *                      (rows x K) split. Default 8. */
 #define QTTS_OPT_STEPWISE 1
 #define QTTS_OPT_TRACE 3
 #define QTTS_OPT_RING_SLOTS 4
