@@ -101,6 +101,8 @@ struct qtts_model {
 
   // staging for qtts_frame_step_host
   qtts_session* st_sess = nullptr;
+  qtts_session* pf_sess = nullptr;  // prefill pass rows as sessions (one per prompt token and session)
+  int32_t* pf_bt = nullptr;         // their block-table rows
   int32_t* st_bt = nullptr;
   int st_bt_cap = 0;
   uint16_t* st_in = nullptr;
@@ -773,6 +775,8 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
   }
   // staging for the host-buffer frame
   m->st_bt_cap = (c.max_context + kPage - 1) / kPage;
+  if ((rc = dalloc(m, &m->pf_sess, kMaxBatch)) || (rc = dalloc(m, &m->pf_bt, (size_t)kMaxBatch * m->st_bt_cap)))
+    return bail(rc);
   if ((rc = dalloc(m, &m->st_sess, kMaxBatch)) || (rc = dalloc(m, &m->st_bt, (size_t)kMaxBatch * m->st_bt_cap)) ||
       (rc = dalloc(m, &m->st_in, (size_t)kMaxBatch * c.hidden)) || (rc = dalloc(m, &m->st_rng, kMaxBatch)) ||
       (rc = dalloc(m, &m->st_seen, (size_t)kMaxBatch * seen_words(c))) ||
@@ -1057,23 +1061,47 @@ int qtts_talker_prefill(qtts_model* m, int B, qtts_session* sess, const int32_t*
   if (B < 1 || B > m->cfg.max_batch) return fail(m, QTTS_E_BATCH, "B=%d outside 1..%d", B, m->cfg.max_batch);
   if (!sess || !bt || bt_stride < 1 || (n_tok > 0 && !embeds) || n_tok < 0)
     return fail(m, QTTS_E_INVALID, "null array, bad block-table stride or negative token count");
+  if (bt_stride > m->st_bt_cap) return fail(m, QTTS_E_INVALID, "bt_stride %d exceeds %d", bt_stride, m->st_bt_cap);
   if (m->cp_pending) return fail(m, QTTS_E_STATE, "a split frame waits for qtts_frame_cp");
   cudaSetDevice(m->device);
   cudaStream_t s = (cudaStream_t)stream;
-  const int s1 = 1 + 5 * m->cfg.n_layers;  // the begin stage and the Talker layers
-  for (int t = 0; t < n_tok; ++t) {
+  const int L = m->cfg.n_layers, H = m->cfg.hidden;
+  const StageDesc* prog = m->prog_dev[m->use_int8 ? 1 : 0];
+  // P prompt tokens of every session per pass: B x P rows (up to the
+  // kMaxBatch rows every per-session buffer holds), each a session of its own
+  // at kv_len + p (row p B + b; embeds are already in that order)
+  const int P_max = std::max(1, kMaxBatch / B);
+  for (int t0 = 0; t0 < n_tok;) {
+    const int P = std::min(P_max, n_tok - t0);
     FrameArgs fa{};
-    fa.B = B;
-    fa.sess = sess;
-    fa.bt = bt;
+    fa.B = B * P;
     fa.bt_stride = bt_stride;
-    fa.in_embeds = embeds + (size_t)t * B * m->cfg.hidden;
-    int rc = take_tag0(m, &fa.tag0);
+    fa.in_embeds = embeds + (size_t)t0 * B * H;
+    if (P == 1) {
+      fa.sess = sess;
+      fa.bt = bt;
+    } else {
+      CK(m, launch_prefill_rows(sess, bt, bt_stride, B, P, m->pf_sess, m->pf_bt, s));
+      fa.sess = m->pf_sess;
+      fa.bt = m->pf_bt;
+    }
+    int rc = take_tag0(m, &fa.tag0);  // one tag base for every launch of the pass
     if (rc) return rc;
-    cudaError_t e = launch_frame(m->prog_dev[m->use_int8 ? 1 : 0], 0, s1, m->g, fa, m->stepwise, s);
-    if (e != cudaSuccess) return cuda_fail(m, e, "prefill launch");
-    e = launch_advance_kv(sess, B, m->g.err, s);
-    if (e != cudaSuccess) return cuda_fail(m, e, "prefill kv_len advance");
+    const Globals gl = m->g;
+    // the begin stage and the Talker layers; with several tokens per session
+    // the launches are cut before each attention stage: token p attends to
+    // tokens < p, whose K/V pages the previous launch wrote (a launch boundary
+    // makes them visible), and to its own K/V in the tagged words
+    int s0 = 0;
+    for (int l = 0; l <= L; ++l) {
+      const int s1 = (P == 1 || l == L) ? 1 + 5 * L : 2 + 5 * l;
+      cudaError_t e = launch_frame(prog, s0, s1, gl, fa, m->stepwise, s);
+      if (e != cudaSuccess) return cuda_fail(m, e, "prefill launch");
+      s0 = s1;
+      if (s1 == 1 + 5 * L) break;
+    }
+    CK(m, launch_advance_kv(sess, B, m->g.err, P, s));
+    t0 += P;
   }
   m->last_stream = s;
   return QTTS_OK;

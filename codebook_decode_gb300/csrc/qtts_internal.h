@@ -205,7 +205,9 @@ cudaError_t launch_kv_scatter(uint16_t* pool, int pool_pages, int nkv, int d, in
 // Requires K % kTcK == 0; t holds ceil(N / 16) * 16 * K bf16; G: the grid the slices are cut for.
 cudaError_t launch_tile_weights(const uint16_t* w, int N, int K, int G, uint16_t* t, cudaStream_t s);
 cudaError_t launch_tile_weights_i8(const int8_t* w, int N, int K, int G, int8_t* t, cudaStream_t s);
-cudaError_t launch_advance_kv(qtts_session* sess, int B, const int* err, cudaStream_t s);
+cudaError_t launch_advance_kv(qtts_session* sess, int B, const int* err, int inc, cudaStream_t s);
+cudaError_t launch_prefill_rows(const qtts_session* sess, const int32_t* bt, int bt_stride, int B, int P,
+                                qtts_session* rsess, int32_t* rbt, cudaStream_t s);
 struct EmbedTables {
   const uint16_t* e[kCodebooks];
   int rows[kCodebooks];

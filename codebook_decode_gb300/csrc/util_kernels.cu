@@ -192,15 +192,38 @@ cudaError_t launch_tile_weights_i8(const int8_t* w, int N, int K, int G, int8_t*
   return cudaGetLastError();
 }
 
-// After a prefill pass: every session's kv_len advances by one, unless the
-// pass set the device error word (then nothing was appended consistently).
-__global__ void advance_kv_kernel(qtts_session* sess, int B, const int* err) {
+// After a prefill pass: every session's kv_len advances by the pass's prompt
+// tokens, unless the pass set the device error word (then nothing was
+// appended consistently).
+__global__ void advance_kv_kernel(qtts_session* sess, int B, const int* err, int inc) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B && *(const volatile int*)err == 0) sess[b].kv_len += 1;
+  if (b < B && *(const volatile int*)err == 0) sess[b].kv_len += inc;
 }
 
-cudaError_t launch_advance_kv(qtts_session* sess, int B, const int* err, cudaStream_t s) {
-  advance_kv_kernel<<<1, 32, 0, s>>>(sess, B, err);
+cudaError_t launch_advance_kv(qtts_session* sess, int B, const int* err, int inc, cudaStream_t s) {
+  advance_kv_kernel<<<1, 32, 0, s>>>(sess, B, err, inc);
+  return cudaGetLastError();
+}
+
+// Rows of a prefill pass over P prompt tokens of B sessions: row r = p B + b
+// is token p of session b, a session of its own with kv_len + p and session
+// b's block-table row (its K/V land in b's pages).
+__global__ void prefill_rows_kernel(const qtts_session* sess, const int32_t* bt, int bt_stride, int B, int P,
+                                    qtts_session* rsess, int32_t* rbt) {
+  const int r = blockIdx.x;
+  if (r >= B * P) return;
+  const int p = r / B, b = r - p * B;
+  if (threadIdx.x == 0) {
+    qtts_session x = sess[b];
+    x.kv_len += p;
+    rsess[r] = x;
+  }
+  for (int i = threadIdx.x; i < bt_stride; i += blockDim.x) rbt[(size_t)r * bt_stride + i] = bt[(size_t)b * bt_stride + i];
+}
+
+cudaError_t launch_prefill_rows(const qtts_session* sess, const int32_t* bt, int bt_stride, int B, int P,
+                                qtts_session* rsess, int32_t* rbt, cudaStream_t s) {
+  prefill_rows_kernel<<<B * P, 128, 0, s>>>(sess, bt, bt_stride, B, P, rsess, rbt);
   return cudaGetLastError();
 }
 
