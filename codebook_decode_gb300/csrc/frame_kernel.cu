@@ -1321,28 +1321,40 @@ __device__ void fill_epi_cache(const StageDesc& d, const Globals& g, const Frame
 }
 
 // Widen the int8 weight tiles a bulk copy left in a ring slot's upper half
-// (nraw bytes) to bf16 over the whole slot, element for element (exact: an
-// int8 value is a bf16 with its low 16 float bits zero). One warp, in
-// 512-byte steps whose reads all precede their writes: step c writes bytes
-// [1024 c, 1024 c + 1024), which hold only the raw bytes of steps <= c.
+// (nraw bytes) to bf16 over the whole slot, element for element. Exact: the
+// byte b of value v gives the float 2^23 + (v + 128) when put under the
+// exponent of 2^23 (bits 0x4B000000 | (b ^ 0x80)); subtracting 2^23 + 128
+// leaves v, whose float has its low 16 bits zero, so its top half is the
+// bf16. One warp, in 1024-byte steps whose reads all precede their writes:
+// step c writes bytes [2048 c, 2048 c + 2048), which hold only the raw bytes
+// of steps <= c.
+__device__ __forceinline__ uint32_t widen2(uint32_t x, int i) {  // bytes i, i + 1 of x (bias-flipped) as 2 bf16
+  const float a = __int_as_float((int)__byte_perm(x, 0x4B000000u, 0x7540u + i)) - 8388736.0f;
+  const float b = __int_as_float((int)__byte_perm(x, 0x4B000000u, 0x7541u + i)) - 8388736.0f;
+  return (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u);
+}
 __device__ __forceinline__ void widen_i8_slot(unsigned char* slot, int nraw, int lane) {
   const unsigned char* raw = slot + kSlotBytes / 2;
-  for (int c0 = 0; c0 < nraw; c0 += 512) {
-    const int o = c0 + lane * 16;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (o < nraw) v = *reinterpret_cast<const uint4*>(raw + o);
-    __syncwarp();
-    if (o < nraw) {
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-      uint32_t out[8];
+  for (int c0 = 0; c0 < nraw; c0 += 1024) {
+    uint4 v[2];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t word = in[i >> 1], sh = (i & 1) * 16;
-        const float a = (float)(int8_t)((word >> sh) & 0xFFu), b = (float)(int8_t)((word >> (sh + 8)) & 0xFFu);
-        out[i] = (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u);
+    for (int h = 0; h < 2; ++h) {
+      const int o = c0 + h * 512 + lane * 16;
+      v[h] = o < nraw ? *reinterpret_cast<const uint4*>(raw + o) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int o = c0 + h * 512 + lane * 16;
+      if (o < nraw) {
+        const uint32_t in[4] = {v[h].x ^ 0x80808080u, v[h].y ^ 0x80808080u, v[h].z ^ 0x80808080u,
+                                v[h].w ^ 0x80808080u};
+        uint32_t out[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = widen2(in[i >> 1], (i & 1) * 2);
+        *reinterpret_cast<uint4*>(slot + 2 * o) = make_uint4(out[0], out[1], out[2], out[3]);
+        *reinterpret_cast<uint4*>(slot + 2 * o + 16) = make_uint4(out[4], out[5], out[6], out[7]);
       }
-      *reinterpret_cast<uint4*>(slot + 2 * o) = make_uint4(out[0], out[1], out[2], out[3]);
-      *reinterpret_cast<uint4*>(slot + 2 * o + 16) = make_uint4(out[4], out[5], out[6], out[7]);
     }
     __syncwarp();
   }
