@@ -1086,6 +1086,15 @@ __device__ __forceinline__ void zero_acc(float (&acc)[U][RT]) {
     for (int r = 0; r < RT; ++r) acc[i][r] = 0.f;
 }
 
+// 1/rms of activation row r of the tile (1 without a norm), from the
+// per-warp sums of squares the norm step left before its barrier.
+__device__ __forceinline__ float row_rfac(const StageDesc& d, const Globals& g, const GemvSmemTail* tail, int r) {
+  if (d.xsrc != X_NORM) return 1.0f;
+  float sum = 0.f;
+  for (int w = 0; w < kCWarps; ++w) sum += tail->sqw[r][w];
+  return 1.0f / sqrtf(sum / (float)d.K + g.eps);
+}
+
 // Add one task's dot products to acc: U rows x up to 1024 of K against nr
 // activation rows, from registers already holding the weight vectors.
 template <typename WT, int U, int RT>
@@ -1143,6 +1152,7 @@ __device__ void gemv_ring(const StageDesc& d, const Seg& sg, int si, const SegSh
   const int K = d.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nsl = (uint32_t)g.ring_slots, nsl_shift = (uint32_t)(__ffs(g.ring_slots) - 1);
+  const float rfac = lane < nr ? row_rfac(d, g, tail, lane) : 1.0f;  // lane r: activation row r
   for (int ul = warp; ul < sh.nu; ul += kCWarps) {
     const int sl = ul / sh.upslot;
     const int ua = sl * sh.upslot;
@@ -1190,7 +1200,7 @@ __device__ void gemv_ring(const StageDesc& d, const Seg& sg, int si, const SegSh
 #pragma unroll
         for (int r = 1; r < RT; ++r)
           if (lane == r) v = acc[i][r];
-        v *= tail->rfac[lane];
+        v *= rfac;
         if (sg.scale) v *= ul * U + i < kScaleCache ? tail->ec.scale[si][ul * U + i] : sg.scale[n0 + i];
         y[i] = v;
       }
@@ -1742,16 +1752,9 @@ __device__ __noinline__ bool stage_gemv(const StageDesc& d, uint32_t tag, const 
       cbar();
     }
     trace_mark(g, 1);
-    // 1/rms per row, ready for phase 2 (after the phase-1 barrier)
-    if (tid < nr) {
-      float f = 1.0f;
-      if (norm) {
-        float sum = 0.f;
-        for (int w2 = 0; w2 < kCWarps; ++w2) sum += tail->sqw[tid][w2];
-        f = 1.0f / sqrtf(sum / (float)K + g.eps);
-      }
-      tail->rfac[tid] = f;
-    }
+    // 1/rms per row for phase 2 of the direct path (read after the phase-1
+    // barrier); ring-path warps take it from the partials themselves
+    if (!use_ring && tid < nr) tail->rfac[tid] = row_rfac(d, g, tail, tid);
     for (int s = 0; s < d.nseg; ++s) {
       const Seg& sg = d.seg[s];
       const SegShare sh = s == 0 ? sh0 : SegShare(sg, K);
