@@ -410,13 +410,12 @@ def main():
                     help="fewest activation rows for the K-split tensor-core GEMV (library default 8; below it only the deepest GEMVs split)")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
-    ws, rank, local = (1, 0, 0)
-    if args.impl == "ours" or args.gpus > 1:
-        ws, rank, local = dist_setup()
     cores = os.cpu_count()
 
     if args.impl == "reference":
-        if rank != 0:
+        # the oracle on the host cores: rank 0 alone runs it (no process group
+        # is needed for that); the other ranks of a multi-GPU launch exit
+        if int(os.environ.get("RANK", "0")) != 0:
             return
         w = synth.make_weights(wl.dims, 1000 + wl.seed)
         t = time.perf_counter()
@@ -435,6 +434,7 @@ def main():
         print(json.dumps(line))
         return
 
+    ws, rank, local = dist_setup()
     import torch
     w = synth.make_weights(wl.dims, 1000 + wl.seed)
     barrier(ws)
