@@ -137,9 +137,16 @@ def max_over_ranks(x, ws):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank, seconds, ws):
+    """Units all ranks processed (each rank the same count) over the slowest
+    rank's time."""
+    return ws * units_per_rank / max_over_ranks(seconds, ws)
 
 
 # --------------------------------------------------------------------------
@@ -347,7 +354,7 @@ def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, tra
     e2e_s = time.perf_counter() - t
     h2d = sess_h.nbytes + B * eng.bt_stride * 4 + emb_h.nbytes + rng_h.nbytes + seen_h.nbytes
     d2h = codes_h.nbytes + eos_h.nbytes + sess_h.nbytes + rng_h.nbytes + seen_h.nbytes
-    res["e2e"] = dict(value=B * e2e_steps / e2e_s, h2d=h2d, d2h=d2h)
+    res["e2e"] = dict(value=B * e2e_steps / e2e_s, s=e2e_s, frames=B * e2e_steps, h2d=h2d, d2h=d2h)
     if trace:
         qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_TRACE, 1)
         eng.sess.copy_(sess0)
@@ -457,7 +464,8 @@ def main():
                          "frac": r["achieved_gbs"] / peak, "traffic": ncu_traffic(wl),
                          "peak_kind": peak_kind, "kernel": "qtts::frame_kernel",
                          "bytes_per_launch": r["bytes_per_frame"], "launch_ms": r["frame_ms"]},
-            "e2e": {"value": ws * r["e2e"]["value"], "unit": UNIT, "h2d_bytes_per_step": r["e2e"]["h2d"],
+            "e2e": {"value": whole_job_rate(r["e2e"]["frames"], r["e2e"]["s"], ws), "unit": UNIT,
+                    "h2d_bytes_per_step": r["e2e"]["h2d"],
                     "d2h_bytes_per_step": r["e2e"]["d2h"]},
             "gpu_launches": 2 * args.steps,
             "clocks": r["clocks"]}
