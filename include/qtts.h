@@ -315,8 +315,9 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
  *                      warp may fill ahead of the compute warps. Default 8.
  *   QTTS_OPT_TC_MIN_ROWS 1..65: a GEMV stage whose activation rows (sessions
  *                      x rows per session) number at least this and at most
- *                      64 runs on the tensor cores (bf16 weights, K a
- *                      multiple of 128); 65 turns the tensor path off.
+ *                      64 runs on the tensor cores (BF16 weights, or INT8
+ *                      widened to bf16 in shared memory; K a multiple of
+ *                      128); 65 turns the tensor path off.
  *                      Default 8.
  *   QTTS_OPT_KSPLIT_MIN_ROWS 1..65: from this many activation rows up, a
  *                      tensor-path GEMV splits K across groups of CTAs
