@@ -70,7 +70,7 @@ extern "C" {
 #define QTTS_DEV_BAD_PAGE 2     /* a block-table entry outside the KV pool */
 #define QTTS_DEV_BAD_SAMPLING 3 /* temperature < 0 or not finite, rep_penalty <= 0 or not finite */
 #define QTTS_DEV_BAD_CODE 4     /* a teacher-forced code outside its codebook */
-#define QTTS_DEV_TIMEOUT 5      /* a grid-wide barrier wait ran out its limit */
+#define QTTS_DEV_TIMEOUT 5      /* a device-side wait (activation words, weight ring, tensor-path barriers) ran out its limit */
 
 #define QTTS_DTYPE_BF16 0
 
