@@ -172,8 +172,9 @@ int qtts_kv_pool_free_count(const qtts_model* m);
 /* Write (read) n_tok tokens of K and V of Talker layer `layer`: token i goes
  * to page pages[i / page_size], slot i % page_size. k, v: [n_tok][n_kv][d]
  * bf16, host or device (read: host). pages: host array of ceil(n_tok /
- * page_size) ids. Synchronous. Places a synthetic prompt prefix (prefill is
- * not part of the frame) and lets tests inspect the cache. */
+ * page_size) ids. Synchronous. Places a given prompt prefix (one computed
+ * from prompt embeddings is qtts_talker_prefill's) and lets tests inspect the
+ * cache. */
 int qtts_kv_write(qtts_model* m, int layer, int n_tok, const int32_t* pages_host, const uint16_t* k,
                   const uint16_t* v);
 int qtts_kv_read(qtts_model* m, int layer, int n_tok, const int32_t* pages_host, uint16_t* k_host,
