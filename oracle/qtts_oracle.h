@@ -25,6 +25,16 @@
  * double); K/V are rounded to bf16 when stored (the cache format). The INT8
  * quantiser and the sampler run in IEEE binary32, the precision the GPU path
  * takes the same integer decisions in; build with -ffp-contract=off.
+ *
+ * Pins: every function below is checked, without a GPU, against values fixed
+ * by the pages or by the mathematics rather than by itself: Philox
+ * known-answer vectors, exact points and accuracy of the log, RMSNorm / RoPE /
+ * SiLU closed forms, linear and attention against library routines and
+ * brute force, the quantiser on crafted ties, sampler special cases and
+ * Gumbel-max frequencies, whole-frame and prefill closed forms on special
+ * weights, batching invariance and causality (tests/test_oracle_*.py).
+ * Parity against a trained Qwen3-TTS is unpinned: no trained weights exist
+ * here, and the random-init weights exercise only the arithmetic.
  */
 #ifndef QTTS_ORACLE_H
 #define QTTS_ORACLE_H
