@@ -3,7 +3,9 @@ written here in numpy (float64) from the method's description rather than
 from the oracle's code: tiny model, general random weights, two sessions
 with different prefixes and histories, three teacher-forced greedy frames.
 Raw logits of all 16 codebooks, the greedy codes, the appended K/V and the
-advanced state must agree. The shapes of the steps (a Talker decode step
+advanced state must agree, with BF16 weights and with INT8 weights
+("Qwen3-TTS Native v0.3.0", What changed: per-output-channel symmetric,
+quantised from BF16). The shapes of the steps (a Talker decode step
 over a paged cache, the final norm and codebook-0 head, the 2048 -> 1024
 style projection into the Code Predictor, 15 Code-Predictor steps each with
 its own head over a cache emptied every frame) follow "Qwen3-TTS PR 5"
@@ -34,11 +36,31 @@ def to_bf16_rne(x):
     return np.where(x == 0.0, 0.0, np.round(x / q) * q)
 
 
+def int8_rows(wbits):
+    """Per-row symmetric INT8 in binary32: scale = max|w| / 127, q = w / scale
+    rounded half to even and clamped to +-127, zero rows scale 0; returned as
+    the float64 matrix scale x q the INT8 GEMM multiplies by."""
+    w = synth.bf16_to_f32(wbits)
+    m = np.abs(w).max(axis=1)
+    scale = (m / np.float32(127.0)).astype(np.float32)
+    safe = np.where(scale == 0, np.float32(1.0), scale)
+    q = np.clip(np.rint((w / safe[:, None]).astype(np.float32)), -127, 127)
+    q[scale == 0] = 0
+    return scale.astype(np.float64)[:, None] * q.astype(np.float64)
+
+
+def is_decode_linear(name):
+    return name.endswith(("q_proj", "k_proj", "v_proj", "o_proj", "gate_proj", "up_proj", "down_proj")) or \
+        name in ("talker.codec_head", "cp.proj") or name.startswith("cp.heads.")
+
+
 class Model:
-    def __init__(self, w, d):
-        self.w, self.d = w, d
+    def __init__(self, w, d, int8=False):
+        self.w, self.d, self.int8 = w, d, int8
 
     def W(self, name):
+        if self.int8 and is_decode_linear(name):
+            return int8_rows(self.w[name])
         return f64(self.w[name])
 
     def rms(self, x, gname):
@@ -90,9 +112,9 @@ def greedy0(l0, seen, d, rep):
     return int(np.argmax(l))
 
 
-def numpy_frames(w, sess, B):
+def numpy_frames(w, sess, B, int8=False):
     d = D
-    M = Model(w, d)
+    M = Model(w, d, int8)
     kv_len = [int(sess.kv_len0[b]) for b in range(B)]
     caches = []
     for b in range(B):
@@ -155,12 +177,13 @@ def weights():
     return synth.make_weights(D, 1234)
 
 
-def test_frames_match_numpy_restatement(orc_lib, weights):
+@pytest.mark.parametrize("int8", [False, True])
+def test_frames_match_numpy_restatement(orc_lib, weights, int8):
     B = 2
     sess = synth.Sessions(D, B, [20, 27], [0, 5], FRAMES + 1, 2077, temperature=0.0, top_k=1, rep_penalty=1.05)
-    ref, ref_caches, ref_len = numpy_frames(weights, sess, B)
+    ref, ref_caches, ref_len = numpy_frames(weights, sess, B, int8)
 
-    O = orc.Oracle(D, weights)
+    O = orc.Oracle(D, weights, use_int8=int8)
     rows = sess.session_array().copy()
     kv = [orc.kv_cache_from_prefix(sess.prefix_kv(b), CAP) for b in range(B)]
     rng, seen = sess.rng_state().copy(), sess.seen_bitmap().copy()
