@@ -83,7 +83,13 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ int read_err(const int* e) { return *(const volatile int*)e; }
 __device__ __forceinline__ void set_err(int* e, int code) { atomicCAS(e, 0, code); }
 
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: a frame takes milliseconds
+// Time limit of every wait for another CTA's data or for weights (default
+// 2 s: a frame takes milliseconds; qtts_set_option can shorten it), copied
+// from Globals at kernel start. Waits for a CTA's own copies and MMAs before
+// it leaves use kDrainNs instead, whatever this limit is.
+__shared__ uint64_t s_wait_ns;
+#define kWaitTimeoutNs s_wait_ns
+constexpr uint64_t kDrainNs = 2000000000ull;
 
 // ---- tagged words (see StageDesc): one 64-bit access carries value and tag ----
 
@@ -340,6 +346,16 @@ __device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, 
   return ok != 0;
 }
 constexpr uint32_t kSuspendNs = 20000;  // recheck the error word and the time limit this often
+
+// Wait for a copy or MMA this CTA issued itself to complete before leaving
+// (its bytes must not land after the CTA is gone): up to kDrainNs, whatever
+// the error word says.
+__device__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test_sleep(bar, parity, kSuspendNs))
+    if (global_timer_ns() - t0 > kDrainNs) return;
+}
 
 // Wait for phase `parity` of `bar` to complete, at most kWaitTimeoutNs; an
 // error word set elsewhere ends the wait too.
@@ -1374,6 +1390,8 @@ __device__ __forceinline__ void widen_i8_slot(unsigned char* slot, int nraw, int
 struct TcState {
   uint64_t xfree[2];  // MMAs reading X buffer b have completed
   uint64_t done;      // every MMA of the current segment has completed
+  uint64_t drain;     // leaving after an error: every MMA issued so far has completed
+  uint32_t issued;    // the issuing thread has issued MMAs in this launch
   uint32_t tmem;      // TMEM base (kTmemCols columns)
   uint32_t xuse;      // X-buffer fills so far (buffer = xuse & 1)
   uint32_t nseg;      // tensor segments finished so far (phase of `done`)
@@ -1510,6 +1528,7 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
           }
           const int e = min(s_end, slot_end);
           if (lane == 0) {
+            ts->issued = 1u;
             uint64_t da = tc_smem_desc(smem_addr(xb) + (uint32_t)((s - c0 * (kTcK / 16)) * 2 * lbo), lbo, 128);
             uint64_t db = tc_smem_desc(wa + (uint32_t)((s - j * sh.kps) * sh.kstep_bytes), sh.rows * 16, 128);
             const uint64_t da_step = (uint64_t)((2 * lbo) >> 4), db_step = (uint64_t)(sh.kstep_bytes >> 4);
@@ -1857,7 +1876,7 @@ __device__ void producer(const StageDesc* prog, int s0, int s1, const Globals& g
     if (!mbar_test(&ring->full[qq % nsl], (qq / nsl) & 1u)) {
       const uint64_t t0 = global_timer_ns();
       while (!mbar_test_sleep(&ring->full[qq % nsl], (qq / nsl) & 1u, kSuspendNs))
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+        if (global_timer_ns() - t0 > kDrainNs) break;
     }
   }
 }
@@ -1983,7 +2002,9 @@ __device__ bool attn_fetch_fold(AttnTile& T, const uint16_t* ksrc, const uint16_
     bulk_load(T.k, ksrc, bytes, &T.bar, policy);
     bulk_load(T.v, vsrc, bytes, &T.bar, policy);
   }
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(&T.bar, parity, err));  // one verdict per warp
+  const bool got = mbar_wait(&T.bar, parity, err);
+  if (!got) mbar_drain(&T.bar, parity);  // never leave with the copy still landing
+  const bool ok = __all_sync(0xffffffffu, got);  // one verdict per warp
   parity ^= 1u;
   if (ok) {
     if (cur_row >= 0) {
@@ -2506,6 +2527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     g = g_param;
     fa = fa_param;
+    s_wait_ns = g_param.wait_ns;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -2534,15 +2556,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tcs.xfree[0], 1);
       mbar_init(&tcs.xfree[1], 1);
       mbar_init(&tcs.done, 1);
+      mbar_init(&tcs.drain, 1);
       mbar_init_fence();
       tcs.xuse = 0u;
       tcs.nseg = 0u;
+      tcs.issued = 0u;
     }
   }
   tc_fence_before();
   cbar();
   tc_fence_after();
   uint32_t q = 0;
+  bool failed = false;
   for (int s = s0; s < s1; ++s) {
     const StageDesc& d = sdesc[s & 1];
     const StageDesc* next = s + 1 < s1 ? &prog[s + 1] : nullptr;
@@ -2567,8 +2592,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     trace_mark(g, 7);
     // no grid barrier: the next stage waits on the tags of the words it reads
-    if (cbar_or(!ok)) break;
+    if (cbar_or(!ok)) {
+      failed = true;
+      break;
+    }
   }
+  // A stage left after an error may have MMAs in flight: the issuing thread
+  // waits until every MMA it issued has completed before TMEM is released.
+  if (failed && tcs.issued && threadIdx.x == kTcIssuer * 32) {
+    tc_commit(&tcs.drain);
+    mbar_drain(&tcs.drain, 0u);
+  }
+  if (failed) cbar();
   // every TMEM read is done (each tensor stage ends at a barrier after its loads)
   if ((threadIdx.x >> 5) == 0) {
     tc_fence_after();

@@ -76,7 +76,16 @@ extern "C" int qtts_kv_write_noalloc(qtts_model* m, int layer, int n_tok, const 
   for (int i = 0; i < np; ++i)
     if (pages_host[i] < 0 || pages_host[i] >= L.pool_pages)
       return model_fail(m, QTTS_E_POOL, "qtts_kv_write_noalloc: page id outside the pool");
+  int prev_dev = -1;
+  if (cudaGetDevice(&prev_dev) != cudaSuccess) prev_dev = -1;
   if (cudaSetDevice(L.device) != cudaSuccess) return model_fail(m, QTTS_E_CUDA, "cudaSetDevice failed");
+  // the caller's current device is put back on every path out
+  struct Restore {
+    int dev, model_dev;
+    ~Restore() {
+      if (dev >= 0 && dev != model_dev) cudaSetDevice(dev);
+    }
+  } restore{prev_dev, L.device};
   void* stage = nullptr;
   void* pages = nullptr;
   const int rc = stage_addresses(L.device, &stage, &pages);

@@ -697,6 +697,7 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
   g.Vc = c.cp_vocab; g.eos_id = c.eos_id; g.n_codes = c.n_codes; g.seen_words = seen_words(c);
   g.max_context = c.max_context; g.eps = c.rms_eps; g.G = sms; g.pool_pages = c.kv_pool_pages;
   g.ring_slots = 8;
+  g.wait_ns = kDefaultWaitNs;
   g.tc_min_rows = 8;
   g.ksplit_min_rows = 8;
 
@@ -1109,7 +1110,8 @@ int qtts_talker_prefill(qtts_model* m, int B, qtts_session* sess, const int32_t*
 
 int qtts_frame_steps(qtts_model* m, int n_frames, int B, qtts_session* sess, const int32_t* bt, int bt_stride,
                      const uint16_t* in_embeds, const uint16_t* text_embeds, qtts_rng* rng, uint32_t* seen,
-                     const int32_t* forced, int32_t* codes_out, uint8_t* eos_out, void* stream) {
+                     const int32_t* forced, int32_t* codes_out, uint8_t* eos_out, float* logits_out,
+                     void* stream) {
   if (!m) return fail(m, QTTS_E_INVALID, "null model");
   if (!m->loaded) return fail(m, QTTS_E_STATE, "load weights first");
   if (n_frames < 1) return fail(m, QTTS_E_INVALID, "n_frames must be >= 1");
@@ -1131,8 +1133,9 @@ int qtts_frame_steps(qtts_model* m, int n_frames, int B, qtts_session* sess, con
   for (int f = 0; f < n_frames; ++f) {
     int32_t* codes = codes_out + (size_t)f * B * kCodebooks;
     const int32_t* frc = forced ? forced + (size_t)f * B * kCodebooks : nullptr;
-    int rc = frame_part(m, PART_ALL, B, sess, bt, bt_stride, in, rng, seen, frc, codes, eos_out + (size_t)f * B,
-                        nullptr, stream);
+    float* lg = logits_out ? logits_out + (size_t)f * B * kCodebooks * m->cfg.vocab0 : nullptr;
+    int rc = frame_part(m, PART_ALL, B, sess, bt, bt_stride, in, rng, seen, frc, codes, eos_out + (size_t)f * B, lg,
+                        stream);
     if (rc) return rc;
     if (f + 1 == n_frames) break;
     // the next frame's input: text + the codes the model consumed (forced ones under teacher forcing)
@@ -1271,6 +1274,11 @@ int qtts_set_option(qtts_model* m, int option, int value) {
   if (option == QTTS_OPT_KSPLIT_MIN_ROWS) {
     if (value < 1 || value > 65) return fail(m, QTTS_E_INVALID, "K-split row threshold must be 1..65");
     m->g.ksplit_min_rows = value;
+    return QTTS_OK;
+  }
+  if (option == QTTS_OPT_WAIT_LIMIT_US) {
+    if (value < 1 || value > 2000000) return fail(m, QTTS_E_INVALID, "wait limit must be 1..2000000 us");
+    m->g.wait_ns = (unsigned long long)value * 1000ull;
     return QTTS_OK;
   }
   if (option == QTTS_OPT_TRACE) {

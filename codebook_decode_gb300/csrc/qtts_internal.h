@@ -30,6 +30,7 @@ constexpr int kTcOverread = 4 * 1024;
 constexpr int kSmemBytes = kWorkBytes + kTailBytes + 128 * 1024 + kTcOverread;
 constexpr int kMaxVocab = 4096;
 constexpr int kMaxGrid = 256;            // persistent CTAs (SMs) the kernel supports
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // device-side wait limit: 2 s (a frame takes ms)
 
 enum StageType { ST_BEGIN = 0, ST_GEMV = 1, ST_ATTN_T = 2, ST_ATTN_CP = 3, ST_SAMPLE = 4 };
 enum XSrc { X_NORM = 0, X_PLAIN = 1 };
@@ -168,6 +169,7 @@ struct Globals {
   long long kpart_words;
   unsigned long long* trace;  // optional [trace_ctas][n_stages][8] %globaltimer stamps, then ring events
   int trace_ctas;         // 2: the first and the last CTA; G: every CTA
+  unsigned long long wait_ns;  // time limit of each wait for other CTAs' data or for weights
 };
 
 struct FrameArgs {

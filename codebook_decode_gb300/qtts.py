@@ -30,6 +30,7 @@ QTTS_OPT_TRACE = 3
 QTTS_OPT_RING_SLOTS = 4
 QTTS_OPT_TC_MIN_ROWS = 5
 QTTS_OPT_KSPLIT_MIN_ROWS = 6
+QTTS_OPT_WAIT_LIMIT_US = 7
 
 
 class QttsError(RuntimeError):
@@ -86,7 +87,7 @@ SIGNATURES = [
     ("qtts_frame_step_host", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
     ("qtts_frame_talker", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
     ("qtts_frame_cp", C.c_int, [_P, C.c_int, _P, _P, C.c_int] + [_P] * 8),
-    ("qtts_frame_steps", C.c_int, [_P, C.c_int, C.c_int, _P, _P, C.c_int] + [_P] * 8),
+    ("qtts_frame_steps", C.c_int, [_P, C.c_int, C.c_int, _P, _P, C.c_int] + [_P] * 9),
     ("qtts_talker_prefill", C.c_int, [_P, C.c_int, _P, _P, C.c_int, _P, C.c_int, _P]),
     ("qtts_frame_status", C.c_int, [_P, C.POINTER(C.c_int)]),
     ("qtts_feedback_embed", C.c_int, [_P, C.c_int, _P, _P, _P, _P]),
@@ -234,10 +235,10 @@ def qtts_frame_cp(m, B, sessions, block_tables, bt_stride, in_embeds, rng, seen,
 
 
 def qtts_frame_steps(m, n_frames, B, sessions, block_tables, bt_stride, in_embeds, text_embeds, rng, seen,
-                     forced_codes, codes_out, eos_out, stream=None):
+                     forced_codes, codes_out, eos_out, logits_out=None, stream=None):
     return _check(m, load_library().qtts_frame_steps(
         m, n_frames, B, ptr(sessions), ptr(block_tables), bt_stride, ptr(in_embeds), ptr(text_embeds), ptr(rng),
-        ptr(seen), ptr(forced_codes), ptr(codes_out), ptr(eos_out), _stream(stream)))
+        ptr(seen), ptr(forced_codes), ptr(codes_out), ptr(eos_out), ptr(logits_out), _stream(stream)))
 
 
 def qtts_talker_prefill(m, B, sessions, block_tables, bt_stride, embeds, n_tok, stream=None):

@@ -191,11 +191,16 @@ int qtts_kv_read(qtts_model* m, int layer, int n_tok, const int32_t* pages_host,
  * library holds until the process exits. Larger writes are rejected with
  * QTTS_E_INVALID: split them. Same arguments and cache result as
  * qtts_kv_write, plus `stream`: the copies and the scatter are queued on it and
- * the call returns without waiting; pinned host inputs must stay untouched
- * until the stream has run the copies. The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture. All calls share the one array, so calls whose work
- * overlaps on the GPU (different streams, no ordering between them) race. */
+ * the call returns without waiting. k and v may be pageable host, pinned host
+ * or device memory (pages_host is host memory): pageable host inputs are
+ * copied before the call returns, while pinned host and device inputs are read
+ * later, in stream order, so they must stay valid and unmodified until the
+ * stream has run the copies. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, in the device's primary context, which
+ * is the context every later call uses); make that first call before any
+ * stream capture. The caller's current device is left as it was. All calls
+ * share the one array, so calls whose work overlaps on the GPU (different
+ * streams, no ordering between them) race. */
 int qtts_kv_write_noalloc(qtts_model* m, int layer, int n_tok, const int32_t* pages_host, const uint16_t* k,
                           const uint16_t* v, void* stream);
 
@@ -258,14 +263,16 @@ int qtts_frame_cp(qtts_model* m, int B, qtts_session* sessions, const int32_t* b
  * on the device (qtts_feedback_embed). Device arrays: text_embeds
  * [n_frames][B][hidden] bf16 (row n_frames-1 unused), forced_codes
  * [n_frames][B][16] or NULL, codes_out [n_frames][B][16], eos_out
- * [n_frames][B]; sessions, block_tables, rng and seen as in qtts_frame_step
- * (advanced once per frame; block tables must already cover kv_len +
- * n_frames positions). Sessions that emit EOS keep running: the caller
- * compacts finished sessions between calls. Asynchronous on `stream`. */
+ * [n_frames][B], logits_out [n_frames][B][16][vocab0] or NULL (each frame's
+ * raw logits, laid out as in qtts_frame_step); sessions, block_tables, rng
+ * and seen as in qtts_frame_step (advanced once per frame; block tables must
+ * already cover kv_len + n_frames positions). Sessions that emit EOS keep
+ * running: the caller compacts finished sessions between calls. Asynchronous
+ * on `stream`. */
 int qtts_frame_steps(qtts_model* m, int n_frames, int B, qtts_session* sessions, const int32_t* block_tables,
                      int bt_stride, const uint16_t* in_embeds, const uint16_t* text_embeds, qtts_rng* rng,
                      uint32_t* seen, const int32_t* forced_codes, int32_t* codes_out, uint8_t* eos_out,
-                     void* stream);
+                     float* logits_out, void* stream);
 
 /* Talker prefill: a prompt of n_tok tokens per session through the Talker
  * layers: the causal prompt pass that runs before the first frame
@@ -325,12 +332,21 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
  *                      whose partial sums one CTA per group adds (fewer
  *                      activation words per CTA, one more exchange); below
  *                      it only GEMVs of at least 8 x 6144 activation values
- *                      (rows x K) split. Default 8. */
+ *                      (rows x K) split. Default 8.
+ *   QTTS_OPT_WAIT_LIMIT_US 1..2000000: the limit, in microseconds, of every
+ *                      device-side wait for another CTA's data or for
+ *                      weights; a wait that runs it out sets
+ *                      QTTS_DEV_TIMEOUT and the frame is abandoned (its
+ *                      work partly done: re-run it from the caller's copy of
+ *                      the state). Default 2000000 (2 s). A short limit is a
+ *                      test of the time-out path, which otherwise a working
+ *                      GPU never takes. */
 #define QTTS_OPT_STEPWISE 1
 #define QTTS_OPT_TRACE 3
 #define QTTS_OPT_RING_SLOTS 4
 #define QTTS_OPT_TC_MIN_ROWS 5
 #define QTTS_OPT_KSPLIT_MIN_ROWS 6
+#define QTTS_OPT_WAIT_LIMIT_US 7
 int qtts_set_option(qtts_model* m, int option, int value);
 
 /* Stage timestamps of the last frame run with QTTS_OPT_TRACE on: 8 values

@@ -1,5 +1,7 @@
 """Shared driver for the GPU parity tests: run the CUDA frame (through the C
 ABI) and the CPU oracle side by side on the same seeded inputs."""
+import ctypes as C
+
 import numpy as np
 import torch
 
@@ -47,32 +49,91 @@ class ParityRun:
         self.confident_agree = 0
         self.argmax_agree = 0
         self.argmax_total = 0
+        self.codes_checked = 0
+        self.kv_synced = None
 
-    def run(self, frames=None, check_oracle=True):
+    def run(self, frames=None, check_oracle=True, free=False, split=False):
+        """Run frames on the GPU and the oracle side by side. Teacher forced by
+        default; free=True lets the GPU sample its own codes and forces the
+        oracle with them, so both commit the same codes. split=True runs each
+        frame as qtts_frame_talker + qtts_frame_cp. Every frame's own sampled
+        codes and EOS flags are checked bit for bit against the oracle's
+        sampler fed the GPU's logits, with the state from before the frame."""
         d = self.d
+        e = self.eng
         for f in range(frames or self.frames):
             emb = self.sess.in_embeds(f)
-            forced = self.sess.forced_codes(f)
-            self.eng.step(to_dev_u16(emb, self.eng.dev), to_dev_i32(forced, self.eng.dev))
-            rc, derr = self.eng.status()
-            assert rc == 0 and derr == 0, (rc, derr, qtts.load_library().qtts_last_error(self.eng.m))
-            got = self.eng.logits.cpu().numpy().astype(np.float64)
+            forced = None if free else self.sess.forced_codes(f)
+            emb_d = to_dev_u16(emb, e.dev)
+            frc_d = None if forced is None else to_dev_i32(forced, e.dev)
+            if split:
+                args = (e.m, e.B, e.sess, e.bt, e.bt_stride, emb_d, e.rng, e.seen, frc_d, e.codes, e.eos, e.logits)
+                qtts.qtts_frame_talker(*args)
+                qtts.qtts_frame_cp(*args)
+            else:
+                e.step(emb_d, frc_d)
+            rc, derr = e.status()
+            assert rc == 0 and derr == 0, (rc, derr, qtts.load_library().qtts_last_error(e.m))
+            got32 = e.logits.cpu().numpy()
+            got = got32.astype(np.float64)
+            codes = e.codes.cpu().numpy()
+            eos = e.eos.cpu().numpy()
             if not check_oracle:
                 continue
-            _, _, ref = self.O.frame_step(self.rows, self.kv, self.cap, emb, self.rng, self.seen, forced=forced)
-            for b in range(self.sess.B):
-                for j in range(16):
-                    V = d.vocab0 if j == 0 else d.cp_vocab
-                    g, r = got[b, j, :V], ref[b, j, :V]
-                    self.rel.append((f, b, j, rel_diff(g, r)))
-                    top2 = np.sort(r)[-2:]
-                    self.argmax_total += 1
-                    same = int(np.argmax(g)) == int(np.argmax(r))
-                    self.argmax_agree += same
-                    if top2[1] - top2[0] > 1.0:
-                        self.confident += 1
-                        self.confident_agree += same
+            rng0, seen0 = self.rng.copy(), self.seen.copy()
+            self.check_sampled(got32, codes, eos, rng0, seen0)
+            _, _, ref = self.O.frame_step(self.rows, self.kv, self.cap, emb, self.rng, self.seen,
+                                          forced=codes if free else forced)
+            self.compare_logits(f, got, ref)
         return self
+
+    def check_sampled(self, logits32, codes, eos, rng0, seen0):
+        """The codes the frame sampled equal the oracle sampler's on the same
+        logits rows, bit for bit (rng and seen set as they were before the
+        frame); eos_out is 1 exactly where codebook 0 sampled eos_id."""
+        d = self.d
+        L = orc.lib()
+        for b in range(self.sess.B):
+            S = orc.session_struct(self.rows[b])
+            for j in range(16):
+                V = d.vocab0 if j == 0 else d.cp_vocab
+                row = np.ascontiguousarray(logits32[b, j, :V], dtype=np.float32)
+                sb = np.ascontiguousarray(seen0[b])
+                want = L.orc_sample(row.ctypes.data, V, j, C.byref(S), int(rng0[b, 0]), int(rng0[b, 1]),
+                                    int(rng0[b, 2]), sb.ctypes.data if j == 0 else None, d.eos_id, d.n_codes)
+                assert int(codes[b, j]) == want, (b, j, int(codes[b, j]), want)
+                self.codes_checked += 1
+            assert int(eos[b]) == int(codes[b, 0] == d.eos_id), (b, int(eos[b]), int(codes[b, 0]))
+
+    def compare_logits(self, f, got, ref):
+        d = self.d
+        for b in range(self.sess.B):
+            for j in range(16):
+                V = d.vocab0 if j == 0 else d.cp_vocab
+                g, r = got[b, j, :V], ref[b, j, :V]
+                self.rel.append((f, b, j, rel_diff(g, r)))
+                top2 = np.sort(r)[-2:]
+                self.argmax_total += 1
+                same = int(np.argmax(g)) == int(np.argmax(r))
+                self.argmax_agree += same
+                if top2[1] - top2[0] > 1.0:
+                    self.confident += 1
+                    self.confident_agree += same
+
+    def sync_oracle_from_gpu(self):
+        """Start the oracle from the GPU's state: sessions, rng, seen set and
+        every layer's cache up to kv_len, read back through the C ABI (the
+        window checks of long runs)."""
+        self.rows = self.eng.sess.cpu().numpy().copy()
+        self.rng = self.eng.rng.cpu().numpy().view(np.uint32).copy()
+        self.seen = self.eng.seen.cpu().numpy().view(np.uint32).copy()
+        for b in range(self.sess.B):
+            n = int(self.rows[b, 0])
+            for l in range(self.d.n_layers):
+                k, v = self.eng.read_kv(b, l, n)
+                self.kv[b][l, 0, :n] = k
+                self.kv[b][l, 1, :n] = v
+        self.kv_synced = self.rows[:, 0].copy()
 
     def max_rel(self, codebooks=range(16)):
         return max(r for (_, _, j, r) in self.rel if j in codebooks)
@@ -92,7 +153,7 @@ class ParityRun:
         d = self.d
         for b in range(self.sess.B):
             n = int(self.rows[b, 0])
-            n0 = int(self.sess.kv_len0[b])
+            n0 = int(self.sess.kv_len0[b] if self.kv_synced is None else self.kv_synced[b])
             for l in (layers if layers is not None else range(d.n_layers)):
                 k, v = self.eng.read_kv(b, l, n)
                 for i, got in enumerate((k, v)):

@@ -1,7 +1,10 @@
 """GPU parity at the full Qwen3-TTS 1.7B-shaped sizes (28-layer 2048-wide
 Talker, 5-layer 1024-wide Code Predictor), on the workloads' own batch sizes,
 length mixes and shuffled paged caches, in the persistent launch the benchmark
-times. The oracle checks teacher-forced windows of each workload."""
+times. The oracle checks teacher-forced windows of each workload (the first
+frames, and the late windows of the B=32 workloads started from the GPU's own
+cache and state), every frame's sampled codes bit for bit against the oracle's
+sampler on the GPU's logits, and a free-running window."""
 import numpy as np
 import pytest
 
@@ -115,3 +118,59 @@ def test_full_b32_long_run_state(full_w):
         torch.cuda.synchronize()
     finally:
         free(run)
+
+
+def test_full_b1_free_running(full_w, oracle_bf16):
+    """Single stream, free running: the GPU commits its own sampled codes
+    (Code-Predictor inputs, seen set), the oracle is forced with them; logits,
+    codes (bit exact on the GPU's logits) and state agree."""
+    s = synth.make_sessions(configs.WORKLOADS["full_b1"], frames=3)
+    run = ParityRun(FULL, full_w, s, 3, oracle=oracle_bf16).run(free=True)
+    try:
+        check(run, TOL_BF16)
+        assert run.codes_checked == 3 * 16
+    finally:
+        free(run)
+
+
+def late_window(full_w, oracle, wl, n_before, n_window, int8):
+    """Advance n_before free-running frames on the GPU, start the oracle from
+    the GPU's cache and state, then check n_window teacher-forced frames."""
+    import torch
+    from codebook_decode_gb300.engine import to_dev_u16
+    s = synth.make_sessions(configs.WORKLOADS[wl], frames=n_before + n_window)
+    run = ParityRun(FULL, full_w, s, n_before + n_window, int8=int8, oracle=oracle)
+    try:
+        for f in range(n_before):
+            run.eng.step(to_dev_u16(s.in_embeds(f), run.eng.dev), None, want_logits=False)
+        assert run.eng.status() == (0, 0)
+        assert np.array_equal(run.eng.sess.cpu().numpy()[:, 0], s.kv_len0 + n_before)
+        run.sync_oracle_from_gpu()
+
+        class Shifted:  # the window's frames draw the inputs of frames n_before, n_before + 1, ...
+            B = s.B
+            kv_len0 = s.kv_len0
+
+            def in_embeds(self, f):
+                return s.in_embeds(n_before + f)
+
+            def forced_codes(self, f):
+                return s.forced_codes(n_before + f)
+        run.sess = Shifted()
+        run.run(n_window)
+        check(run, TOL_INT8 if int8 else TOL_BF16)
+        torch.cuda.synchronize()
+    finally:
+        free(run)
+
+
+def test_full_b32_late_window(full_w, oracle_bf16):
+    """Config 3 (B=32, ragged and staggered contexts): frames 248..255 against
+    the oracle started from the GPU's cache and state after 248 frames."""
+    late_window(full_w, oracle_bf16, "full_b32", 248, 8, False)
+
+
+def test_full_int8_b32_late_window(full_w, oracle_int8):
+    """Config 4 (INT8 weights, B=32): frames 120..127 against the oracle
+    started from the GPU's cache and state after 120 frames."""
+    late_window(full_w, oracle_int8, "int8_b32", 120, 8, True)

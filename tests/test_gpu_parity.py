@@ -2,8 +2,10 @@
 same seeded inputs. Gates: teacher-forced logits within 1.0% (BF16) / 1.5%
 (INT8) of the logit scale per row, 100% raw-argmax agreement where the
 oracle's top-2 margin exceeds 1, state (kv_len, frame counter, seen set)
-exact, cache contents to bf16 rounding, INT8 weights and sampled codes bit
-exact."""
+exact, cache contents to bf16 rounding, INT8 weights bit exact, and the codes
+each frame samples (and its EOS flags) bit exact against the oracle's sampler
+fed that frame's own logits (ParityRun.check_sampled), teacher forced and
+free running."""
 import ctypes as C
 
 import numpy as np
@@ -90,6 +92,62 @@ def test_gemv_path_choice(tiny_w, B, tc_min, ks_min, int8):
         assert run.max_rel() < (TOL_INT8 if int8 else TOL_BF16), run.max_rel()
         assert run.confident_agree == run.confident
         run.check_state()
+    finally:
+        free(run)
+
+
+def test_tiny_free_running_vs_oracle(tiny_w):
+    """B=5 free running with sampling on: the GPU's own sampled codes feed its
+    Code Predictor and seen set; the oracle, forced with those codes, agrees
+    on logits and state, and each code is the oracle sampler's on the GPU's
+    logits."""
+    s = tiny_sessions(5, [0, 1, 15, 16, 45], [0, 3, 1, 7, 2], T=0.9, k=50, r=1.05)
+    run = ParityRun(TINY, tiny_w, s, 4, shuffle=True).run(free=True)
+    try:
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+        assert run.codes_checked == 4 * 5 * 16
+        run.check_state()
+        run.check_kv()
+    finally:
+        free(run)
+
+
+def test_tiny_eos_allowed(tiny_w):
+    """EOS unmasked in codebook 0, temperature 1.3 without top-k (EOS is
+    sampled on some frames): codes and eos_out against the oracle sampler."""
+    s = tiny_sessions(6, [3, 9, 17, 30, 2, 11], T=1.3, k=0, r=1.2, eos=1)
+    run = ParityRun(TINY, tiny_w, s, 6, shuffle=True).run(free=True)
+    try:
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+        run.check_state()
+    finally:
+        free(run)
+
+
+@pytest.mark.parametrize("B,tc_min,ks_min", [(1, 65, 65), (3, 1, 1)])
+def test_wait_limit_runs_out_then_recovers(tiny_w, B, tc_min, ks_min):
+    """A 1 us limit on every device-side wait: the frame's waits for other
+    CTAs' words run out, the frame ends with QTTS_DEV_TIMEOUT (returned as
+    QTTS_E_TIMEOUT) instead of hanging, each CTA first draining its own bulk
+    copies and MMAs; with the default limit back the same model runs frames
+    that match the oracle. CUDA-core path (B=1) and tensor path with K split
+    (B=3)."""
+    s = tiny_sessions(B, [20, 7, 33][:B], T=0.9, k=50, r=1.05)
+    run = ParityRun(TINY, tiny_w, s, 2, tc_min_rows=tc_min, ksplit_min_rows=ks_min)
+    try:
+        e = run.eng
+        assert qtts.qtts_set_option(e.m, qtts.QTTS_OPT_WAIT_LIMIT_US, 1) == 0
+        e.step(to_dev_u16(s.in_embeds(0), e.dev), to_dev_i32(s.forced_codes(0), e.dev))
+        assert e.status() == (qtts.QTTS_E_TIMEOUT, qtts.QTTS_DEV_TIMEOUT)
+        assert qtts.qtts_set_option(e.m, qtts.QTTS_OPT_WAIT_LIMIT_US, 2000000) == 0
+        # the abandoned frame may have advanced part of the state: start again from the caller's copy
+        e.sess.copy_(torch.from_numpy(s.session_array()).to(e.dev))
+        e.rng.copy_(to_dev_i32(s.rng_state(), e.dev))
+        e.seen.copy_(to_dev_i32(s.seen_bitmap(), e.dev))
+        run.run(2)
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+        run.check_state()
+        run.check_kv()
     finally:
         free(run)
 

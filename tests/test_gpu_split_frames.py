@@ -1,14 +1,16 @@
 """GPU: the frame split into its Talker and Code-Predictor halves
 (qtts_frame_talker + qtts_frame_cp) and the multi-frame loop with on-device
-feedback (qtts_frame_steps) give exactly the results of the one-call frame
-(qtts_frame_step) and of frame + qtts_feedback_embed called frame by frame."""
+feedback (qtts_frame_steps) against the oracle (logits, sampled codes bit
+exact on the GPU's logits, state, cache), and bit for bit against the
+one-call frame (qtts_frame_step) and frame + qtts_feedback_embed called frame
+by frame."""
 import numpy as np
 import pytest
 import torch
 
 from codebook_decode_gb300 import configs, qtts, synth
 from codebook_decode_gb300.engine import to_dev_i32, to_dev_u16
-from gpu_helpers import ParityRun, free
+from gpu_helpers import TOL_BF16, ParityRun, free
 
 pytestmark = pytest.mark.gpu
 
@@ -85,7 +87,7 @@ def test_frame_steps_equals_frame_and_feedback_loop(tiny_w, forced):
             eos = torch.zeros(n, e.B, dtype=torch.uint8, device=e.dev)
             if fused:
                 qtts.qtts_frame_steps(e.m, n, e.B, e.sess, e.bt, e.bt_stride, emb0, text, e.rng, e.seen, frc, codes,
-                                      eos)
+                                      eos, None)
             else:
                 cur = emb0
                 nxt = torch.empty_like(emb0)
@@ -101,3 +103,55 @@ def test_frame_steps_equals_frame_and_feedback_loop(tiny_w, forced):
             free(run)
     for x, y in zip(outs[0], outs[1]):
         assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("free_run", [False, True])
+def test_split_halves_match_oracle(tiny_w, free_run):
+    """qtts_frame_talker then qtts_frame_cp, frame by frame, against the
+    oracle: logits, every sampled code, state and cache."""
+    s = sessions(4, 3)
+    run = ParityRun(TINY, tiny_w, s, 3).run(free=free_run, split=True)
+    try:
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+        assert run.codes_checked == 3 * 4 * 16
+        run.check_state()
+        run.check_kv()
+    finally:
+        free(run)
+
+
+@pytest.mark.parametrize("forced", [False, True])
+def test_frame_steps_match_oracle(tiny_w, forced):
+    """qtts_frame_steps over n frames with the feedback built on the device,
+    against the oracle run frame by frame on inputs text + sum_j E_j[c_j] of
+    the codes each frame committed (the forced ones under teacher forcing,
+    else the GPU's own): every frame's logits, its sampled codes bit exact on
+    those logits, then state and cache."""
+    n = 4
+    s = sessions(3, n)
+    run = ParityRun(TINY, tiny_w, s, n)
+    e = run.eng
+    try:
+        text = np.stack([s.text_embeds(f) for f in range(n)])
+        frc = np.stack([s.forced_codes(f) for f in range(n)]) if forced else None
+        codes = torch.zeros(n, e.B, 16, dtype=torch.int32, device=e.dev)
+        eos = torch.zeros(n, e.B, dtype=torch.uint8, device=e.dev)
+        logits = torch.zeros(n, e.B, 16, TINY.vocab0, dtype=torch.float32, device=e.dev)
+        qtts.qtts_frame_steps(e.m, n, e.B, e.sess, e.bt, e.bt_stride, to_dev_u16(s.in_embeds(0), e.dev),
+                              to_dev_u16(text, e.dev), e.rng, e.seen,
+                              to_dev_i32(frc, e.dev) if forced else None, codes, eos, logits)
+        assert e.status() == (0, 0)
+        codes, eos, logits = codes.cpu().numpy(), eos.cpu().numpy(), logits.cpu().numpy()
+        emb = s.in_embeds(0)
+        for f in range(n):
+            committed = frc[f] if forced else codes[f]
+            rng0, seen0 = run.rng.copy(), run.seen.copy()
+            run.check_sampled(logits[f], codes[f], eos[f], rng0, seen0)
+            _, _, ref = run.O.frame_step(run.rows, run.kv, run.cap, emb, run.rng, run.seen, forced=committed)
+            run.compare_logits(f, logits[f].astype(np.float64), ref)
+            emb = synth.bf16_bits(run.O.feedback(committed, text[f]).astype(np.float32))
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+        run.check_state()
+        run.check_kv()
+    finally:
+        free(run)
