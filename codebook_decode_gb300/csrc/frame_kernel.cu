@@ -1416,9 +1416,9 @@ constexpr int kTcPairs = (kTcXBytes / 4 / 2 + kTcStagers * 32 - 1) / (kTcStagers
 // TMEM over all of K. Stager warps fill 32 KB activation tiles (several
 // 128-wide K chunks per pass, two buffers) while the issuer's MMAs read the
 // other buffer; a commit frees each weight slot and activation buffer when its
-// MMAs are done. The epilogue adds the hi and lo lanes; a CTA of a later
-// K-slice then hands its partial sums to slice 0, which adds them, applies
-// 1/rms and runs the stage's epilogue.
+// MMAs are done. The epilogue adds the hi and lo lanes; with a K split, the
+// CTAs of the slices exchange partial sums so that each adds up 1/S of the
+// share's rows, applies 1/rms and runs their epilogues.
 __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, const Globals& g, const FrameArgs& fa,
                               unsigned char* smem, Ring* ring, TcState* ts, uint32_t& q) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1585,69 +1585,69 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
       rsq[tid] = t;
     }
     cbar();
-    // K-split exchange area of this segment: per later slice, [16 n_groups][rows]
-    // partial sums then [rows] partial sums of squares
+    // K-split exchange area of this segment: per slice, [16 n_groups][rows]
+    // partial sums then [rows] partial sums of squares. Rows [o0, o1) of the
+    // share belong to this slice: it hands its partial sums of the other
+    // slices' rows to them, adds theirs of its own rows and runs the
+    // epilogues of its own rows (every slice takes 1/S of the share).
     const int npad = (sg.N + kTcRows - 1) / kTcRows * kTcRows;
     const size_t slice_words = (size_t)npad * rows + rows;
-    uint64_t* kp = nullptr;
+    const int n_base = sh.g0 * kTcRows;
+    const int o0 = nsr * sh.ks / sh.S, o1 = nsr * (sh.ks + 1) / sh.S;  // whole units: nsr / S is a multiple of 4
+    const int nown = (o1 - o0) * rows;
     if (sh.S > 1) {
       long long off = 0;
       for (int sp = 0; sp < si; ++sp)
         if (tc_split(d.seg[sp], rows, K, g)) off += tc_kpart_words(d.seg[sp].N, K, (int)gridDim.x, kTcMaxActRows);
-      kp = g.kpart + (size_t)((tag - fa.tag0) & 1u) * (size_t)g.kpart_words + (size_t)off;
-    }
-    const int n_base = sh.g0 * kTcRows;
-    if (sh.ks > 0) {
-      // a later K-slice: hand the partial sums to slice 0 and stop here
-      uint64_t* dst = kp + (size_t)(sh.ks - 1) * slice_words;
-      for (int idx = tid; idx < nres; idx += kCThreads) {
-        const int n = idx / rows, r = idx - n * rows;
+      uint64_t* kp = g.kpart + (size_t)((tag - fa.tag0) & 1u) * (size_t)g.kpart_words + (size_t)off;
+      uint64_t* dst = kp + (size_t)sh.ks * slice_words;
+      const int nother = nres - nown;
+      for (int idx = tid; idx < nother; idx += kCThreads) {
+        int n = idx / rows;
+        const int r = idx - n * rows;
+        if (n >= o0) n += o1 - o0;  // skip the own rows
         st_ll(dst + (size_t)(n_base + n) * rows + r, res[r * nsr + n], tag);
       }
       if (tid < rows) st_ll(dst + (size_t)npad * rows + tid, rsq[tid], tag);
-      cbar();  // res is read before the next share's fills
-      trace_mark(g, 3);
-      continue;
-    }
-    if (sh.S > 1) {
-      // slice 0: add the later slices' partial sums (in slice order) and sums of squares
-      const uint64_t* srcb = kp;
+      cbar();  // the own sums of squares are sent before the others' are added to them
+      // the other slices' partial sums of the own rows (in slice order) and their sums of squares
+      const int ks = sh.ks;
       ok &= ll_gather_add<4, kTcMaxSplit - 1>(
-          nres + rows, sh.S - 1, [&](int) { return tag; },
+          nown + rows, sh.S - 1, [&](int) { return tag; },
           [&](int i, int k) {
-            const uint64_t* b = srcb + (size_t)k * slice_words;
-            if (i >= nres) return b + (size_t)npad * rows + (i - nres);
-            const int n = i / rows, r = i - n * rows;
+            const uint64_t* b = kp + (size_t)(k < ks ? k : k + 1) * slice_words;
+            if (i >= nown) return b + (size_t)npad * rows + (i - nown);
+            const int n = o0 + i / rows, r = i - (i / rows) * rows;
             return b + (size_t)(n_base + n) * rows + r;
           },
           [&](int i) {
-            if (i >= nres) return rsq + (i - nres);
-            const int n = i / rows, r = i - n * rows;
+            if (i >= nown) return rsq + (i - nown);
+            const int n = o0 + i / rows, r = i - (i / rows) * rows;
             return res + r * nsr + n;
           },
           g.err);
     }
     if (sg.epi == E_RESID) {
-      // the residual operands of the share's rows, into the free low half
+      // the residual operands of the own rows, into the free low half
       ok &= ll_gather_add<2, 1>(
-          nres, 1, [&](int i) { return fa.tag0 + (uint32_t)sg.r_ws[(i % rows) % d.rps]; },
+          nown, 1, [&](int i) { return fa.tag0 + (uint32_t)sg.r_ws[(i % rows) % d.rps]; },
           [&](int i, int) {
-            const int n = i / rows, r = i - n * rows;
+            const int n = o0 + i / rows, r = i - (i / rows) * rows;
             const int n0 = min(n_base + n, sg.N - 1);  // padding rows read a real word and never use it
             return sg.resid + (size_t)out_row_of(sg, d.rps, r) * sg.out_stride + n0;
           },
           [&](int i) {
-            const int n = i / rows, r = i - n * rows;
+            const int n = o0 + i / rows, r = i - (i / rows) * rows;
             return res + nres + r * nsr + n;
           },
           g.err);
     }
     if (cbar_or(!ok)) return false;
-    // epilogue: one thread per (unit, activation row)
+    // epilogue of the own rows: one thread per (unit, activation row)
     const int U = sg.unit;
-    const int nunits = nsr / U;
+    const int u_own0 = o0 / U, nunits = (o1 - o0) / U;
     for (int idx = tid; idx < nunits * rows; idx += kCThreads) {
-      const int ul = idx / rows, r = idx - ul * rows;
+      const int ul = u_own0 + idx / rows, r = idx - (idx / rows) * rows;
       const int n0 = n_base + ul * U;
       if (n0 >= sg.N) continue;  // padding rows of the last group
       const float f = norm ? 1.0f / sqrtf(rsq[r] / (float)K + g.eps) : 1.0f;

@@ -82,11 +82,12 @@ __host__ __device__ inline bool tc_fits(int N, int K, int G, int S) {
 // K-split of a tensor-path segment (N rows, K) over a grid of G CTAs: the
 // grid's first S C CTAs (C = G / S) form S K-slices; CTA c of slice s takes
 // the 16-row groups [n_groups c / C, n_groups (c + 1) / C) over the 128-wide
-// K chunks [s K / S, (s + 1) K / S). A CTA of slice s > 0 hands its partial
-// sums to CTA c of slice 0, which adds them and runs the epilogue. Among the
+// K chunks [s K / S, (s + 1) K / S). The CTAs c of the S slices split the
+// share's rows S ways: each hands its partial sums of the others' rows to
+// them, adds theirs of its own rows and runs their epilogues. Among the
 // powers of two S <= kTcMaxSplit that divide K / kTcK and keep a share within
 // kTcMaxRows rows, S minimises the words a CTA reads per activation row: its K range
-// (K / S) plus the partial sums slice 0 gathers ((S - 1) x its rows); ties
+// (K / S) plus the partial sums exchanged ((S - 1) x its rows); ties
 // take the smaller S. 0: none fits. A second copy of the weight tiles is
 // packed for this partition (C CTAs per slice); a stage takes it from
 // ksplit_min_rows activation rows up, else the one-slice copy (S = 1).
@@ -105,12 +106,14 @@ __host__ __device__ inline int tc_ksplit(int N, int K, int G) {
   }
   return best;
 }
-// Words of the partial-sum exchange area one K-split segment needs: per slice
-// s > 0, [n_groups * 16][rows] partial sums then [rows] partial sums of squares.
+// Words of the partial-sum exchange area one K-split segment needs: per
+// slice, [n_groups * 16][rows] partial sums then [rows] partial sums of
+// squares (each slice runs the epilogues of 1/S of the rows of its share and
+// gathers the other slices' partial sums of those rows).
 __host__ __device__ inline long long tc_kpart_words(int N, int K, int G, int rows) {
   const int S = tc_ksplit(N, K, G);
   const long long npad = (long long)(N + kTcRows - 1) / kTcRows * kTcRows;
-  return S > 1 ? (long long)(S - 1) * (npad * rows + rows) : 0;
+  return S > 1 ? (long long)S * (npad * rows + rows) : 0;
 }
 
 struct alignas(16) StageDesc {
