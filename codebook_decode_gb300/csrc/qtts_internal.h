@@ -98,7 +98,7 @@ __host__ __device__ inline int tc_ksplit(int N, int K, int G) {
   for (int S = 1; S <= kTcMaxSplit; S *= 2) {
     if (!tc_fits(N, K, G, S)) continue;
     const int rows = (ngroups + G / S - 1) / (G / S) * kTcRows;
-    const int cost = K / S + (S - 1) * rows;
+    const int cost = K / S + (S - 1) * rows / S;
     if (!best || cost < best_cost) {
       best = S;
       best_cost = cost;
