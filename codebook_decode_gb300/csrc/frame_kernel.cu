@@ -1346,19 +1346,20 @@ __device__ void fill_epi_cache(const StageDesc& d, const Globals& g, const Frame
   }
 }
 
-// Widen the int8 weight tiles a bulk copy left in a ring slot's upper half
-// (nraw bytes) to bf16 over the whole slot, element for element. Exact: the
-// byte b of value v gives the float 2^23 + (v + 128) when put under the
+// The int8 weight tiles a bulk copy leaves in a ring slot's upper half (nraw
+// bytes) are widened to bf16 over the whole slot, element for element. Exact:
+// the byte b of value v gives the float 2^23 + (v + 128) when put under the
 // exponent of 2^23 (bits 0x4B000000 | (b ^ 0x80)); subtracting 2^23 + 128
 // leaves v, whose float has its low 16 bits zero, so its top half is the
-// bf16. One warp, in 1024-byte steps whose reads all precede their writes:
-// step c writes bytes [2048 c, 2048 c + 2048), which hold only the raw bytes
-// of steps <= c.
+// bf16. Raw step c (1024 bytes) is written to bytes [2048 c, 2048 c + 2048),
+// which hold raw bytes of steps 2c - 8 and 2c - 7.
 __device__ __forceinline__ uint32_t widen2(uint32_t x, int i) {  // bytes i, i + 1 of x (bias-flipped) as 2 bf16
   const float a = __int_as_float((int)__byte_perm(x, 0x4B000000u, 0x7540u + i)) - 8388736.0f;
   const float b = __int_as_float((int)__byte_perm(x, 0x4B000000u, 0x7541u + i)) - 8388736.0f;
   return (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u);
 }
+// The whole slot by one warp, in 1024-byte steps in order (each step's reads
+// precede its writes, and its output overlaps only raw bytes of steps <= c).
 __device__ __forceinline__ void widen_i8_slot(unsigned char* slot, int nraw, int lane) {
   const unsigned char* raw = slot + kSlotBytes / 2;
   for (int c0 = 0; c0 < nraw; c0 += 1024) {
@@ -1385,6 +1386,39 @@ __device__ __forceinline__ void widen_i8_slot(unsigned char* slot, int nraw, int
     __syncwarp();
   }
 }
+
+// Barrier of the tensor path's stager warps only (id 5; 1 is cbar, 2.. the
+// Code-Predictor attention groups).
+constexpr int kStagerBarrier = 5;
+// The same split over `nw` warps, one 1024-byte raw step per
+// warp of `nw` warps (warp index w; raw steps <= nw): every warp reads its raw
+// bytes, then, after a barrier of the nw warps, writes its widened ones (a
+// step's output overlaps earlier steps' raw bytes).
+__device__ __forceinline__ void widen_i8_slot_split(unsigned char* slot, int nraw, int w, int lane, int nw) {
+  const unsigned char* raw = slot + kSlotBytes / 2;
+  uint4 v[2];
+  const int c0 = w * 1024;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int o = c0 + h * 512 + lane * 16;
+    v[h] = o < nraw ? *reinterpret_cast<const uint4*>(raw + o) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  asm volatile("bar.sync %0, %1;" ::"n"(kStagerBarrier), "r"(nw * 32) : "memory");
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int o = c0 + h * 512 + lane * 16;
+    if (o < nraw) {
+      const uint32_t in[4] = {v[h].x ^ 0x80808080u, v[h].y ^ 0x80808080u, v[h].z ^ 0x80808080u,
+                              v[h].w ^ 0x80808080u};
+      uint32_t out[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = widen2(in[i >> 1], (i & 1) * 2);
+      *reinterpret_cast<uint4*>(slot + 2 * o) = make_uint4(out[0], out[1], out[2], out[3]);
+      *reinterpret_cast<uint4*>(slot + 2 * o + 16) = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+  }
+}
+static_assert(kSlotBytes / 2 <= 1024 * 10, "an int8 slot's raw steps must not outnumber the stager warps");
 
 // Tensor-path state kept across stages in shared memory.
 struct TcState {
@@ -1500,7 +1534,22 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
             *reinterpret_cast<uint32_t*>(ct + (lr >> 3) * 128 + (lr & 7) * 16) = l0 | ((uint32_t)l1 << 16);
           }
         }
-        fence_proxy_async_smem();  // the activation tiles are read by the tensor cores (async proxy)
+        if (sh.es == 1) {
+          // widen the int8 weight slots whose first K step is in this pass
+          // (the issuer then only waits and issues), one raw step per stager
+          // warp; at most ring_slots - 1 of them: those the producer can fill
+          // before this pass's MMAs free any slot (the issuer widens the rest)
+          const int s_lo = c0 * (kTcK / 16), s_hi = c1 * (kTcK / 16);
+          const int jj0 = (s_lo + sh.kps - 1) / sh.kps;
+          for (int jj = jj0; jj * sh.kps < s_hi && jj < jj0 + (int)nsl - 1; ++jj) {
+            const uint32_t qq = q + (uint32_t)jj;
+            const int sl = (int)(qq & (nsl - 1u));
+            ok &= ring_wait_full(ring, sl, qq >> nsl_shift, g.err);
+            widen_i8_slot_split(ring_slot(smem, sl), (min(nks, (jj + 1) * sh.kps) - jj * sh.kps) * sh.rows * 16, warp,
+                                lane, kTcStagers);
+          }
+        }
+        fence_proxy_async_smem();  // the activation tiles (and widened weights) are read by the tensor cores
       }
       cbar();
       if (pass == 0) trace_mark(g, 1);
@@ -1512,14 +1561,15 @@ __device__ __noinline__ bool stage_gemv_tc(const StageDesc& d, uint32_t tag, con
         for (int s = c0 * (kTcK / 16); s < s_end;) {
           const int j = s / sh.kps;
           const int slot_end = min(nks, (j + 1) * sh.kps);
-          if (j != slot_j) {  // next weight slot: the whole warp waits (and widens int8 tiles)
+          if (j != slot_j) {  // next weight slot: its first K step is in this pass
             slot_j = j;
             const uint32_t qq = q + (uint32_t)j;
             slot = (int)(qq & (nsl - 1u));
             ok &= ring_wait_full(ring, slot, qq >> nsl_shift, g.err);
             if (lane == 0) trace_ring(g, qq, 1);
             unsigned char* sp = ring_slot(smem, slot);
-            if (sh.es == 1) {
+            // int8: the stagers widened the pass's first ring_slots - 1 new slots; the warp widens the rest
+            if (sh.es == 1 && j >= (c0 * (kTcK / 16) + sh.kps - 1) / sh.kps + (int)nsl - 1) {
               widen_i8_slot(sp, (slot_end - j * sh.kps) * sh.rows * 16, lane);
               fence_proxy_async_smem();  // read by the tensor cores next
               __syncwarp();
