@@ -1747,49 +1747,92 @@ __device__ __noinline__ bool stage_gemv(const StageDesc& d, uint32_t tag, const 
 
   for (int r0 = 0; r0 < rows; r0 += RT) {
     const int nr = min(RT, rows - r0);
-    cbar();
+    if (r0) cbar();  // the previous tile is done with the activation rows (the stage loop's barrier covers the first)
     // (1) the tile's input words and this CTA's residual operands: every
     //     load is issued before the first wait, one round trip for the lot
     bool ok = true;
     const int nres = has_resid ? sh0.nu * nr : 0;  // <= kResidFloats <= 2 * kCThreads
     uint64_t rw[2] = {0, 0};
     const uint64_t* rp[2] = {nullptr, nullptr};
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int idx = tid + u * kCThreads;
-      if (idx < nres) {
-        const int ul = idx / nr, r = idx - ul * nr;
-        rp[u] = s0.resid + (size_t)out_row_of(s0, d.rps, r0 + r) * s0.out_stride + (sh0.u0 + ul) * s0.unit;
-        rw[u] = ld_ll(rp[u]);
-      }
-    }
-    if (use_ring && warp == kCWarps - 1) fill_epi_cache(d, g, fa, r0, nr, K, &tail->ec);
+    // a single-row tile folds the RMSNorm into the staging: gains loaded with
+    // the words, x g stored, sums of squares kept per thread
+    const bool fold = norm && nr == 1;
+    float sq1 = 0.f;
     {
       constexpr int NB = 4;
-      const int npair = nr * K / 2;
+      const int hk = K / 2, npair = nr * hk;
+      // this thread's pairs follow one another kCThreads apart: pair p of tile row r
+      // (no divisions on the way to the first loads)
+      int r = tid / hk, p = tid - r * hk;
+      const bool two = d.rps == 2;  // rows per session: 1 or 2
+      const uint32_t tag_p0 = fa.tag0 + (uint32_t)d.x_ws[0], tag_p1 = fa.tag0 + (uint32_t)d.x_ws[1];
       for (int base = tid; base < npair; base += kCThreads * NB) {
         uint64_t w[NB][2];
         const uint64_t* ps[NB];
-        uint32_t tg[NB];
+        uint32_t tg[NB], gw[NB];
 #pragma unroll
         for (int u = 0; u < NB; ++u) {
           const int i = base + u * kCThreads;
           ps[u] = nullptr;
           tg[u] = 0;
+          gw[u] = 0;
           w[u][0] = w[u][1] = 0;
           if (i < npair) {
-            const int e = 2 * i, r = e / K, k = e - r * K;
-            ps[u] = d.x + (size_t)rm.in_row(r0 + r) * d.x_stride + k;
-            tg[u] = fa.tag0 + (uint32_t)d.x_ws[(r0 + r) % d.rps];
+            const int rr = r0 + r;  // stage row: session rr / rps, position rr % rps
+            const int in_row = two ? (rr >> 1) * d.in_rps + d.in_off + (rr & 1) : rr * d.in_rps + d.in_off;
+            ps[u] = d.x + (size_t)in_row * d.x_stride + 2 * p;
+            tg[u] = (two && (rr & 1)) ? tag_p1 : tag_p0;
             ld_ll2(ps[u], w[u][0], w[u][1]);
+            if (fold) gw[u] = __ldg(reinterpret_cast<const unsigned*>(d.gain + 2 * p));
           }
+          p += kCThreads;
+          while (p >= hk) {
+            p -= hk;
+            ++r;
+          }
+        }
+        if (base == tid) {
+          // this CTA's residual operands, issued after the first input loads
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int idx = tid + u * kCThreads;
+            if (idx < nres) {
+              const int ul = idx / nr, rr = idx - ul * nr;
+              rp[u] = s0.resid + (size_t)out_row_of(s0, d.rps, r0 + rr) * s0.out_stride + (sh0.u0 + ul) * s0.unit;
+              rw[u] = ld_ll(rp[u]);
+            }
+          }
+          // the epilogue operands (one warp), once its input loads are out
+          if (use_ring && warp == kCWarps - 1) fill_epi_cache(d, g, fa, r0, nr, K, &tail->ec);
         }
         ok &= ll_settle<NB>(ps, tg, w, g.err);
 #pragma unroll
         for (int u = 0; u < NB; ++u) {
           const int i = base + u * kCThreads;
-          if (i < npair) *reinterpret_cast<float2*>(xs + 2 * i) = make_float2(ll_val(w[u][0]), ll_val(w[u][1]));
+          if (i < npair) {
+            float x0 = ll_val(w[u][0]), x1 = ll_val(w[u][1]);
+            if (fold) {
+              sq1 = fmaf(x0, x0, sq1);
+              sq1 = fmaf(x1, x1, sq1);
+              x0 *= bf_lo(gw[u]);
+              x1 *= bf_hi(gw[u]);
+            }
+            *reinterpret_cast<float2*>(xs + 2 * i) = make_float2(x0, x1);
+          }
         }
+      }
+      if (npair <= tid) {
+        // no input pair for this thread: the residual operands still go out
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int idx = tid + u * kCThreads;
+          if (idx < nres) {
+            const int ul = idx / nr, rr = idx - ul * nr;
+            rp[u] = s0.resid + (size_t)out_row_of(s0, d.rps, r0 + rr) * s0.out_stride + (sh0.u0 + ul) * s0.unit;
+            rw[u] = ld_ll(rp[u]);
+          }
+        }
+        if (use_ring && warp == kCWarps - 1) fill_epi_cache(d, g, fa, r0, nr, K, &tail->ec);
       }
     }
 #pragma unroll
@@ -1801,9 +1844,13 @@ __device__ __noinline__ bool stage_gemv(const StageDesc& d, uint32_t tag, const 
         tail->resid[ul * RT + r] = ll_val(rw[u]);
       }
     }
+    if (fold) {
+      const float t = warp_sum(sq1);
+      if (lane == 0) tail->sqw[0][warp] = t;
+    }
     if (cbar_or(!ok)) return false;
     // (2) RMSNorm: x <- g x in place, per-warp sums of squares of each row
-    if (norm) {
+    if (norm && !fold) {
       for (int r = 0; r < nr; ++r) {
         float sq = 0.f;
         for (int k = tid * 2; k < K; k += kCThreads * 2) {
