@@ -49,6 +49,18 @@ def measured_peak_gbs():
     return 6800.0, "fallback"
 
 
+def measured_peak_tflops():
+    """Dense bf16 tensor peak for a kernel timed inside a longer run (the
+    sustained figure), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        if "bf16_tflops_sustained" in j:
+            return float(j["bf16_tflops_sustained"]), "measured sustained"
+    return 1700.0, "fallback"
+
+
 def ncu_traffic(wl):
     """DRAM bytes per frame-kernel launch from the committed ncu capture, or
     None when the kernel source changed since it was taken or the capture was
@@ -201,6 +213,35 @@ def talker_pass_weight_bytes(d, int8):
     return d.n_layers * per_layer * (1 if int8 else 2)
 
 
+PREFILL_MAX_ROWS = 1024  # rows (sessions x prompt tokens) of one prefill chunk
+
+
+def prefill_flops(d, kv_len0, n_tok):
+    """Algorithmic FLOPs of a prompt pass: 2 per weight and token for every
+    layer's QKV and, except the last layer (whose outputs after its K/V are
+    not observable), O, gate/up and down; plus 4 x q dims per attended
+    position (scores and the weighted sum of V) in those layers."""
+    qkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim * d.hidden
+    rest = d.hidden * d.n_q_heads * d.head_dim + 3 * d.ffn * d.hidden
+    toks = len(kv_len0) * n_tok
+    attended = sum(int(n0) * n_tok + n_tok * (n_tok + 1) // 2 for n0 in kv_len0)
+    return (2 * toks * (d.n_layers * qkv + (d.n_layers - 1) * rest)
+            + 4 * d.n_q_heads * d.head_dim * attended * (d.n_layers - 1))
+
+
+def prefill_kv_bytes(d, kv_len0, n_tok, per_chunk):
+    """Algorithmic cache bytes of a prompt pass in chunks of per_chunk tokens
+    per session: each chunk reads every position before it once (a query
+    block of the chunk reuses a K/V tile for all its tokens) and writes its
+    own positions once."""
+    t_tok = d.n_layers * 2 * d.n_kv_heads * d.head_dim * 2  # K and V of one token, all layers
+    n = 0
+    for n0 in kv_len0:
+        for t0 in range(0, n_tok, per_chunk):
+            n += (int(n0) + t0) * t_tok + min(per_chunk, n_tok - t0) * t_tok
+    return n
+
+
 def run_prefill(wl, n_tok, reps, local, weights):
     """Talker prefill throughput: every session of the workload takes an
     n_tok-token prompt after its prefix (kv_len rewound between repetitions,
@@ -232,16 +273,17 @@ def run_prefill(wl, n_tok, reps, local, weights):
     rc, derr = qtts.qtts_frame_status(eng.m, raise_on_error=False)
     assert rc == 0 and derr == 0, (rc, derr)
     ms = statistics.median(times)
-    t_tok = d.n_layers * 2 * d.n_kv_heads * d.head_dim * 2  # K and V of one token, all layers
-    kv = sum(sum(int(n0) + t + 1 for t in range(n_tok)) for n0 in sess.kv_len0) * t_tok + wl.batch * n_tok * t_tok
-    # a pass takes 32 // B prompt tokens of every session and streams the
-    # Talker weights once for all of them
-    per_pass = max(1, 32 // wl.batch)
-    passes = (n_tok + per_pass - 1) // per_pass
-    nbytes = passes * talker_pass_weight_bytes(d, wl.int8) + kv
+    # a chunk takes PREFILL_MAX_ROWS // B prompt tokens of every session,
+    # streams the Talker weights (BF16, also for INT8 models) once for all of
+    # them, reads each session's cached K/V once and writes the chunk's
+    per_chunk = max(1, PREFILL_MAX_ROWS // wl.batch)
+    chunks = (n_tok + per_chunk - 1) // per_chunk
+    nbytes = chunks * talker_pass_weight_bytes(d, False) + prefill_kv_bytes(d, sess.kv_len0, n_tok, per_chunk)
+    flops = prefill_flops(d, sess.kv_len0, n_tok)
     eng.release_pages()
     eng.close()
-    return dict(tokens_per_s=wl.batch * n_tok / (ms / 1e3), ms=ms, bytes=nbytes, achieved_gbs=nbytes / (ms / 1e3) / 1e9)
+    return dict(tokens_per_s=wl.batch * n_tok / (ms / 1e3), ms=ms, bytes=nbytes, achieved_gbs=nbytes / (ms / 1e3) / 1e9,
+                flops=flops, achieved_tflops=flops / (ms / 1e3) / 1e12, chunks=chunks)
 
 
 def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, trace_file=None, tc_min_rows=None,
@@ -482,14 +524,23 @@ def main():
                 sweep[name] = {"frames_per_s": o.batch * min(args.steps, 50) / (rr["total_ms"] / 1e3),
                                "frame_ms": rr["frame_ms"], "achieved_gbs": rr["achieved_gbs"],
                                "frac": rr["achieved_gbs"] / peak, "bytes_per_frame": rr["bytes_per_frame"]}
-            for name, n_tok in (("full_b1", 64), ("full_b8", 64)):
+            tc_peak, tc_kind = measured_peak_tflops()
+            for name, n_tok in (("full_b1", 64), ("full_b1", 512), ("full_b1", 1024), ("full_b8", 64),
+                                ("full_b8", 128)):
                 o = configs.WORKLOADS[name]
                 rp = run_prefill(o, n_tok, 3, local, w)
+                t_hbm = rp["bytes"] / (peak * 1e9)
+                t_tc = rp["flops"] / (tc_peak * 1e12)
+                bound = "tensor" if t_tc > t_hbm else "hbm"
                 sweep[f"prefill_{name}_{n_tok}tok"] = {
                     "tokens_per_s": rp["tokens_per_s"], "ms": rp["ms"], "achieved_gbs": rp["achieved_gbs"],
-                    "frac": rp["achieved_gbs"] / peak, "bytes": rp["bytes"],
-                    "what": f"Talker prefill of {n_tok} prompt tokens for each of {o.batch} session(s), "
-                            f"{max(1, 32 // o.batch)} token(s) per session per pass"}
+                    "hbm_frac": rp["achieved_gbs"] / peak, "bytes": rp["bytes"],
+                    "achieved_tflops": rp["achieved_tflops"], "tensor_frac": rp["achieved_tflops"] / tc_peak,
+                    "flops": rp["flops"], "bound": bound,
+                    "frac": rp["achieved_tflops"] / tc_peak if bound == "tensor" else rp["achieved_gbs"] / peak,
+                    "peak": {"hbm_gbs": peak, "bf16_tflops": tc_peak, "kind": tc_kind},
+                    "what": f"Talker prefill of {n_tok} prompt tokens for each of {o.batch} session(s) after its "
+                            f"prefix, {rp['chunks']} chunk(s) of up to {PREFILL_MAX_ROWS} rows"}
             line["sweep"] = sweep
         print(json.dumps(line))
     barrier(ws)

@@ -13,7 +13,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqtts.so")
-SOURCES = ["frame_kernel.cu", "util_kernels.cu", "qtts_api.cu", "kv_noalloc.cu"]
+SOURCES = ["frame_kernel.cu", "util_kernels.cu", "qtts_api.cu", "kv_noalloc.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 

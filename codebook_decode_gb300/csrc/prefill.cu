@@ -1,0 +1,772 @@
+// prefill.cu -- the Talker prompt pass over whole chunks of prompt tokens.
+//
+// "Qwen3-TTS PR 5: 1.7B CustomVoice, VoiceDesign and Base": section Graph
+// (talker_prefill, the causal prompt pass through the Talker layers before
+// the first frame) and section "What changed" (one packed prefill over a
+// bucket of 32..1024 prompt tokens). "Qwen3-TTS Native v0.3.0", "What
+// changed": prefill stays BF16 when decode runs on INT8 weights, so this pass
+// always reads the BF16 weights.
+//
+// A chunk is M = B x P rows, row p B + b being prompt token p of session b at
+// position kv_len_b + p. Per Talker layer, kernels on one stream:
+//   norm     RMSNorm of the residual rows, packed as bf16 hi + lo tiles
+//   gemm     QKV on the tcgen05 tensor cores, fp32 partial sums per K-slice
+//   qkv      RoPE; K and V rounded to bf16 into the sessions' pages; q kept
+//   attn     causal attention over each session's pages, packed hi + lo
+//   gemm     O, then norm adds it to the residual and normalises
+//   gemm     gate/up, then swiglu packs silu(gate) x up
+//   gemm     down, then norm adds it and applies the next layer's input norm
+// The last layer stops after its K/V: nothing after them is observable.
+//
+// Activations enter the GEMMs as two bf16 operands, hi = bf16(a) and
+// lo = bf16(a - hi), accumulated into one fp32 sum, so a product carries ~16
+// mantissa bits of the fp32 activation against bf16 weights (the decode
+// path's tensor stages do the same).
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "qtts_internal.h"
+
+namespace qtts {
+
+namespace {
+
+// ---- small device helpers (this translation unit's own) ----
+
+__device__ __forceinline__ float bf2f(uint32_t h16) { return __uint_as_float(h16 << 16); }
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+__device__ __forceinline__ uint64_t gtimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ int err_now(const int* e) { return *(const volatile int*)e; }
+__device__ __forceinline__ void err_set(int* e, int code) { atomicCAS(e, 0, code); }
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_expect(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `b`, at most `ns` nanoseconds.
+__device__ bool bar_wait(uint64_t* b, uint32_t parity, uint64_t ns) {
+  if (bar_try(b, parity)) return true;
+  const uint64_t t0 = gtimer_ns();
+  while (!bar_try(b, parity))
+    if (gtimer_ns() - t0 > ns) return false;
+  return true;
+}
+// global -> shared bulk copy, completing `bytes` of the barrier's transaction
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   saddr(dst)),
+               "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(saddr(b))
+               : "memory");
+}
+
+// tcgen05: K-major canonical operand layout without swizzle (core matrices of
+// 8 rows x 16 bytes; lbo = bytes between core matrices along K, sbo along the
+// rows), descriptor version 1
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, both K-major
+constexpr uint32_t umma_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(b))
+               : "memory");
+}
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// ---- GEMM operand tiles ----
+// Activations: [m tile of 128 rows][64-wide K chunk][hi | lo] images; weights
+// (packed at load): [256-row tile][K chunk] images. Inside an image of R rows:
+// element (r, k) at ((k / 8) * R / 8 + r / 8) * 64 + (r % 8) * 8 + k % 8.
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 3;
+constexpr int kAImg = kBM * kBK;                    // elements of one hi or lo image (16 KB)
+constexpr int kWImg = kBN * kBK;                    // 32 KB
+constexpr int kStageBytes = (2 * kAImg + kWImg) * 2;  // 64 KB
+constexpr int kGemmSmem = kStages * kStageBytes;
+constexpr int kGemmThreads = 192;                   // warp 0 copies, warp 1 issues MMAs, warps 2-5 drain TMEM
+constexpr uint32_t kTmemCols = 256;
+
+__host__ __device__ __forceinline__ int core_off(int r, int k, int R) {
+  return (k >> 3) * (R * 8) + (r >> 3) * 64 + (r & 7) * 8 + (k & 7);
+}
+__host__ __device__ __forceinline__ size_t a_off(int r, int k, int KC, int hl) {
+  return ((size_t)((r >> 7) * KC + (k >> 6)) * 2 + hl) * kAImg + core_off(r & 127, k & 63, kBM);
+}
+__host__ __device__ __forceinline__ size_t w_off(int n, int k, int KC) {
+  return (size_t)((n >> 8) * KC + (k >> 6)) * kWImg + core_off(n & 255, k & 63, kBN);
+}
+
+// hi and lo of eight consecutive activation values (k % 8 == 0) of row r
+__device__ __forceinline__ void put8(uint16_t* A, int r, int k, int KC, const float (&v)[8]) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint16_t h0 = f2bf(v[2 * j]), h1 = f2bf(v[2 * j + 1]);
+    const uint16_t l0 = f2bf(v[2 * j] - bf2f(h0)), l1 = f2bf(v[2 * j + 1] - bf2f(h1));
+    h[j] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    l[j] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+  }
+  *reinterpret_cast<uint4*>(A + a_off(r, k, KC, 0)) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(A + a_off(r, k, KC, 1)) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// ---------------------------------------------------------------------------
+// weights -> tiles (load time): rows past N and columns past K are zero
+// ---------------------------------------------------------------------------
+__global__ void pack_weights_kernel(const uint16_t* __restrict__ w, int N, int K, int Npad, int KC,
+                                    uint16_t* __restrict__ dst) {
+  const long long groups = (long long)Npad * KC * (kBK / 8);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < groups;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int n = (int)(i / (KC * (kBK / 8)));
+    const int k = (int)(i % (KC * (kBK / 8))) * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (n < N && k < K) v = *reinterpret_cast<const uint4*>(w + (size_t)n * K + k);
+    *reinterpret_cast<uint4*>(dst + w_off(n, k, KC)) = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// GEMM: out[s][m][n] = sum over K-slice s of A[m][k] W[n][k]
+// One CTA per (256-row weight tile, 128-row activation tile, K-slice); a
+// 3-stage ring of 64-wide K chunks filled by bulk copies; one thread issues
+// M = 128, N = 256, K = 16 MMAs (hi, then lo, for each K step) into a
+// 128 x 256 fp32 TMEM accumulator; four warps read it back.
+// ---------------------------------------------------------------------------
+struct GemmArgs {
+  const uint16_t* A;
+  const uint16_t* W;
+  float* out;  // [S][Mpad][Npad]
+  int KC, S, Mpad, Npad;
+  int* err;
+  unsigned long long wait_ns;
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int failed;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = blockIdx.x, mt = blockIdx.y, s = blockIdx.z;
+  const int kc0 = (int)((long long)s * a.KC / a.S), kc1 = (int)((long long)(s + 1) * a.KC / a.S);
+  const int nk = kc1 - kc0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      bar_init(&full[i], 1);
+      bar_init(&empty[i], 1);
+    }
+    bar_init(&done, 1);
+    failed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
+                 "n"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = tmem_base;
+  int issued_uses = 0;  // producer: stage uses whose copies were issued
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < nk; ++i) {
+      const int st = i % kStages, u = i / kStages;
+      if (u > 0 && !bar_wait(&empty[st], (u - 1) & 1, a.wait_ns)) {
+        err_set(a.err, QTTS_DEV_TIMEOUT);
+        failed = 1;
+        break;
+      }
+      if (*(volatile int*)&failed) break;
+      unsigned char* base = smem + st * kStageBytes;
+      const int kc = kc0 + i;
+      bar_expect(&full[st], kStageBytes);
+      bulk_g2s(base, a.A + (size_t)(mt * a.KC + kc) * 2 * kAImg, 2 * kAImg * 2, &full[st]);
+      bulk_g2s(base + 2 * kAImg * 2, a.W + (size_t)(nt * a.KC + kc) * kWImg, kWImg * 2, &full[st]);
+      issued_uses = i + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = umma_idesc(kBM, kBN);
+    for (int i = 0; i < nk; ++i) {
+      const int st = i % kStages, u = i / kStages;
+      if (!bar_wait(&full[st], u & 1, a.wait_ns)) {
+        err_set(a.err, QTTS_DEV_TIMEOUT);
+        failed = 1;
+        break;
+      }
+      tc_after();
+      const uint32_t base = saddr(smem + st * kStageBytes);
+#pragma unroll
+      for (int ks = 0; ks < kBK / 16; ++ks) {
+        const uint64_t dhi = umma_desc(base + ks * 2 * (kBM * 16), kBM * 16, 128);
+        const uint64_t dlo = umma_desc(base + kAImg * 2 + ks * 2 * (kBM * 16), kBM * 16, 128);
+        const uint64_t dw = umma_desc(base + 2 * kAImg * 2 + ks * 2 * (kBN * 16), kBN * 16, 128);
+        umma(tmem, dhi, dw, idesc, (i > 0 || ks > 0) ? 1u : 0u);
+        umma(tmem, dlo, dw, idesc, 1u);
+      }
+      umma_commit(&empty[st]);
+    }
+    umma_commit(&done);  // also after a failure: completes once the issued MMAs have
+  } else if (warp >= 2) {
+    const int q = warp & 3;  // this warp's TMEM lane quarter
+    int okl = 0;
+    if (lane == 0) okl = bar_wait(&done, 0, a.wait_ns) ? 1 : 0;
+    const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // one verdict per warp: the loads below are warp-wide
+    __syncwarp();
+    if (!ok) {
+      err_set(a.err, QTTS_DEV_TIMEOUT);
+      failed = 1;
+    } else {
+      tc_after();
+      const int row = mt * kBM + q * 32 + lane;
+      float* o = a.out + ((size_t)s * a.Mpad + row) * a.Npad + (size_t)nt * kBN;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 16; ++c) {
+        uint32_t r[16];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 16)));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(o + c * 16 + 4 * j) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+      }
+    }
+  }
+  tc_before();
+  __syncthreads();
+  if (failed) {
+    // nothing may land in shared memory or TMEM after the CTA is gone:
+    // wait (bounded) for the last issued copies and the MMAs
+    if (warp == 0 && lane == 0)
+      for (int i = (issued_uses > kStages ? issued_uses - kStages : 0); i < issued_uses; ++i)
+        bar_wait(&full[i % kStages], (i / kStages) & 1, 2000000000ull);
+    if (warp == 1 && lane == 0) bar_wait(&done, 0, 2000000000ull);
+    __syncthreads();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tc_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// row kernels (one CTA per chunk row)
+// ---------------------------------------------------------------------------
+
+constexpr int kRowThreads = 256;
+
+// deterministic CTA sum: warps' shuffle trees, then the warps in order
+__device__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+  return t;
+}
+
+struct NormArgs {
+  const uint16_t* emb;   // first layer: the prompt embeddings [M][H] bf16, else nullptr
+  float* x;              // residual rows [M][H] fp32
+  const float* part;     // added to x first (nullptr: none): [S][Mpad][Npad] partial sums
+  int S, Mpad, Npad;
+  const uint16_t* gain;  // RMSNorm gain [H] (nullptr: no norm, no packing)
+  float eps;
+  int H, KC;             // K chunks of the packed rows (H rounded up to 64)
+  uint16_t* A;
+};
+
+// x = emb (or x + sum of partials); then A = pack(x * rms(x)^-1 * gain)
+__global__ void __launch_bounds__(kRowThreads) norm_kernel(NormArgs a) {
+  __shared__ float red[kRowThreads / 32];
+  const int r = blockIdx.x;
+  float* x = a.x + (size_t)r * a.H;
+  float ss = 0.f;
+  for (int k = threadIdx.x * 8; k < a.H; k += kRowThreads * 8) {
+    float v[8];
+    if (a.emb) {
+      const uint4 e = *reinterpret_cast<const uint4*>(a.emb + (size_t)r * a.H + k);
+      const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = bf2f(ew[j] & 0xFFFFu);
+        v[2 * j + 1] = bf2f(ew[j] >> 16);
+      }
+    } else {
+      const float4 x0 = *reinterpret_cast<const float4*>(x + k), x1 = *reinterpret_cast<const float4*>(x + k + 4);
+      v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+    }
+    if (a.part)
+      for (int s = 0; s < a.S; ++s) {
+        const float* p = a.part + ((size_t)s * a.Mpad + r) * a.Npad + k;
+        const float4 p0 = *reinterpret_cast<const float4*>(p), p1 = *reinterpret_cast<const float4*>(p + 4);
+        v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+        v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+      }
+    *reinterpret_cast<float4*>(x + k) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(x + k + 4) = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+  }
+  if (!a.gain) return;
+  const float tot = block_sum(ss, red);
+  const float rs = 1.0f / sqrtf(tot / (float)a.H + a.eps);
+  for (int k = threadIdx.x * 8; k < a.KC * kBK; k += kRowThreads * 8) {
+    float v[8];
+    if (k < a.H) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = x[k + j] * rs * bf2f(a.gain[k + j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.f;  // K padding
+    }
+    put8(a.A, r, k, a.KC, v);
+  }
+}
+
+struct QkvArgs {
+  const float* part;  // [S][Mpad][Npad]
+  int S, Mpad, Npad;
+  int B;
+  const qtts_session* sess;
+  const int32_t* bt;
+  int bt_stride;
+  int layer, nq, nkv, d;
+  uint16_t* kv_pool;
+  int pool_pages;
+  const float* rope_cos;  // [max_context][d/2]
+  const float* rope_sin;
+  float* q;               // [M][nq d]
+  int* err;
+};
+
+// QKV epilogue of row r: fused rows come as rotate-half pairs (dims i and
+// i + d/2 of one q or k head), then v in pairs of adjacent dims
+__global__ void __launch_bounds__(kRowThreads) qkv_kernel(QkvArgs a) {
+  if (err_now(a.err)) return;  // the chunk's sessions failed validation
+  const int r = blockIdx.x, b = r % a.B, p = r / a.B;
+  const int pos = a.sess[b].kv_len + p;
+  const int half = a.d / 2;
+  const int nqk = (a.nq + a.nkv) * a.d;
+  const int npair = (a.nq + 2 * a.nkv) * a.d / 2;
+  int page = a.bt[(size_t)b * a.bt_stride + pos / kPage];
+  if (page < 0 || page >= a.pool_pages) {  // checked before the chunk; stay in bounds regardless
+    err_set(a.err, QTTS_DEV_BAD_PAGE);
+    return;
+  }
+  for (int u = threadIdx.x; u < npair; u += kRowThreads) {
+    const int n0 = 2 * u;
+    float y0 = 0.f, y1 = 0.f;
+    for (int s = 0; s < a.S; ++s) {
+      const float2 t = *reinterpret_cast<const float2*>(a.part + ((size_t)s * a.Mpad + r) * a.Npad + n0);
+      y0 += t.x;
+      y1 += t.y;
+    }
+    if (n0 < nqk) {
+      const bool is_q = n0 < a.nq * a.d;
+      const int rel = is_q ? n0 : n0 - a.nq * a.d;
+      const int head = rel / a.d, i = (rel % a.d) / 2;
+      const float c = a.rope_cos[(size_t)pos * half + i], sn = a.rope_sin[(size_t)pos * half + i];
+      const float o0 = y0 * c - y1 * sn;
+      const float o1 = y1 * c + y0 * sn;
+      if (is_q) {
+        float* qr = a.q + (size_t)r * a.nq * a.d + head * a.d;
+        qr[i] = o0;
+        qr[i + half] = o1;
+      } else {
+        uint16_t* kp = a.kv_pool +
+                       ((((size_t)a.layer * a.pool_pages + page) * 2 + 0) * a.nkv + head) * kPage * a.d +
+                       (size_t)(pos % kPage) * a.d;
+        kp[i] = f2bf(o0);
+        kp[i + half] = f2bf(o1);
+      }
+    } else {
+      const int rel = n0 - nqk;
+      const int head = rel / a.d, e = rel % a.d;
+      uint16_t* vp = a.kv_pool + ((((size_t)a.layer * a.pool_pages + page) * 2 + 1) * a.nkv + head) * kPage * a.d +
+                     (size_t)(pos % kPage) * a.d;
+      *reinterpret_cast<uint32_t*>(vp + e) = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
+    }
+  }
+}
+
+struct SwigluArgs {
+  const float* part;  // [S][Mpad][Npad], columns 2j = gate j, 2j + 1 = up j
+  int S, Mpad, Npad;
+  int F, KC;
+  uint16_t* A;
+};
+
+__global__ void __launch_bounds__(kRowThreads) swiglu_kernel(SwigluArgs a) {
+  const int r = blockIdx.x;
+  for (int k = threadIdx.x * 8; k < a.KC * kBK; k += kRowThreads * 8) {
+    float v[8];
+    if (k < a.F) {
+      float y[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) y[j] = 0.f;
+      for (int s = 0; s < a.S; ++s) {
+        const float* p = a.part + ((size_t)s * a.Mpad + r) * a.Npad + 2 * k;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 t = *reinterpret_cast<const float4*>(p + 4 * j);
+          y[4 * j] += t.x; y[4 * j + 1] += t.y; y[4 * j + 2] += t.z; y[4 * j + 3] += t.w;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float g = y[2 * j];
+        v[j] = g / (1.0f + expf(-g)) * y[2 * j + 1];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.f;  // K padding
+    }
+    put8(a.A, r, k, a.KC, v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// causal attention: one CTA per (session, kv head, 32 query vectors: the
+// group's q heads of 32 / grp consecutive prompt tokens); 8 warps of 4
+// vectors; keys in tiles of 32 positions read from the pages (the chunk's
+// own K/V included), one position per lane, online softmax per vector
+// ---------------------------------------------------------------------------
+constexpr int kAttnVecs = 32;
+constexpr int kAttnThreads = 256;
+
+struct AttnArgs {
+  const float* q;  // [M][nq d], RoPE applied
+  int B, P;
+  const qtts_session* sess;
+  const int32_t* bt;
+  int bt_stride;
+  int layer, nq, nkv;
+  const uint16_t* kv_pool;
+  int pool_pages;
+  uint16_t* A;     // packed output rows, K = nq d
+  int KC;
+  int* err;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
+  constexpr int E = HD / 32;  // output dims per lane
+  extern __shared__ __align__(16) float asmem[];
+  float* qs = asmem;                  // [32][HD]
+  float* kt = qs + kAttnVecs * HD;    // [HD][32]: K transposed
+  float* vs = kt + HD * 32;           // [32][HD]
+  if (err_now(a.err)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
+  const int grp = a.nq / a.nkv;
+  const int tpc = kAttnVecs / grp;  // prompt tokens per CTA
+  const int p0 = blockIdx.y * tpc, p1 = min(a.P, p0 + tpc);
+  const int nv = (p1 - p0) * grp;
+  const int kv0 = a.sess[b].kv_len;
+  const float scale = 1.0f / sqrtf((float)HD);
+  // vector v: token p0 + v / grp, q head kvh * grp + v % grp
+  for (int i = threadIdx.x; i < kAttnVecs * HD; i += kAttnThreads) {
+    const int v = i / HD, e = i % HD;
+    float val = 0.f;
+    if (v < nv) {
+      const int p = p0 + v / grp, qh = kvh * grp + v % grp;
+      val = a.q[(size_t)(p * a.B + b) * a.nq * HD + qh * HD + e];
+    }
+    qs[i] = val;
+  }
+  float m[4], l[4], o[4][E];
+  int last[4];  // last position vector i attends to (-1: no vector)
+  int last_max = -1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int v = warp * 4 + i;
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+    last[i] = v < nv ? kv0 + p0 + v / grp : -1;
+    last_max = max(last_max, last[i]);
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[i][e] = 0.f;
+  }
+  const int npos = kv0 + p1;  // positions 0 .. npos - 1
+  for (int t0 = 0; t0 < npos; t0 += 32) {
+    __syncthreads();
+    // K and V of positions t0 .. t0 + 31 (two pages), 8 dims per thread step
+    for (int i = threadIdx.x; i < 2 * 32 * (HD / 8); i += kAttnThreads) {
+      const int kv = i / (32 * (HD / 8)), rem = i % (32 * (HD / 8));
+      const int j = rem / (HD / 8), e = (rem % (HD / 8)) * 8;
+      const int pos = t0 + j;
+      float v8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (pos < npos) {
+        const int page = a.bt[(size_t)b * a.bt_stride + pos / kPage];
+        if (page >= 0 && page < a.pool_pages) {
+          const uint4 w = *reinterpret_cast<const uint4*>(
+              a.kv_pool + ((((size_t)a.layer * a.pool_pages + page) * 2 + kv) * a.nkv + kvh) * kPage * HD +
+              (size_t)(pos % kPage) * HD + e);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            v8[2 * u] = bf2f(ww[u] & 0xFFFFu);
+            v8[2 * u + 1] = bf2f(ww[u] >> 16);
+          }
+        }
+      }
+      if (kv == 0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) kt[(e + u) * 32 + j] = v8[u];
+      } else {
+        *reinterpret_cast<float4*>(vs + j * HD + e) = make_float4(v8[0], v8[1], v8[2], v8[3]);
+        *reinterpret_cast<float4*>(vs + j * HD + e + 4) = make_float4(v8[4], v8[5], v8[6], v8[7]);
+      }
+    }
+    __syncthreads();
+    if (last_max < t0) continue;  // every vector of the warp ends before this tile
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* q0 = qs + (warp * 4) * HD;
+#pragma unroll 4
+    for (int e = 0; e < HD; e += 4) {
+      const float k0 = kt[e * 32 + lane], k1 = kt[(e + 1) * 32 + lane], k2 = kt[(e + 2) * 32 + lane],
+                  k3 = kt[(e + 3) * 32 + lane];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 qv = *reinterpret_cast<const float4*>(q0 + i * HD + e);
+        s[i] = fmaf(qv.x, k0, s[i]);
+        s[i] = fmaf(qv.y, k1, s[i]);
+        s[i] = fmaf(qv.z, k2, s[i]);
+        s[i] = fmaf(qv.w, k3, s[i]);
+      }
+    }
+    float pj[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool valid = t0 + lane <= last[i];
+      const float sc = valid ? s[i] * scale : -INFINITY;
+      const float mt = warp_max_f(sc);
+      if (mt == -INFINITY) {  // no key of this tile for vector i
+        pj[i] = 0.f;
+        continue;
+      }
+      const float mn = fmaxf(m[i], mt);
+      const float corr = expf(m[i] - mn);  // 0 on the first tile (m = -inf)
+      pj[i] = valid ? expf(sc - mn) : 0.f;
+      l[i] = l[i] * corr + warp_sum_f(pj[i]);
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[i][e] *= corr;
+      m[i] = mn;
+    }
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j) {
+      float vv[E];
+      if constexpr (E == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(vs + j * HD + lane * 4);
+        vv[0] = t.x; vv[1] = t.y; vv[2] = t.z; vv[3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(vs + j * HD + lane * 2);
+        vv[0] = t.x; vv[1] = t.y;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float pb = __shfl_sync(0xffffffffu, pj[i], j);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[i][e] = fmaf(pb, vv[e], o[i][e]);
+      }
+    }
+  }
+  // out: hi + lo of o / l at row (p, b), K index qh * HD + lane * E + e
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int v = warp * 4 + i;
+    if (v >= nv) continue;
+    const int p = p0 + v / grp, qh = kvh * grp + v % grp;
+    const int r = p * a.B + b;
+    const int k = qh * HD + lane * E;
+    const float inv = 1.0f / l[i];
+    uint16_t h[E], lo[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float val = o[i][e] * inv;
+      h[e] = f2bf(val);
+      lo[e] = f2bf(val - bf2f(h[e]));
+    }
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint2*>(a.A + a_off(r, k, a.KC, 0)) =
+          make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16));
+      *reinterpret_cast<uint2*>(a.A + a_off(r, k, a.KC, 1)) =
+          make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+    } else {
+      *reinterpret_cast<uint32_t*>(a.A + a_off(r, k, a.KC, 0)) = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
+      *reinterpret_cast<uint32_t*>(a.A + a_off(r, k, a.KC, 1)) = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// chunk validation: every session's positions kv_len .. kv_len + P - 1 fit
+// the context and its block table, and every page the chunk reads or writes
+// is in the pool
+// ---------------------------------------------------------------------------
+__global__ void check_kernel(const qtts_session* sess, const int32_t* bt, int bt_stride, int B, int P,
+                             int max_context, int pool_pages, int* err) {
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    const int kv = sess[b].kv_len;
+    if (kv < 0 || kv + P > max_context || kv + P > bt_stride * kPage) {
+      if (threadIdx.x == 0) err_set(err, QTTS_DEV_BAD_SESSION);
+      continue;
+    }
+    const int np = (kv + P + kPage - 1) / kPage;
+    for (int i = threadIdx.x; i < np; i += blockDim.x) {
+      const int page = bt[(size_t)b * bt_stride + i];
+      if (page < 0 || page >= pool_pages) err_set(err, QTTS_DEV_BAD_PAGE);
+    }
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+size_t pf_packed_elems(int N, int K) {
+  return (size_t)((N + kBN - 1) / kBN) * kBN * ((K + kBK - 1) / kBK) * kBK;
+}
+
+size_t pf_act_elems(int rows, int maxK) {
+  return (size_t)((rows + kBM - 1) / kBM) * ((maxK + kBK - 1) / kBK) * 2 * kAImg;
+}
+
+size_t pf_part_floats(int rows, int maxN) {
+  return (size_t)((rows + kBM - 1) / kBM) * kBM * ((maxN + kBN - 1) / kBN) * kBN;
+}
+
+cudaError_t pf_setup() {
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * kAttnVecs * 128 * 4);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * kAttnVecs * 64 * 4);
+  return e;
+}
+
+cudaError_t pf_pack_weights(const uint16_t* w, int N, int K, uint16_t* dst, cudaStream_t s) {
+  const int Npad = (N + kBN - 1) / kBN * kBN, KC = (K + kBK - 1) / kBK;
+  const long long groups = (long long)Npad * KC * (kBK / 8);
+  const int blocks = (int)std::min<long long>((groups + 255) / 256, 8192);
+  pack_weights_kernel<<<blocks, 256, 0, s>>>(w, N, K, Npad, KC, dst);
+  return cudaGetLastError();
+}
+
+// K-slices of a GEMM with `tiles` output tiles over KC K chunks: fewest
+// (waves of the grid x K chunks a CTA runs), ties to fewer slices, within the
+// partial-sum buffer
+static int pf_splits(int tiles, int KC, int G, size_t cap) {
+  const size_t tile_floats = (size_t)kBM * kBN;
+  int best = 1;
+  long long best_cost = (long long)((tiles + G - 1) / G) * KC;
+  for (int S = 2; S <= 8 && S <= KC; ++S) {
+    if ((size_t)S * tiles * tile_floats > cap) break;
+    const long long cost = (long long)((tiles * S + G - 1) / G) * ((KC + S - 1) / S);
+    if (cost < best_cost) {
+      best = S;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, const int32_t* bt, int bt_stride,
+                     const uint16_t* embeds, cudaStream_t s) {
+  const int M = B * P;
+  if (M < 1 || M > c.max_rows) return cudaErrorInvalidValue;
+  const int Mt = (M + kBM - 1) / kBM, Mpad = Mt * kBM;
+  const int KH = (c.H + kBK - 1) / kBK, KA = (c.nq * c.d + kBK - 1) / kBK, KF = (c.F + kBK - 1) / kBK;
+  check_kernel<<<std::min(B, 32), 128, 0, s>>>(sess, bt, bt_stride, B, P, c.max_context, c.pool_pages, c.err);
+  int S = 1, Npad = 0;
+  auto gemm = [&](const uint16_t* W, int N, int K) {
+    const int Nt = (N + kBN - 1) / kBN, KC = (K + kBK - 1) / kBK;
+    S = pf_splits(Nt * Mt, KC, c.G, c.part_floats);
+    Npad = Nt * kBN;
+    GemmArgs ga{c.A, W, c.part, KC, S, Mpad, Npad, c.err, c.wait_ns};
+    gemm_kernel<<<dim3(Nt, Mt, S), kGemmThreads, kGemmSmem, s>>>(ga);
+  };
+  auto norm = [&](const uint16_t* emb, bool add, const uint16_t* gain) {
+    NormArgs na{emb, c.x, add ? c.part : nullptr, S, Mpad, Npad, gain, c.eps, c.H, KH, c.A};
+    norm_kernel<<<M, kRowThreads, 0, s>>>(na);
+  };
+  norm(embeds, false, c.layers[0].in_norm);
+  const int grp = c.nq / c.nkv;
+  const int tpc = kAttnVecs / grp;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const PfLayer& L = c.layers[l];
+    gemm(L.qkv, (c.nq + 2 * c.nkv) * c.d, c.H);
+    QkvArgs qa{c.part, S, Mpad, Npad, B, sess, bt, bt_stride, l, c.nq, c.nkv, c.d, c.kv_pool, c.pool_pages,
+               c.rope_cos, c.rope_sin, c.q, c.err};
+    qkv_kernel<<<M, kRowThreads, 0, s>>>(qa);
+    if (l == c.n_layers - 1) break;  // the last layer's K/V are all a prompt pass leaves
+    AttnArgs aa{c.q, B, P, sess, bt, bt_stride, l, c.nq, c.nkv, c.kv_pool, c.pool_pages, c.A, KA, c.err};
+    const dim3 ag(B * c.nkv, (P + tpc - 1) / tpc);
+    if (c.d == 128)
+      attn_kernel<128><<<ag, kAttnThreads, 3 * kAttnVecs * 128 * 4, s>>>(aa);
+    else
+      attn_kernel<64><<<ag, kAttnThreads, 3 * kAttnVecs * 64 * 4, s>>>(aa);
+    gemm(L.o, c.H, c.nq * c.d);
+    norm(nullptr, true, L.post_norm);
+    gemm(L.gu, 2 * c.F, c.H);
+    SwigluArgs sa{c.part, S, Mpad, Npad, c.F, KF, c.A};
+    swiglu_kernel<<<M, kRowThreads, 0, s>>>(sa);
+    gemm(L.down, c.H, c.F);
+    norm(nullptr, true, c.layers[l + 1].in_norm);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace qtts

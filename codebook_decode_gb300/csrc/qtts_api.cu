@@ -28,6 +28,7 @@ struct LinW {
   int8_t* tqk = nullptr;  // q as tensor-core tiles for the K-split partition
   int8_t* q = nullptr;    // int8 [N][K]
   float* s = nullptr;     // [N]
+  uint16_t* pf = nullptr; // Talker weights only: bf16 tiles of the prefill GEMMs (pf_pack_weights)
   int N = 0, K = 0;
 };
 
@@ -99,10 +100,12 @@ struct qtts_model {
   uint32_t cp_tag0 = 0;       // that frame's tag base
   uint16_t* fb[2] = {nullptr, nullptr};  // qtts_frame_steps: next-frame inputs [max_batch][H]
 
+  // prefill: per-layer weight tiles and gains, scratch (built with the weights)
+  std::vector<PfLayer> pf_layers;
+  PfCtx pf{};
+
   // staging for qtts_frame_step_host
   qtts_session* st_sess = nullptr;
-  qtts_session* pf_sess = nullptr;  // prefill pass rows as sessions (one per prompt token and session)
-  int32_t* pf_bt = nullptr;         // their block-table rows
   int32_t* st_bt = nullptr;
   int st_bt_cap = 0;
   uint16_t* st_in = nullptr;
@@ -638,6 +641,36 @@ int build_tensor_tiles(qtts_model* m, bool i8) {
   return QTTS_OK;
 }
 
+// Prefill GEMM tiles of every Talker weight (always the bf16 ones) and the
+// prefill scratch for chunks of up to kPfMaxRows rows.
+int build_prefill(qtts_model* m) {
+  const qtts_config& c = m->cfg;
+  m->pf_layers.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    LayerW& L = m->tl[l];
+    for (LinW* W : {&L.qkv, &L.o, &L.gu, &L.down}) {
+      AL(m, W->pf, pf_packed_elems(W->N, W->K));
+      CK(m, pf_pack_weights(W->w, W->N, W->K, W->pf, 0));
+    }
+    m->pf_layers[l] = PfLayer{L.qkv.pf, L.o.pf, L.gu.pf, L.down.pf, L.in_norm, L.post_norm};
+  }
+  PfCtx& p = m->pf;
+  p.n_layers = c.n_layers; p.H = c.hidden; p.nq = c.n_q_heads; p.nkv = c.n_kv_heads; p.d = c.head_dim;
+  p.F = c.ffn; p.eps = c.rms_eps; p.G = m->G; p.layers = m->pf_layers.data();
+  p.kv_pool = m->kv_pool; p.pool_pages = c.kv_pool_pages; p.max_context = c.max_context;
+  p.rope_cos = m->g.rope_cos; p.rope_sin = m->g.rope_sin; p.err = m->g.err;
+  p.max_rows = kPfMaxRows;
+  const int maxK = std::max(std::max(c.hidden, c.n_q_heads * c.head_dim), c.ffn);
+  const int maxN = std::max(std::max(c.hidden, (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim), 2 * c.ffn);
+  p.part_floats = pf_part_floats(kPfMaxRows, maxN);
+  AL(m, p.x, (size_t)kPfMaxRows * c.hidden);
+  AL(m, p.q, (size_t)kPfMaxRows * c.n_q_heads * c.head_dim);
+  AL(m, p.A, pf_act_elems(kPfMaxRows, maxK));
+  AL(m, p.part, p.part_floats);
+  CK(m, cudaDeviceSynchronize());
+  return QTTS_OK;
+}
+
 }  // namespace
 
 // ==========================================================================
@@ -668,6 +701,7 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
     return fail(nullptr, QTTS_E_CUDA, "no CUDA device %d", device);
   if (cudaSetDevice(device) != cudaSuccess) return fail(nullptr, QTTS_E_CUDA, "cudaSetDevice(%d) failed", device);
   cudaError_t e = frame_kernel_setup();
+  if (e == cudaSuccess) e = pf_setup();
   if (e != cudaSuccess) return fail(nullptr, QTTS_E_CUDA, "kernel setup: %s", cudaGetErrorString(e));
   int coop = 0, sms = 0;
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
@@ -776,8 +810,6 @@ int qtts_create(const qtts_config* cfg, int device, qtts_model** out) {
   }
   // staging for the host-buffer frame
   m->st_bt_cap = (c.max_context + kPage - 1) / kPage;
-  if ((rc = dalloc(m, &m->pf_sess, kMaxBatch)) || (rc = dalloc(m, &m->pf_bt, (size_t)kMaxBatch * m->st_bt_cap)))
-    return bail(rc);
   if ((rc = dalloc(m, &m->st_sess, kMaxBatch)) || (rc = dalloc(m, &m->st_bt, (size_t)kMaxBatch * m->st_bt_cap)) ||
       (rc = dalloc(m, &m->st_in, (size_t)kMaxBatch * c.hidden)) || (rc = dalloc(m, &m->st_rng, kMaxBatch)) ||
       (rc = dalloc(m, &m->st_seen, (size_t)kMaxBatch * seen_words(c))) ||
@@ -863,6 +895,7 @@ int qtts_load_weights(qtts_model* m, const qtts_tensor* t, int n) {
   if (rc) return rc;
   if ((rc = build_tables(m, false))) return rc;
   if ((rc = build_tensor_tiles(m, false))) return rc;
+  if ((rc = build_prefill(m))) return rc;
   if ((rc = upload_program(m, false))) return rc;
   m->loaded = true;
   return QTTS_OK;
@@ -1062,45 +1095,17 @@ int qtts_talker_prefill(qtts_model* m, int B, qtts_session* sess, const int32_t*
   if (B < 1 || B > m->cfg.max_batch) return fail(m, QTTS_E_BATCH, "B=%d outside 1..%d", B, m->cfg.max_batch);
   if (!sess || !bt || bt_stride < 1 || (n_tok > 0 && !embeds) || n_tok < 0)
     return fail(m, QTTS_E_INVALID, "null array, bad block-table stride or negative token count");
-  if (bt_stride > m->st_bt_cap) return fail(m, QTTS_E_INVALID, "bt_stride %d exceeds %d", bt_stride, m->st_bt_cap);
   if (m->cp_pending) return fail(m, QTTS_E_STATE, "a split frame waits for qtts_frame_cp");
   cudaSetDevice(m->device);
   cudaStream_t s = (cudaStream_t)stream;
-  const int L = m->cfg.n_layers, H = m->cfg.hidden;
-  const StageDesc* prog = m->prog_dev[m->use_int8 ? 1 : 0];
-  // P prompt tokens of every session per pass: B x P rows (up to the
-  // kMaxBatch rows every per-session buffer holds), each a session of its own
-  // at kv_len + p (row p B + b; embeds are already in that order)
-  const int P_max = std::max(1, kMaxBatch / B);
+  const int H = m->cfg.hidden;
+  PfCtx ctx = m->pf;
+  ctx.wait_ns = m->g.wait_ns;
+  // chunks of P tokens of every session: B x P <= kPfMaxRows rows
+  const int P_max = std::max(1, kPfMaxRows / B);
   for (int t0 = 0; t0 < n_tok;) {
     const int P = std::min(P_max, n_tok - t0);
-    FrameArgs fa{};
-    fa.B = B * P;
-    fa.bt_stride = bt_stride;
-    fa.in_embeds = embeds + (size_t)t0 * B * H;
-    if (P == 1) {
-      fa.sess = sess;
-      fa.bt = bt;
-    } else {
-      CK(m, launch_prefill_rows(sess, bt, bt_stride, B, P, m->pf_sess, m->pf_bt, s));
-      fa.sess = m->pf_sess;
-      fa.bt = m->pf_bt;
-    }
-    int rc = take_tag0(m, &fa.tag0);  // one tag base for every launch of the pass
-    if (rc) return rc;
-    const Globals gl = m->g;
-    // the begin stage and the Talker layers; with several tokens per session
-    // the launches are cut before each attention stage: token p attends to
-    // tokens < p, whose K/V pages the previous launch wrote (a launch boundary
-    // makes them visible), and to its own K/V in the tagged words
-    int s0 = 0;
-    for (int l = 0; l <= L; ++l) {
-      const int s1 = (P == 1 || l == L) ? 1 + 5 * L : 2 + 5 * l;
-      cudaError_t e = launch_frame(prog, s0, s1, gl, fa, m->stepwise, s);
-      if (e != cudaSuccess) return cuda_fail(m, e, "prefill launch");
-      s0 = s1;
-      if (s1 == 1 + 5 * L) break;
-    }
+    CK(m, pf_chunk(ctx, B, P, sess, bt, bt_stride, embeds + (size_t)t0 * B * H, s));
     CK(m, launch_advance_kv(sess, B, m->g.err, P, s));
     t0 += P;
   }

@@ -211,14 +211,47 @@ cudaError_t launch_kv_scatter(uint16_t* pool, int pool_pages, int nkv, int d, in
 cudaError_t launch_tile_weights(const uint16_t* w, int N, int K, int G, uint16_t* t, cudaStream_t s);
 cudaError_t launch_tile_weights_i8(const int8_t* w, int N, int K, int G, int8_t* t, cudaStream_t s);
 cudaError_t launch_advance_kv(qtts_session* sess, int B, const int* err, int inc, cudaStream_t s);
-cudaError_t launch_prefill_rows(const qtts_session* sess, const int32_t* bt, int bt_stride, int B, int P,
-                                qtts_session* rsess, int32_t* rbt, cudaStream_t s);
 struct EmbedTables {
   const uint16_t* e[kCodebooks];
   int rows[kCodebooks];
 };
 cudaError_t launch_feedback(int B, int H, const int32_t* codes, const uint16_t* text, EmbedTables tables,
                             uint16_t* out, cudaStream_t s);
+
+// prefill.cu: the Talker prompt pass over chunks of up to kPfMaxRows rows
+// (B sessions x P prompt tokens, row p B + b), on tcgen05 GEMMs
+constexpr int kPfMaxRows = 1024;
+struct PfLayer {
+  const uint16_t *qkv, *o, *gu, *down;  // weights as prefill GEMM tiles (pf_pack_weights)
+  const uint16_t *in_norm, *post_norm;  // RMSNorm gains [H] bf16
+};
+struct PfCtx {
+  int n_layers, H, nq, nkv, d, F;
+  float eps;
+  int G;                    // SMs
+  const PfLayer* layers;    // host array [n_layers]
+  uint16_t* kv_pool;
+  int pool_pages, max_context;
+  const float* rope_cos;    // [max_context][d/2]
+  const float* rope_sin;
+  int* err;
+  unsigned long long wait_ns;
+  // scratch (device): residual rows, q rows, packed GEMM inputs, partial sums
+  float* x;                 // [kPfMaxRows][H]
+  float* q;                 // [kPfMaxRows][nq d]
+  uint16_t* A;              // pf_act_elems(kPfMaxRows, max(H, nq d, F))
+  float* part;              // part_floats
+  size_t part_floats;
+  int max_rows;
+};
+size_t pf_packed_elems(int N, int K);  // bf16 elements of one weight's prefill tiles
+size_t pf_act_elems(int rows, int maxK);
+size_t pf_part_floats(int rows, int maxN);
+cudaError_t pf_setup();
+cudaError_t pf_pack_weights(const uint16_t* w, int N, int K, uint16_t* dst, cudaStream_t s);
+// one chunk: validate, run the layers, append K/V (kv_len is not advanced here)
+cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, const int32_t* bt, int bt_stride,
+                     const uint16_t* embeds, cudaStream_t s);
 
 // qtts_api.cu: model internals for other translation units
 struct KvLayout {

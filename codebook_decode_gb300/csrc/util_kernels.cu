@@ -205,26 +205,4 @@ cudaError_t launch_advance_kv(qtts_session* sess, int B, const int* err, int inc
   return cudaGetLastError();
 }
 
-// Rows of a prefill pass over P prompt tokens of B sessions: row r = p B + b
-// is token p of session b, a session of its own with kv_len + p and session
-// b's block-table row (its K/V land in b's pages).
-__global__ void prefill_rows_kernel(const qtts_session* sess, const int32_t* bt, int bt_stride, int B, int P,
-                                    qtts_session* rsess, int32_t* rbt) {
-  const int r = blockIdx.x;
-  if (r >= B * P) return;
-  const int p = r / B, b = r - p * B;
-  if (threadIdx.x == 0) {
-    qtts_session x = sess[b];
-    x.kv_len += p;
-    rsess[r] = x;
-  }
-  for (int i = threadIdx.x; i < bt_stride; i += blockDim.x) rbt[(size_t)r * bt_stride + i] = bt[(size_t)b * bt_stride + i];
-}
-
-cudaError_t launch_prefill_rows(const qtts_session* sess, const int32_t* bt, int bt_stride, int B, int P,
-                                qtts_session* rsess, int32_t* rbt, cudaStream_t s) {
-  prefill_rows_kernel<<<B * P, 128, 0, s>>>(sess, bt, bt_stride, B, P, rsess, rbt);
-  return cudaGetLastError();
-}
-
 }  // namespace qtts

@@ -277,19 +277,25 @@ int qtts_frame_steps(qtts_model* m, int n_frames, int B, qtts_session* sessions,
 /* Talker prefill: a prompt of n_tok tokens per session through the Talker
  * layers: the causal prompt pass that runs before the first frame
  * ("Qwen3-TTS PR 5: 1.7B CustomVoice, VoiceDesign and Base", section Graph,
- * talker_prefill). Token t of session b sits at position kv_len_b + t and its
- * K/V are appended to the session's paged cache exactly as a decode frame
- * appends the new token's; no head, no sampling, no Code Predictor. A pass
- * takes P = 32 / B tokens of every session at once as B x P rows of
- * the frame program's begin and Talker stages (row p B + b: token p of
- * session b, at kv_len_b + p), with its launches cut before each attention
- * stage so a token reads the earlier tokens' K/V from the pages; then
- * kv_len += P. sessions, block_tables, bt_stride: as for qtts_frame_step
- * (kv_len advanced by n_tok in place; the block tables must cover
- * kv_len + n_tok). embeds: device [n_tok][B][hidden] bf16 (caller owns).
- * Asynchronous on `stream`; device-side errors (bad session or page) stop the
- * kv_len advance of that pass and are read with qtts_frame_status. Not
- * allowed between qtts_frame_talker and qtts_frame_cp (QTTS_E_STATE). */
+ * talker_prefill), packed into chunks like the page's token buckets (section
+ * "What changed": 32..1024 tokens). Token t of session b sits at position
+ * kv_len_b + t and its K/V are appended to the session's paged cache exactly
+ * as a decode frame appends the new token's; no head, no sampling, no Code
+ * Predictor. A chunk takes P = min(n_tok left, 1024 / B) tokens of every
+ * session as B x P rows (row p B + b: token p of session b) and runs each
+ * layer as whole-chunk kernels: RMSNorm, the QKV, O, gate/up and down
+ * projections as tcgen05 tensor-core GEMMs over all rows (activations as
+ * bf16 hi + lo pairs, fp32 accumulation), RoPE and the K/V append, causal
+ * attention over the pages (earlier chunks and the chunk's own tokens); then
+ * kv_len += P. The weights are the BF16 ones even with qtts_set_int8(m, 1):
+ * prefill stays BF16 ("Qwen3-TTS Native v0.3.0", "What changed").
+ * sessions, block_tables, bt_stride: as for qtts_frame_step (kv_len advanced
+ * by n_tok in place; the block tables must cover kv_len + n_tok, which must
+ * not exceed max_context). embeds: device [n_tok][B][hidden] bf16 (caller
+ * owns). Asynchronous on `stream`; device-side errors (bad session or page,
+ * found before a chunk writes anything) stop that chunk and every later one
+ * and are read with qtts_frame_status. Not allowed between
+ * qtts_frame_talker and qtts_frame_cp (QTTS_E_STATE). */
 int qtts_talker_prefill(qtts_model* m, int B, qtts_session* sessions, const int32_t* block_tables, int bt_stride,
                         const uint16_t* embeds, int n_tok, void* stream);
 

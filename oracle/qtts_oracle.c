@@ -477,7 +477,9 @@ int orc_frame_step(const orc_model* m, int B, orc_session* sess, uint16_t* const
 
 /* Talker prefill (header): the decode step's Talker layers, one prompt token
  * after another, which is the causal prompt pass the pages describe the
- * serving stacks running before the first frame. */
+ * serving stacks running before the first frame. Always on the BF16 weights:
+ * with INT8 decode enabled, prefill stays BF16 ("Qwen3-TTS Native v0.3.0",
+ * "What changed"). */
 int orc_talker_prefill(const orc_model* m, int B, orc_session* sess, uint16_t* const* kv, int kv_cap,
                        const uint16_t* embeds, int n_tok) {
   const orc_dims* D = &m->d;
@@ -493,7 +495,7 @@ int orc_talker_prefill(const orc_model* m, int B, orc_session* sess, uint16_t* c
       for (int i = 0; i < H; i++) x[i] = orc_from_bf16(embeds[((size_t)t * B + b) * H + i]);
       for (int l = 0; l < D->n_layers; l++) {
         uint16_t* kc = kv[b] + (size_t)l * 2 * kv_cap * t_tok;
-        run_layer(&m->talker[l], &tl, m->use_int8, x, pos, kc, kc + (size_t)kv_cap * t_tok);
+        run_layer(&m->talker[l], &tl, 0, x, pos, kc, kc + (size_t)kv_cap * t_tok);
       }
     }
     sess[b].kv_len += n_tok;

@@ -137,3 +137,34 @@ def test_library_frame_weight_bytes(d, int8):
     finally:
         eng.close()
         torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("d", [configs.TINY, configs.FULL])
+def test_prefill_flops_brute_force(d):
+    """The prefill FLOP model against a count token by token and layer by
+    layer from the model's tensor list: 2 FLOPs per weight for QKV in every
+    layer and for O, gate/up and down in all but the last; 4 per q dimension
+    and attended position (positions 0..kv_len + t) in those layers."""
+    shapes = {name: shape for name, shape, kind in synth.tensor_specs(d) if kind == "weight"}
+    kv0, n_tok = [5, 17, 0], 4
+    n = 0
+    for n0 in kv0:
+        for t in range(n_tok):
+            for l in range(d.n_layers):
+                pre = f"talker.layers.{l}."
+                for proj in ("q_proj", "k_proj", "v_proj"):
+                    n += 2 * shapes[pre + proj][0] * shapes[pre + proj][1]
+                if l == d.n_layers - 1:
+                    continue
+                for proj in ("o_proj", "gate_proj", "up_proj", "down_proj"):
+                    n += 2 * shapes[pre + proj][0] * shapes[pre + proj][1]
+                n += 4 * d.n_q_heads * d.head_dim * (n0 + t + 1)
+    assert bench.prefill_flops(d, kv0, n_tok) == n
+
+
+def test_prefill_kv_bytes_by_hand():
+    """Tiny model, one session with 10 cached positions and a 5-token prompt
+    in chunks of 2: chunk reads 10, 12, 14 positions and writes 2, 2, 1; a
+    position is 2 layers x K and V x 4 kv heads x 64 dims x 2 bytes."""
+    t_tok = 2 * 2 * 4 * 64 * 2
+    assert bench.prefill_kv_bytes(configs.TINY, [10], 5, 2) == (10 + 12 + 14 + 2 + 2 + 1) * t_tok

@@ -1,9 +1,11 @@
-"""GPU parity of the Talker prefill (qtts_talker_prefill) against the oracle's
-prompt pass: appended K/V to bf16 rounding at every layer and position,
-kv_len advanced by the prompt length, and the first decode frames after the
-prompt within the logit tolerance; on the CUDA-core and tensor-core GEMV
-paths, BF16 and INT8, with ragged prefixes across page boundaries, passes of
-one or several prompt tokens per session, and prompts split across calls."""
+"""GPU parity of the Talker prefill (qtts_talker_prefill: chunks of up to
+1,024 rows on tcgen05 GEMMs, RoPE/KV append, causal attention) against the
+oracle's prompt pass: appended K/V to bf16 rounding at every layer and
+position, kv_len advanced by the prompt length, and the first decode frames
+after the prompt within the logit tolerance. Covers ragged prefixes across
+page boundaries, chunks spanning several 128-row tiles with a ragged tail,
+prompts longer than one chunk, prompts split across calls, INT8 models (whose
+prefill stays BF16), full widths with several tiles, and the full model."""
 import numpy as np
 import pytest
 import torch
@@ -27,12 +29,14 @@ def sessions(d, B, prefixes, frames):
                           rep_penalty=1.05)
 
 
-@pytest.mark.parametrize("B,n_tok,tc_min,int8", [(1, 20, None, False), (3, 37, None, False), (9, 18, None, False),
-                                                 (3, 21, 1, False), (9, 17, None, True), (2, 19, None, True)])
-def test_prefill_matches_oracle(tiny_w, B, n_tok, tc_min, int8):
+@pytest.mark.parametrize("B,n_tok,int8", [(1, 20, False), (3, 37, False), (9, 18, False), (9, 17, True),
+                                         (2, 19, True), (3, 300, False), (1, 1100, False)])
+def test_prefill_matches_oracle(tiny_w, B, n_tok, int8):
+    """(3, 300): 900 rows, 8 row tiles with a ragged tail; (1, 1100): two
+    chunks (1,024 + 76 tokens)."""
     prefixes = [5, 16, 31, 0, 44, 9, 15, 33, 2]
     s = sessions(TINY, B, prefixes, n_tok + 3)
-    run = ParityRun(TINY, tiny_w, s, n_tok + 2, shuffle=True, int8=int8, tc_min_rows=tc_min)  # room for prompt + 2 frames
+    run = ParityRun(TINY, tiny_w, s, n_tok + 2, shuffle=True, int8=int8)  # room for prompt + 2 frames
     try:
         e = s.prompt_embeds(n_tok)
         run.eng.prefill(to_dev_u16(e, run.eng.dev))
@@ -106,6 +110,27 @@ def test_full_size_prefill(tiny_w):
         run.O.talker_prefill(run.rows, run.kv, run.cap, e)
         run.check_state()
         run.check_kv(layers=[0, d.n_layers - 1])
+        run.run(frames=1)
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+    finally:
+        free(run)
+
+
+def test_full_width_prefill_several_tiles():
+    """Full widths with 2 Talker layers, B = 2 x 160 tokens: 320 rows over 3
+    row tiles (the last half full) and every weight tile of the full widths;
+    the cache at both layers against the oracle, then one frame's logits."""
+    d = configs.Dims(**{**configs.FULL.as_dict(), "n_layers": 2})
+    w = synth.make_weights(d, 1002)
+    s = sessions(d, 2, [100, 37], 164)
+    run = ParityRun(d, w, s, 162, shuffle=True)
+    try:
+        e = s.prompt_embeds(160)
+        run.eng.prefill(to_dev_u16(e, run.eng.dev))
+        assert run.eng.status() == (0, 0)
+        run.O.talker_prefill(run.rows, run.kv, run.cap, e)
+        run.check_state()
+        run.check_kv()
         run.run(frames=1)
         assert run.max_rel() < TOL_BF16, run.max_rel()
     finally:

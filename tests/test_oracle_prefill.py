@@ -111,6 +111,28 @@ def test_prefill_chunks_compose(orc_lib, weights, int8):
         assert np.array_equal(kv1[b], kv2[b])
 
 
+def test_prefill_stays_bf16_under_int8(orc_lib, weights):
+    """With INT8 decode enabled the prompt pass still runs on the BF16 weights
+    ("Qwen3-TTS Native v0.3.0", What changed): its K/V equal the BF16 model's
+    bit for bit, while an INT8 decode frame after it differs from BF16's."""
+    s = sessions(2, 4)
+    e = prompt(5, 2, seed=11)
+    rows_b, kv_b = prefill(weights, s, e, int8=False)
+    rows_i, kv_i = prefill(weights, s, e, int8=True)
+    assert np.array_equal(rows_b, rows_i)
+    for b in range(2):
+        assert np.array_equal(kv_b[b], kv_i[b])
+    outs = []
+    for int8 in (False, True):
+        O = orc.Oracle(D, weights, use_int8=int8)
+        rows = rows_b.copy()
+        kv = [k.copy() for k in kv_b]
+        rng, seen = s.rng_state().copy(), s.seen_bitmap().copy()
+        O.frame_step(rows, kv, CAP, e[0], rng, seen, forced=s.forced_codes(0), want_logits=False)
+        outs.append(kv)
+    assert not np.array_equal(outs[0][0], outs[1][0])
+
+
 def test_prefill_matches_decode_frames(orc_lib, weights):
     """The prompt pass writes the K/V the decode frame would write for the
     same inputs, one token per frame (teacher-forced, so the sampler does not
