@@ -46,16 +46,6 @@ __device__ __forceinline__ uint64_t gtimer_ns() {
 __device__ __forceinline__ int err_now(const int* e) { return *(const volatile int*)e; }
 __device__ __forceinline__ void err_set(int* e, int code) { atomicCAS(e, 0, code); }
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ float warp_max_f(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum_f(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 
 __device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(n) : "memory");
@@ -476,13 +466,19 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_kernel(SwigluArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// causal attention: one CTA per (session, kv head, 32 query vectors: the
-// group's q heads of 32 / grp consecutive prompt tokens); 8 warps of 4
-// vectors; keys in tiles of 32 positions read from the pages (the chunk's
-// own K/V included), one position per lane, online softmax per vector
+// causal attention on the tensor cores (mma.sync m16n8k16, bf16 operands,
+// fp32 accumulation), flash style: one CTA per (session, kv head, block of
+// prompt tokens), each warp 16 query rows = the group's q heads of 16 / grp
+// consecutive tokens; K/V tiles of 64 positions from the pages into shared
+// memory (double buffered, cp.async), S = Q K^T, online softmax per row in
+// registers, O += P V. Q and P enter as bf16 hi + lo pairs (two MMAs each),
+// K and V are the cache's bf16 values.
 // ---------------------------------------------------------------------------
-constexpr int kAttnVecs = 32;
-constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = 2;
+constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kAttnKT = 64;  // positions per K/V tile
+__host__ __device__ constexpr int attn_ld(int HD) { return HD + 8; }  // padded row: conflict-free ldmatrix
+__host__ __device__ constexpr int attn_smem(int HD) { return 2 * 2 * kAttnKT * attn_ld(HD) * 2; }
 
 struct AttnArgs {
   const float* q;  // [M][nq d], RoPE applied
@@ -498,153 +494,215 @@ struct AttnArgs {
   int* err;
 };
 
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(__cvta_generic_to_global(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// (hi, lo) bf16 pairs of two fp32 values
+__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const uint16_t hx = f2bf(x), hy = f2bf(y);
+  hi = (uint32_t)hx | ((uint32_t)hy << 16);
+  lo = (uint32_t)f2bf(x - bf2f(hx)) | ((uint32_t)f2bf(y - bf2f(hy)) << 16);
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
-  constexpr int E = HD / 32;  // output dims per lane
-  extern __shared__ __align__(16) float asmem[];
-  float* qs = asmem;                  // [32][HD]
-  float* kt = qs + kAttnVecs * HD;    // [HD][32]: K transposed
-  float* vs = kt + HD * 32;           // [32][HD]
+  constexpr int LD = attn_ld(HD);
+  constexpr int NKS = HD / 16;  // k steps of Q K^T; pairs of 8-wide dim tiles of P V
+  constexpr int NDT = HD / 8;   // 8-wide output dim tiles
+  extern __shared__ __align__(16) uint16_t kvs[];  // [2 buffers][K | V][kAttnKT][LD]
   if (err_now(a.err)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
   const int b = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
   const int grp = a.nq / a.nkv;
-  const int tpc = kAttnVecs / grp;  // prompt tokens per CTA
-  const int p0 = blockIdx.y * tpc, p1 = min(a.P, p0 + tpc);
-  const int nv = (p1 - p0) * grp;
+  const int tw = 16 / grp;  // tokens per warp
+  const int pc0 = blockIdx.y * kAttnWarps * tw;
+  const int pw0 = pc0 + warp * tw;
   const int kv0 = a.sess[b].kv_len;
   const float scale = 1.0f / sqrtf((float)HD);
-  // vector v: token p0 + v / grp, q head kvh * grp + v % grp
-  for (int i = threadIdx.x; i < kAttnVecs * HD; i += kAttnThreads) {
-    const int v = i / HD, e = i % HD;
-    float val = 0.f;
-    if (v < nv) {
-      const int p = p0 + v / grp, qh = kvh * grp + v % grp;
-      val = a.q[(size_t)(p * a.B + b) * a.nq * HD + qh * HD + e];
+  // rows g and g + 8 of this lane: row i is token pw0 + i % tw, q head kvh grp + i / tw
+  int tok[2], head[2], lastpos[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = g + 8 * h;
+    tok[h] = pw0 + i % tw;
+    head[h] = kvh * grp + i / tw;
+    lastpos[h] = tok[h] < a.P ? kv0 + tok[h] : -1;  // -1: padding row
+  }
+  const int warp_last = kv0 + min(a.P, pw0 + tw) - 1;  // < kv0 when the warp has no token
+  const int cta_last = kv0 + min(a.P, pc0 + kAttnWarps * tw) - 1;
+  const int npos = cta_last + 1;
+  // Q fragments (A operand, row major 16 x 16 per k step), hi and lo
+  uint32_t qh[NKS][4], ql[NKS][4];
+#pragma unroll
+  for (int ks = 0; ks < NKS; ++ks)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int h = j & 1;                       // a0a1: row g; a2a3: row g+8; then cols + 8
+      const int col = 16 * ks + 2 * c + 8 * (j >> 1);
+      float2 v = make_float2(0.f, 0.f);
+      if (lastpos[h] >= 0)
+        v = *reinterpret_cast<const float2*>(a.q + (size_t)(tok[h] * a.B + b) * a.nq * HD + head[h] * HD + col);
+      split2(v.x, v.y, qh[ks][j], ql[ks][j]);
     }
-    qs[i] = val;
-  }
-  float m[4], l[4], o[4][E];
-  int last[4];  // last position vector i attends to (-1: no vector)
-  int last_max = -1;
+  float o[NDT][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int v = warp * 4 + i;
-    m[i] = -INFINITY;
-    l[i] = 0.f;
-    last[i] = v < nv ? kv0 + p0 + v / grp : -1;
-    last_max = max(last_max, last[i]);
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[i][e] = 0.f;
-  }
-  const int npos = kv0 + p1;  // positions 0 .. npos - 1
-  for (int t0 = 0; t0 < npos; t0 += 32) {
-    __syncthreads();
-    // K and V of positions t0 .. t0 + 31 (two pages), 8 dims per thread step
-    for (int i = threadIdx.x; i < 2 * 32 * (HD / 8); i += kAttnThreads) {
-      const int kv = i / (32 * (HD / 8)), rem = i % (32 * (HD / 8));
+  for (int j = 0; j < NDT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+  const uint32_t sbase = saddr(kvs);
+  const int ntiles = (npos + kAttnKT - 1) / kAttnKT;
+  auto load_tile = [&](int t, int buf) {
+    // K and V of positions t*KT .. t*KT + KT - 1: 16-byte pieces, zero past npos
+    for (int i = threadIdx.x; i < 2 * kAttnKT * (HD / 8); i += kAttnThreads) {
+      const int kv = i / (kAttnKT * (HD / 8)), rem = i % (kAttnKT * (HD / 8));
       const int j = rem / (HD / 8), e = (rem % (HD / 8)) * 8;
-      const int pos = t0 + j;
-      float v8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const int pos = t * kAttnKT + j;
+      const uint16_t* src = a.kv_pool;
+      int bytes = 0;
       if (pos < npos) {
         const int page = a.bt[(size_t)b * a.bt_stride + pos / kPage];
-        if (page >= 0 && page < a.pool_pages) {
-          const uint4 w = *reinterpret_cast<const uint4*>(
-              a.kv_pool + ((((size_t)a.layer * a.pool_pages + page) * 2 + kv) * a.nkv + kvh) * kPage * HD +
-              (size_t)(pos % kPage) * HD + e);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            v8[2 * u] = bf2f(ww[u] & 0xFFFFu);
-            v8[2 * u + 1] = bf2f(ww[u] >> 16);
-          }
+        if (page >= 0 && page < a.pool_pages) {  // checked before the chunk
+          src = a.kv_pool + ((((size_t)a.layer * a.pool_pages + page) * 2 + kv) * a.nkv + kvh) * kPage * HD +
+                (size_t)(pos % kPage) * HD + e;
+          bytes = 16;
         }
       }
-      if (kv == 0) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) kt[(e + u) * 32 + j] = v8[u];
-      } else {
-        *reinterpret_cast<float4*>(vs + j * HD + e) = make_float4(v8[0], v8[1], v8[2], v8[3]);
-        *reinterpret_cast<float4*>(vs + j * HD + e + 4) = make_float4(v8[4], v8[5], v8[6], v8[7]);
-      }
+      cp_async16(sbase + (uint32_t)((((buf * 2 + kv) * kAttnKT + j) * LD + e) * 2), src, bytes);
+    }
+    cp_async_commit();
+  };
+  if (ntiles > 0) load_tile(0, 0);
+  for (int t = 0; t < ntiles; ++t) {
+    if (t + 1 < ntiles) {
+      load_tile(t + 1, (t + 1) & 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-    if (last_max < t0) continue;  // every vector of the warp ends before this tile
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* q0 = qs + (warp * 4) * HD;
-#pragma unroll 4
-    for (int e = 0; e < HD; e += 4) {
-      const float k0 = kt[e * 32 + lane], k1 = kt[(e + 1) * 32 + lane], k2 = kt[(e + 2) * 32 + lane],
-                  k3 = kt[(e + 3) * 32 + lane];
+    if (warp_last >= t * kAttnKT) {
+      const int buf = t & 1;
+      const uint32_t kb = sbase + (uint32_t)((buf * 2 + 0) * kAttnKT * LD * 2);
+      const uint32_t vb = sbase + (uint32_t)((buf * 2 + 1) * kAttnKT * LD * 2);
+      const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: this lane's matrix and row
+      // S = Q K^T for 64 positions: 8 tiles of 8
+      float sc[8][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 qv = *reinterpret_cast<const float4*>(q0 + i * HD + e);
-        s[i] = fmaf(qv.x, k0, s[i]);
-        s[i] = fmaf(qv.y, k1, s[i]);
-        s[i] = fmaf(qv.z, k2, s[i]);
-        s[i] = fmaf(qv.w, k3, s[i]);
+      for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < NKS; ++ks)
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          uint32_t kf[4];  // positions 16np + 8 (mi / 2) + mr, dims 16ks + 8 (mi % 2)
+          ldsm_x4(kf, kb + (uint32_t)(((16 * np + 8 * (mi >> 1) + mr) * LD + 16 * ks + 8 * (mi & 1)) * 2));
+          mma_bf16(sc[2 * np], qh[ks], kf[0], kf[1]);
+          mma_bf16(sc[2 * np], ql[ks], kf[0], kf[1]);
+          mma_bf16(sc[2 * np + 1], qh[ks], kf[2], kf[3]);
+          mma_bf16(sc[2 * np + 1], ql[ks], kf[2], kf[3]);
+        }
+      // scale, causal mask, online softmax (rows g and g + 8; a row's values sit in the 4 lanes of a group)
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h = e >> 1;
+          const int pos = t * kAttnKT + 8 * j + 2 * c + (e & 1);
+          const float v = pos <= lastpos[h] ? sc[j][e] * scale : -INFINITY;
+          sc[j][e] = v;
+          mx[h] = fmaxf(mx[h], v);
+        }
+      float corr[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        const float mn = fmaxf(mrow[h], mx[h]);
+        corr[h] = mn == -INFINITY ? 1.f : expf(mrow[h] - mn);  // 0 while the row had nothing yet
+        mrow[h] = mn;
+      }
+      float rs[2] = {0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h = e >> 1;
+          const float p = sc[j][e] == -INFINITY ? 0.f : expf(sc[j][e] - mrow[h]);
+          sc[j][e] = p;
+          rs[h] += p;
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
+        rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
+        lrow[h] = lrow[h] * corr[h] + rs[h];
+      }
+#pragma unroll
+      for (int j = 0; j < NDT; ++j) {
+        o[j][0] *= corr[0];
+        o[j][1] *= corr[0];
+        o[j][2] *= corr[1];
+        o[j][3] *= corr[1];
+      }
+      // O += P V: P's accumulator tiles (2kk, 2kk + 1) are the A fragment of k step kk
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t ph[4], pl[4];
+        split2(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
+        split2(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
+        split2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
+        split2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+        for (int dp = 0; dp < NKS; ++dp) {
+          uint32_t vf[4];  // positions 16kk + 8 (mi % 2) + mr, dims 16dp + 8 (mi / 2), transposed
+          ldsm_x4_t(vf, vb + (uint32_t)(((16 * kk + 8 * (mi & 1) + mr) * LD + 16 * dp + 8 * (mi >> 1)) * 2));
+          mma_bf16(o[2 * dp], ph, vf[0], vf[1]);
+          mma_bf16(o[2 * dp], pl, vf[0], vf[1]);
+          mma_bf16(o[2 * dp + 1], ph, vf[2], vf[3]);
+          mma_bf16(o[2 * dp + 1], pl, vf[2], vf[3]);
+        }
       }
     }
-    float pj[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const bool valid = t0 + lane <= last[i];
-      const float sc = valid ? s[i] * scale : -INFINITY;
-      const float mt = warp_max_f(sc);
-      if (mt == -INFINITY) {  // no key of this tile for vector i
-        pj[i] = 0.f;
-        continue;
-      }
-      const float mn = fmaxf(m[i], mt);
-      const float corr = expf(m[i] - mn);  // 0 on the first tile (m = -inf)
-      pj[i] = valid ? expf(sc - mn) : 0.f;
-      l[i] = l[i] * corr + warp_sum_f(pj[i]);
-#pragma unroll
-      for (int e = 0; e < E; ++e) o[i][e] *= corr;
-      m[i] = mn;
-    }
-#pragma unroll 4
-    for (int j = 0; j < 32; ++j) {
-      float vv[E];
-      if constexpr (E == 4) {
-        const float4 t = *reinterpret_cast<const float4*>(vs + j * HD + lane * 4);
-        vv[0] = t.x; vv[1] = t.y; vv[2] = t.z; vv[3] = t.w;
-      } else {
-        const float2 t = *reinterpret_cast<const float2*>(vs + j * HD + lane * 2);
-        vv[0] = t.x; vv[1] = t.y;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float pb = __shfl_sync(0xffffffffu, pj[i], j);
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[i][e] = fmaf(pb, vv[e], o[i][e]);
-      }
-    }
+    __syncthreads();  // the buffer is refilled two tiles on
   }
-  // out: hi + lo of o / l at row (p, b), K index qh * HD + lane * E + e
+  // out: hi + lo of O / l at row (token, b), K index head * HD + dim
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int v = warp * 4 + i;
-    if (v >= nv) continue;
-    const int p = p0 + v / grp, qh = kvh * grp + v % grp;
-    const int r = p * a.B + b;
-    const int k = qh * HD + lane * E;
-    const float inv = 1.0f / l[i];
-    uint16_t h[E], lo[E];
+  for (int h = 0; h < 2; ++h) {
+    if (lastpos[h] < 0) continue;
+    const int r = tok[h] * a.B + b;
+    const float inv = 1.0f / lrow[h];
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float val = o[i][e] * inv;
-      h[e] = f2bf(val);
-      lo[e] = f2bf(val - bf2f(h[e]));
-    }
-    if constexpr (E == 4) {
-      *reinterpret_cast<uint2*>(a.A + a_off(r, k, a.KC, 0)) =
-          make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16));
-      *reinterpret_cast<uint2*>(a.A + a_off(r, k, a.KC, 1)) =
-          make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
-    } else {
-      *reinterpret_cast<uint32_t*>(a.A + a_off(r, k, a.KC, 0)) = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
-      *reinterpret_cast<uint32_t*>(a.A + a_off(r, k, a.KC, 1)) = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
+    for (int j = 0; j < NDT; ++j) {
+      const int k = head[h] * HD + 8 * j + 2 * c;
+      uint32_t hi, lo;
+      split2(o[j][2 * h] * inv, o[j][2 * h + 1] * inv, hi, lo);
+      *reinterpret_cast<uint32_t*>(a.A + a_off(r, k, a.KC, 0)) = hi;
+      *reinterpret_cast<uint32_t*>(a.A + a_off(r, k, a.KC, 1)) = lo;
     }
   }
 }
@@ -691,9 +749,9 @@ size_t pf_part_floats(int rows, int maxN) {
 cudaError_t pf_setup() {
   cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * kAttnVecs * 128 * 4);
+    e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem(128));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * kAttnVecs * 64 * 4);
+    e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem(64));
   return e;
 }
 
@@ -744,7 +802,7 @@ cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, con
   };
   norm(embeds, false, c.layers[0].in_norm);
   const int grp = c.nq / c.nkv;
-  const int tpc = kAttnVecs / grp;
+  const int tpc = kAttnWarps * (16 / grp);  // prompt tokens per attention CTA
   for (int l = 0; l < c.n_layers; ++l) {
     const PfLayer& L = c.layers[l];
     gemm(L.qkv, (c.nq + 2 * c.nkv) * c.d, c.H);
@@ -755,9 +813,9 @@ cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, con
     AttnArgs aa{c.q, B, P, sess, bt, bt_stride, l, c.nq, c.nkv, c.kv_pool, c.pool_pages, c.A, KA, c.err};
     const dim3 ag(B * c.nkv, (P + tpc - 1) / tpc);
     if (c.d == 128)
-      attn_kernel<128><<<ag, kAttnThreads, 3 * kAttnVecs * 128 * 4, s>>>(aa);
+      attn_kernel<128><<<ag, kAttnThreads, attn_smem(128), s>>>(aa);
     else
-      attn_kernel<64><<<ag, kAttnThreads, 3 * kAttnVecs * 64 * 4, s>>>(aa);
+      attn_kernel<64><<<ag, kAttnThreads, attn_smem(64), s>>>(aa);
     gemm(L.o, c.H, c.nq * c.d);
     norm(nullptr, true, L.post_norm);
     gemm(L.gu, 2 * c.F, c.H);
