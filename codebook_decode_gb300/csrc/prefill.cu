@@ -467,16 +467,19 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_kernel(SwigluArgs a) {
 
 // ---------------------------------------------------------------------------
 // causal attention on the tensor cores (mma.sync m16n8k16, bf16 operands,
-// fp32 accumulation), flash style: one CTA per (session, kv head, block of
-// prompt tokens), each warp 16 query rows = the group's q heads of 16 / grp
-// consecutive tokens; K/V tiles of 64 positions from the pages into shared
-// memory (double buffered, cp.async), S = Q K^T, online softmax per row in
-// registers, O += P V. Q and P enter as bf16 hi + lo pairs (two MMAs each),
-// K and V are the cache's bf16 values.
+// fp32 accumulation), flash style, split over the key positions: one CTA per
+// (session, kv head, block of prompt tokens, chunk of kAttnChunk positions),
+// each warp 16 query rows = the group's q heads of 16 / grp consecutive
+// tokens; K/V tiles of 64 positions from the pages into shared memory (double
+// buffered, cp.async), S = Q K^T, online softmax per row in registers (base
+// 2), O += P V; the chunk's unnormalised O, running max and sum go to a
+// scratch area that a second kernel combines in chunk order. Q and P enter
+// as bf16 hi + lo pairs (two MMAs each), K and V are the cache's bf16 values.
 // ---------------------------------------------------------------------------
 constexpr int kAttnWarps = 2;
 constexpr int kAttnThreads = kAttnWarps * 32;
-constexpr int kAttnKT = 64;  // positions per K/V tile
+constexpr int kAttnKT = 64;      // positions per K/V tile
+constexpr int kAttnChunk = 256;  // positions per CTA (4 tiles)
 __host__ __device__ constexpr int attn_ld(int HD) { return HD + 8; }  // padded row: conflict-free ldmatrix
 __host__ __device__ constexpr int attn_smem(int HD) { return 2 * 2 * kAttnKT * attn_ld(HD) * 2; }
 
@@ -489,8 +492,9 @@ struct AttnArgs {
   int layer, nq, nkv;
   const uint16_t* kv_pool;
   int pool_pages;
-  uint16_t* A;     // packed output rows, K = nq d
-  int KC;
+  float* po;       // partials [(row nq + head) maxc + chunk][d + 4]: O (unnormalised), max (base 2), sum, 2 pad
+                   // (a multiple of 4 floats, so the rows stay 16-byte aligned)
+  int maxc;
   int* err;
 };
 
@@ -521,6 +525,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+__device__ __forceinline__ constexpr int h_of(int e) { return e >> 1; }  // accumulator element -> row g (0) or g + 8 (1)
 // (hi, lo) bf16 pairs of two fp32 values
 __device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
   const uint16_t hx = f2bf(x), hy = f2bf(y);
@@ -543,7 +548,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   const int pc0 = blockIdx.y * kAttnWarps * tw;
   const int pw0 = pc0 + warp * tw;
   const int kv0 = a.sess[b].kv_len;
-  const float scale = 1.0f / sqrtf((float)HD);
+  const int chunk = blockIdx.z;
+  // scores in base 2: q.k / sqrt(d) * log2(e)
+  const float scale = 1.4426950408889634f / sqrtf((float)HD);
   // rows g and g + 8 of this lane: row i is token pw0 + i % tw, q head kvh grp + i / tw
   int tok[2], head[2], lastpos[2];
 #pragma unroll
@@ -556,6 +563,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   const int warp_last = kv0 + min(a.P, pw0 + tw) - 1;  // < kv0 when the warp has no token
   const int cta_last = kv0 + min(a.P, pc0 + kAttnWarps * tw) - 1;
   const int npos = cta_last + 1;
+  if (chunk * kAttnChunk >= npos) return;  // no position of this chunk is needed by the block
   // Q fragments (A operand, row major 16 x 16 per k step), hi and lo
   uint32_t qh[NKS][4], ql[NKS][4];
 #pragma unroll
@@ -575,7 +583,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
   const uint32_t sbase = saddr(kvs);
-  const int ntiles = (npos + kAttnKT - 1) / kAttnKT;
+  const int t_begin = chunk * (kAttnChunk / kAttnKT);
+  const int t_end = min((npos + kAttnKT - 1) / kAttnKT, t_begin + kAttnChunk / kAttnKT);
   auto load_tile = [&](int t, int buf) {
     // K and V of positions t*KT .. t*KT + KT - 1: 16-byte pieces, zero past npos
     for (int i = threadIdx.x; i < 2 * kAttnKT * (HD / 8); i += kAttnThreads) {
@@ -596,17 +605,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     }
     cp_async_commit();
   };
-  if (ntiles > 0) load_tile(0, 0);
-  for (int t = 0; t < ntiles; ++t) {
-    if (t + 1 < ntiles) {
-      load_tile(t + 1, (t + 1) & 1);
+  load_tile(t_begin, 0);
+  for (int t = t_begin; t < t_end; ++t) {
+    if (t + 1 < t_end) {
+      load_tile(t + 1, (t + 1 - t_begin) & 1);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
     if (warp_last >= t * kAttnKT) {
-      const int buf = t & 1;
+      const int buf = (t - t_begin) & 1;
       const uint32_t kb = sbase + (uint32_t)((buf * 2 + 0) * kAttnKT * LD * 2);
       const uint32_t vb = sbase + (uint32_t)((buf * 2 + 1) * kAttnKT * LD * 2);
       const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: this lane's matrix and row
@@ -625,25 +634,39 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
           mma_bf16(sc[2 * np + 1], qh[ks], kf[2], kf[3]);
           mma_bf16(sc[2 * np + 1], ql[ks], kf[2], kf[3]);
         }
-      // scale, causal mask, online softmax (rows g and g + 8; a row's values sit in the 4 lanes of a group)
+      // scale, causal mask (only where the tile reaches past the warp's first
+      // token: rows of padding tokens are never written, so unmasked is fine
+      // for them), online softmax (rows g and g + 8; a row's values sit in the
+      // 4 lanes of a group)
       float mx[2] = {-INFINITY, -INFINITY};
+      if ((t + 1) * kAttnKT - 1 > kv0 + pw0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h = e >> 1;
-          const int pos = t * kAttnKT + 8 * j + 2 * c + (e & 1);
-          const float v = pos <= lastpos[h] ? sc[j][e] * scale : -INFINITY;
-          sc[j][e] = v;
-          mx[h] = fmaxf(mx[h], v);
-        }
+          for (int e = 0; e < 4; ++e) {
+            const int h = e >> 1;
+            const int pos = t * kAttnKT + 8 * j + 2 * c + (e & 1);
+            const float v = pos <= lastpos[h] ? sc[j][e] * scale : -INFINITY;
+            sc[j][e] = v;
+            mx[h] = fmaxf(mx[h], v);
+          }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v = sc[j][e] * scale;
+            sc[j][e] = v;
+            mx[h_of(e)] = fmaxf(mx[h_of(e)], v);
+          }
+      }
       float corr[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
         const float mn = fmaxf(mrow[h], mx[h]);
-        corr[h] = mn == -INFINITY ? 1.f : expf(mrow[h] - mn);  // 0 while the row had nothing yet
+        corr[h] = mn == -INFINITY ? 1.f : exp2f(mrow[h] - mn);  // 0 while the row had nothing yet
         mrow[h] = mn;
       }
       float rs[2] = {0.f, 0.f};
@@ -652,7 +675,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int h = e >> 1;
-          const float p = sc[j][e] == -INFINITY ? 0.f : expf(sc[j][e] - mrow[h]);
+          const float p = sc[j][e] == -INFINITY ? 0.f : exp2f(sc[j][e] - mrow[h]);
           sc[j][e] = p;
           rs[h] += p;
         }
@@ -690,20 +713,56 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     }
     __syncthreads();  // the buffer is refilled two tiles on
   }
-  // out: hi + lo of O / l at row (token, b), K index head * HD + dim
+  // the chunk's partial state of each real row: O (unnormalised), max, sum
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     if (lastpos[h] < 0) continue;
     const int r = tok[h] * a.B + b;
-    const float inv = 1.0f / lrow[h];
+    float* dst = a.po + ((size_t)(r * a.nq + head[h]) * a.maxc + chunk) * (HD + 4);
 #pragma unroll
-    for (int j = 0; j < NDT; ++j) {
-      const int k = head[h] * HD + 8 * j + 2 * c;
-      uint32_t hi, lo;
-      split2(o[j][2 * h] * inv, o[j][2 * h + 1] * inv, hi, lo);
-      *reinterpret_cast<uint32_t*>(a.A + a_off(r, k, a.KC, 0)) = hi;
-      *reinterpret_cast<uint32_t*>(a.A + a_off(r, k, a.KC, 1)) = lo;
+    for (int j = 0; j < NDT; ++j)
+      *reinterpret_cast<float2*>(dst + 8 * j + 2 * c) = make_float2(o[j][2 * h], o[j][2 * h + 1]);
+    if (c == 0) {
+      dst[HD] = mrow[h];
+      dst[HD + 1] = lrow[h];
     }
+  }
+}
+
+struct CombineArgs {
+  const float* po;
+  int maxc, B, nq, d, KC;
+  const qtts_session* sess;
+  uint16_t* A;
+  int* err;
+};
+
+// O of row r and every q head: the chunks' partial states merged in chunk
+// order (max of the maxima, weights 2^(m_c - m)), packed as hi + lo
+__global__ void __launch_bounds__(kRowThreads) attn_combine_kernel(CombineArgs a) {
+  if (err_now(a.err)) return;
+  const int r = blockIdx.x, b = r % a.B, p = r / a.B;
+  const int nc = (a.sess[b].kv_len + p + 1 + kAttnChunk - 1) / kAttnChunk;  // chunks holding this row's positions
+  for (int u = threadIdx.x; u < a.nq * a.d / 8; u += kRowThreads) {
+    const int head = (u * 8) / a.d, e = (u * 8) % a.d;
+    const float* src = a.po + (size_t)(r * a.nq + head) * a.maxc * (a.d + 4);
+    float m = -INFINITY;
+    for (int ch = 0; ch < nc; ++ch) m = fmaxf(m, src[(size_t)ch * (a.d + 4) + a.d]);
+    float l = 0.f, v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int ch = 0; ch < nc; ++ch) {
+      const float* pc = src + (size_t)ch * (a.d + 4);
+      const float mc = pc[a.d];
+      if (mc == -INFINITY) continue;  // no position of the chunk for this row
+      const float w = exp2f(mc - m);
+      l += w * pc[a.d + 1];
+      const float4 x0 = *reinterpret_cast<const float4*>(pc + e), x1 = *reinterpret_cast<const float4*>(pc + e + 4);
+      v[0] += w * x0.x; v[1] += w * x0.y; v[2] += w * x0.z; v[3] += w * x0.w;
+      v[4] += w * x1.x; v[5] += w * x1.y; v[6] += w * x1.z; v[7] += w * x1.w;
+    }
+    const float inv = 1.0f / l;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] *= inv;
+    put8(a.A, r, head * a.d + e, a.KC, v);
   }
 }
 
@@ -740,6 +799,12 @@ size_t pf_packed_elems(int N, int K) {
 
 size_t pf_act_elems(int rows, int maxK) {
   return (size_t)((rows + kBM - 1) / kBM) * ((maxK + kBK - 1) / kBK) * 2 * kAImg;
+}
+
+int pf_attn_chunks(int max_context) { return (max_context + kAttnChunk - 1) / kAttnChunk; }
+
+size_t pf_attn_floats(int rows, int nq, int d, int max_context) {
+  return (size_t)rows * nq * pf_attn_chunks(max_context) * (d + 4);
 }
 
 size_t pf_part_floats(int rows, int maxN) {
@@ -803,6 +868,7 @@ cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, con
   norm(embeds, false, c.layers[0].in_norm);
   const int grp = c.nq / c.nkv;
   const int tpc = kAttnWarps * (16 / grp);  // prompt tokens per attention CTA
+  const int maxc = pf_attn_chunks(c.max_context);
   for (int l = 0; l < c.n_layers; ++l) {
     const PfLayer& L = c.layers[l];
     gemm(L.qkv, (c.nq + 2 * c.nkv) * c.d, c.H);
@@ -810,12 +876,14 @@ cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, con
                c.rope_cos, c.rope_sin, c.q, c.err};
     qkv_kernel<<<M, kRowThreads, 0, s>>>(qa);
     if (l == c.n_layers - 1) break;  // the last layer's K/V are all a prompt pass leaves
-    AttnArgs aa{c.q, B, P, sess, bt, bt_stride, l, c.nq, c.nkv, c.kv_pool, c.pool_pages, c.A, KA, c.err};
-    const dim3 ag(B * c.nkv, (P + tpc - 1) / tpc);
+    AttnArgs aa{c.q, B, P, sess, bt, bt_stride, l, c.nq, c.nkv, c.kv_pool, c.pool_pages, c.po, maxc, c.err};
+    const dim3 ag(B * c.nkv, (P + tpc - 1) / tpc, maxc);
     if (c.d == 128)
       attn_kernel<128><<<ag, kAttnThreads, attn_smem(128), s>>>(aa);
     else
       attn_kernel<64><<<ag, kAttnThreads, attn_smem(64), s>>>(aa);
+    CombineArgs ca{c.po, maxc, B, c.nq, c.d, KA, sess, c.A, c.err};
+    attn_combine_kernel<<<M, kRowThreads, 0, s>>>(ca);
     gemm(L.o, c.H, c.nq * c.d);
     norm(nullptr, true, L.post_norm);
     gemm(L.gu, 2 * c.F, c.H);

@@ -242,11 +242,14 @@ struct PfCtx {
   uint16_t* A;              // pf_act_elems(kPfMaxRows, max(H, nq d, F))
   float* part;              // part_floats
   size_t part_floats;
+  float* po;                // attention partials: pf_attn_floats(kPfMaxRows, nq, d, max_context)
   int max_rows;
 };
 size_t pf_packed_elems(int N, int K);  // bf16 elements of one weight's prefill tiles
 size_t pf_act_elems(int rows, int maxK);
 size_t pf_part_floats(int rows, int maxN);
+int pf_attn_chunks(int max_context);
+size_t pf_attn_floats(int rows, int nq, int d, int max_context);
 cudaError_t pf_setup();
 cudaError_t pf_pack_weights(const uint16_t* w, int N, int K, uint16_t* dst, cudaStream_t s);
 // one chunk: validate, run the layers, append K/V (kv_len is not advanced here)
