@@ -157,41 +157,45 @@ __global__ void pack_weights_kernel(const uint16_t* __restrict__ w, int N, int K
 
 // ---------------------------------------------------------------------------
 // GEMM: out[s][m][n] = sum over K-slice s of A[m][k] W[n][k]
-// One CTA per (256-row weight tile, 128-row activation tile, K-slice); a
-// 3-stage ring of 64-wide K chunks filled by bulk copies; one thread issues
-// M = 128, N = 256, K = 16 MMAs (hi, then lo, for each K step) into a
-// 128 x 256 fp32 TMEM accumulator; four warps read it back.
+// Persistent: one CTA per SM walks the work units (256-row weight tile,
+// 128-row activation tile, K-slice) round-robin. Warp 0 fills a 3-stage ring
+// of 64-wide K chunks by bulk copies, running ahead across units; one thread
+// of warp 1 issues M = 128, N = 256, K = 16 MMAs (hi, then lo, for each K
+// step) into one of two 128 x 256 fp32 TMEM accumulators; warps 2-5 drain
+// the other accumulator (the previous unit) meanwhile.
 // ---------------------------------------------------------------------------
 struct GemmArgs {
   const uint16_t* A;
   const uint16_t* W;
   float* out;  // [S][Mpad][Npad]
   int KC, S, Mpad, Npad;
+  int Nt, Mt;  // tiles: units = Nt Mt S, unit u = (u % Nt, u / Nt % Mt, u / (Nt Mt))
   int* err;
   unsigned long long wait_ns;
 };
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
   __shared__ int failed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = blockIdx.x, mt = blockIdx.y, s = blockIdx.z;
-  const int kc0 = (int)((long long)s * a.KC / a.S), kc1 = (int)((long long)(s + 1) * a.KC / a.S);
-  const int nk = kc1 - kc0;
+  const int units = a.Nt * a.Mt * a.S;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       bar_init(&full[i], 1);
       bar_init(&empty[i], 1);
     }
-    bar_init(&done, 1);
+    for (int i = 0; i < 2; ++i) {
+      bar_init(&acc_full[i], 1);
+      bar_init(&acc_empty[i], 4);  // one lane of each epilogue warp
+    }
     failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
-                 "n"(kTmemCols)
+                 "n"(2 * kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -199,59 +203,94 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
   __syncthreads();
   tc_after();
   const uint32_t tmem = tmem_base;
-  int issued_uses = 0;  // producer: stage uses whose copies were issued
+  int consumed = 0;   // MMA thread: ring uses whose copies it waited for
+  int issued_mma = 0; // MMA thread: units whose MMAs it issued
+  auto unit_k = [&](int u, int& kc0, int& nk) {
+    const int s = u / (a.Nt * a.Mt);
+    kc0 = (int)((long long)s * a.KC / a.S);
+    nk = (int)((long long)(s + 1) * a.KC / a.S) - kc0;
+  };
 
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < nk; ++i) {
-      const int st = i % kStages, u = i / kStages;
-      if (u > 0 && !bar_wait(&empty[st], (u - 1) & 1, a.wait_ns)) {
-        err_set(a.err, QTTS_DEV_TIMEOUT);
-        failed = 1;
-        break;
+    int it = 0;  // ring use counter across units
+    for (int u = blockIdx.x; u < units && !*(volatile int*)&failed; u += gridDim.x) {
+      const int nt = u % a.Nt, mt = (u / a.Nt) % a.Mt;
+      int kc0, nk;
+      unit_k(u, kc0, nk);
+      for (int i = 0; i < nk; ++i, ++it) {
+        const int st = it % kStages, use = it / kStages;
+        if (use > 0 && !bar_wait(&empty[st], (use - 1) & 1, a.wait_ns)) {
+          err_set(a.err, QTTS_DEV_TIMEOUT);
+          failed = 1;
+          break;
+        }
+        unsigned char* base = smem + st * kStageBytes;
+        const int kc = kc0 + i;
+        bar_expect(&full[st], kStageBytes);
+        bulk_g2s(base, a.A + (size_t)(mt * a.KC + kc) * 2 * kAImg, 2 * kAImg * 2, &full[st]);
+        bulk_g2s(base + 2 * kAImg * 2, a.W + (size_t)(nt * a.KC + kc) * kWImg, kWImg * 2, &full[st]);
       }
-      if (*(volatile int*)&failed) break;
-      unsigned char* base = smem + st * kStageBytes;
-      const int kc = kc0 + i;
-      bar_expect(&full[st], kStageBytes);
-      bulk_g2s(base, a.A + (size_t)(mt * a.KC + kc) * 2 * kAImg, 2 * kAImg * 2, &full[st]);
-      bulk_g2s(base + 2 * kAImg * 2, a.W + (size_t)(nt * a.KC + kc) * kWImg, kWImg * 2, &full[st]);
-      issued_uses = i + 1;
     }
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = umma_idesc(kBM, kBN);
-    for (int i = 0; i < nk; ++i) {
-      const int st = i % kStages, u = i / kStages;
-      if (!bar_wait(&full[st], u & 1, a.wait_ns)) {
+    int it = 0, j = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+      const int buf = j & 1;
+      const uint32_t acc = tmem + (uint32_t)(buf * kTmemCols);
+      // the epilogue has drained this accumulator (unit j - 2)
+      if (j >= 2 && !bar_wait(&acc_empty[buf], ((j >> 1) - 1) & 1, a.wait_ns)) {
         err_set(a.err, QTTS_DEV_TIMEOUT);
         failed = 1;
         break;
       }
       tc_after();
-      const uint32_t base = saddr(smem + st * kStageBytes);
+      int kc0, nk;
+      unit_k(u, kc0, nk);
+      bool ok = true;
+      for (int i = 0; i < nk; ++i, ++it) {
+        const int st = it % kStages, use = it / kStages;
+        if (!bar_wait(&full[st], use & 1, a.wait_ns)) {
+          err_set(a.err, QTTS_DEV_TIMEOUT);
+          failed = 1;
+          ok = false;
+          break;
+        }
+        tc_after();
+        const uint32_t base = saddr(smem + st * kStageBytes);
 #pragma unroll
-      for (int ks = 0; ks < kBK / 16; ++ks) {
-        const uint64_t dhi = umma_desc(base + ks * 2 * (kBM * 16), kBM * 16, 128);
-        const uint64_t dlo = umma_desc(base + kAImg * 2 + ks * 2 * (kBM * 16), kBM * 16, 128);
-        const uint64_t dw = umma_desc(base + 2 * kAImg * 2 + ks * 2 * (kBN * 16), kBN * 16, 128);
-        umma(tmem, dhi, dw, idesc, (i > 0 || ks > 0) ? 1u : 0u);
-        umma(tmem, dlo, dw, idesc, 1u);
+        for (int ks = 0; ks < kBK / 16; ++ks) {
+          const uint64_t dhi = umma_desc(base + ks * 2 * (kBM * 16), kBM * 16, 128);
+          const uint64_t dlo = umma_desc(base + kAImg * 2 + ks * 2 * (kBM * 16), kBM * 16, 128);
+          const uint64_t dw = umma_desc(base + 2 * kAImg * 2 + ks * 2 * (kBN * 16), kBN * 16, 128);
+          umma(acc, dhi, dw, idesc, (i > 0 || ks > 0) ? 1u : 0u);
+          umma(acc, dlo, dw, idesc, 1u);
+        }
+        consumed = it + 1;
+        umma_commit(&empty[st]);
       }
-      umma_commit(&empty[st]);
+      umma_commit(&acc_full[buf]);  // also after a failure: completes once the issued MMAs have
+      issued_mma = j + 1;
+      if (!ok) break;
     }
-    umma_commit(&done);  // also after a failure: completes once the issued MMAs have
   } else if (warp >= 2) {
     const int q = warp & 3;  // this warp's TMEM lane quarter
-    int okl = 0;
-    if (lane == 0) okl = bar_wait(&done, 0, a.wait_ns) ? 1 : 0;
-    const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // one verdict per warp: the loads below are warp-wide
-    __syncwarp();
-    if (!ok) {
-      err_set(a.err, QTTS_DEV_TIMEOUT);
-      failed = 1;
-    } else {
+    int j = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+      const int buf = j & 1;
+      int okl = 0;
+      if (lane == 0) okl = bar_wait(&acc_full[buf], (j >> 1) & 1, a.wait_ns) ? 1 : 0;
+      const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // one verdict per warp: the loads are warp-wide
+      __syncwarp();
+      if (!ok) {
+        err_set(a.err, QTTS_DEV_TIMEOUT);
+        failed = 1;
+        break;
+      }
       tc_after();
+      const int nt = u % a.Nt, mt = (u / a.Nt) % a.Mt, s = u / (a.Nt * a.Mt);
       const int row = mt * kBM + q * 32 + lane;
       float* o = a.out + ((size_t)s * a.Mpad + row) * a.Npad + (size_t)nt * kBN;
+      const uint32_t acc = tmem + (uint32_t)(buf * kTmemCols) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < kBN / 16; ++c) {
         uint32_t r[16];
@@ -259,29 +298,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
               "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 16)));
+            : "r"(acc + (uint32_t)(c * 16)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(o + c * 16 + 4 * j) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        for (int jj = 0; jj < 4; ++jj)
+          *reinterpret_cast<uint4*>(o + c * 16 + 4 * jj) =
+              make_uint4(r[4 * jj], r[4 * jj + 1], r[4 * jj + 2], r[4 * jj + 3]);
       }
+      tc_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&acc_empty[buf])) : "memory");
     }
   }
   tc_before();
   __syncthreads();
   if (failed) {
-    // nothing may land in shared memory or TMEM after the CTA is gone:
-    // wait (bounded) for the last issued copies and the MMAs
-    if (warp == 0 && lane == 0)
-      for (int i = (issued_uses > kStages ? issued_uses - kStages : 0); i < issued_uses; ++i)
+    // nothing may land in shared memory or TMEM after the CTA is gone: wait
+    // (bounded) for copies that may still be in flight (one use past the
+    // last consumed per stage) and for the issued MMAs
+    if (warp == 1 && lane == 0) {
+      for (int i = consumed; i < consumed + kStages; ++i)
         bar_wait(&full[i % kStages], (i / kStages) & 1, 2000000000ull);
-    if (warp == 1 && lane == 0) bar_wait(&done, 0, 2000000000ull);
+      if (issued_mma > 0) bar_wait(&acc_full[(issued_mma - 1) & 1], ((issued_mma - 1) >> 1) & 1, 2000000000ull);
+    }
     __syncthreads();
   }
   if (warp == 0) {
     __syncwarp();
     tc_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(2 * kTmemCols) : "memory");
   }
 }
 
@@ -858,8 +903,8 @@ cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, con
     const int Nt = (N + kBN - 1) / kBN, KC = (K + kBK - 1) / kBK;
     S = pf_splits(Nt * Mt, KC, c.G, c.part_floats);
     Npad = Nt * kBN;
-    GemmArgs ga{c.A, W, c.part, KC, S, Mpad, Npad, c.err, c.wait_ns};
-    gemm_kernel<<<dim3(Nt, Mt, S), kGemmThreads, kGemmSmem, s>>>(ga);
+    GemmArgs ga{c.A, W, c.part, KC, S, Mpad, Npad, Nt, Mt, c.err, c.wait_ns};
+    gemm_kernel<<<std::min(Nt * Mt * S, c.G), kGemmThreads, kGemmSmem, s>>>(ga);
   };
   auto norm = [&](const uint16_t* emb, bool add, const uint16_t* gain) {
     NormArgs na{emb, c.x, add ? c.part : nullptr, S, Mpad, Npad, gain, c.eps, c.H, KH, c.A};
