@@ -104,13 +104,16 @@ __device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_
 __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
 // ---- GEMM operand tiles ----
-// Activations: [m tile of 128 rows][64-wide K chunk][hi | lo] images; weights
+// Activations: [m tile of 128 rows][32-wide K chunk][hi | lo] images; weights
 // (packed at load): [256-row tile][K chunk] images. Inside an image of R rows:
 // element (r, k) at ((k / 8) * R / 8 + r / 8) * 64 + (r % 8) * 8 + k % 8.
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 3;
-constexpr int kAImg = kBM * kBK;                    // elements of one hi or lo image (16 KB)
-constexpr int kWImg = kBN * kBK;                    // 32 KB
-constexpr int kStageBytes = (2 * kAImg + kWImg) * 2;  // 64 KB
+constexpr int kBM = 128, kBN = 256, kBK = 32, kStages = 6;
+// 32-wide K chunks in 6 stages keep 5 x 32 KB of copies in flight per SM
+// while one stage feeds the MMAs (64-wide chunks in 3 stages: 2 x 64 KB,
+// which measured ~1.6x slower per chunk)
+constexpr int kAImg = kBM * kBK;                    // elements of one hi or lo image (8 KB)
+constexpr int kWImg = kBN * kBK;                    // 16 KB
+constexpr int kStageBytes = (2 * kAImg + kWImg) * 2;  // 32 KB
 constexpr int kGemmSmem = kStages * kStageBytes;
 constexpr int kGemmThreads = 192;                   // warp 0 copies, warp 1 issues MMAs, warps 2-5 drain TMEM
 constexpr uint32_t kTmemCols = 256;
@@ -119,10 +122,10 @@ __host__ __device__ __forceinline__ int core_off(int r, int k, int R) {
   return (k >> 3) * (R * 8) + (r >> 3) * 64 + (r & 7) * 8 + (k & 7);
 }
 __host__ __device__ __forceinline__ size_t a_off(int r, int k, int KC, int hl) {
-  return ((size_t)((r >> 7) * KC + (k >> 6)) * 2 + hl) * kAImg + core_off(r & 127, k & 63, kBM);
+  return ((size_t)((r / kBM) * KC + k / kBK) * 2 + hl) * kAImg + core_off(r % kBM, k % kBK, kBM);
 }
 __host__ __device__ __forceinline__ size_t w_off(int n, int k, int KC) {
-  return (size_t)((n >> 8) * KC + (k >> 6)) * kWImg + core_off(n & 255, k & 63, kBN);
+  return (size_t)((n / kBN) * KC + k / kBK) * kWImg + core_off(n % kBN, k % kBK, kBN);
 }
 
 // hi and lo of eight consecutive activation values (k % 8 == 0) of row r
@@ -158,8 +161,8 @@ __global__ void pack_weights_kernel(const uint16_t* __restrict__ w, int N, int K
 // ---------------------------------------------------------------------------
 // GEMM: out[s][m][n] = sum over K-slice s of A[m][k] W[n][k]
 // Persistent: one CTA per SM walks the work units (256-row weight tile,
-// 128-row activation tile, K-slice) round-robin. Warp 0 fills a 3-stage ring
-// of 64-wide K chunks by bulk copies, running ahead across units; one thread
+// 128-row activation tile, K-slice) round-robin. Warp 0 fills a 6-stage ring
+// of 32-wide K chunks by bulk copies, running ahead across units; one thread
 // of warp 1 issues M = 128, N = 256, K = 16 MMAs (hi, then lo, for each K
 // step) into one of two 128 x 256 fp32 TMEM accumulators; warps 2-5 drain
 // the other accumulator (the previous unit) meanwhile.
@@ -360,51 +363,65 @@ struct NormArgs {
   uint16_t* A;
 };
 
-// x = emb (or x + sum of partials); then A = pack(x * rms(x)^-1 * gain)
+// x = emb (or x + sum of partials); then A = pack(x * rms(x)^-1 * gain).
+// Each thread keeps its groups of 8 values in registers between the passes.
+constexpr int kNormGroups = 5;  // groups of 8 per thread: H up to 5 x 2048
+static_assert(kNormGroups * kRowThreads * 8 >= kWorkBytes / 8, "the widest accepted hidden size fits the registers");
 __global__ void __launch_bounds__(kRowThreads) norm_kernel(NormArgs a) {
   __shared__ float red[kRowThreads / 32];
   const int r = blockIdx.x;
   float* x = a.x + (size_t)r * a.H;
+  float v[kNormGroups][8];
   float ss = 0.f;
-  for (int k = threadIdx.x * 8; k < a.H; k += kRowThreads * 8) {
-    float v[8];
+#pragma unroll
+  for (int gi = 0; gi < kNormGroups; ++gi) {
+    const int k = (threadIdx.x + gi * kRowThreads) * 8;
+    if (k >= a.H) break;
     if (a.emb) {
       const uint4 e = *reinterpret_cast<const uint4*>(a.emb + (size_t)r * a.H + k);
       const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        v[2 * j] = bf2f(ew[j] & 0xFFFFu);
-        v[2 * j + 1] = bf2f(ew[j] >> 16);
+        v[gi][2 * j] = bf2f(ew[j] & 0xFFFFu);
+        v[gi][2 * j + 1] = bf2f(ew[j] >> 16);
       }
     } else {
       const float4 x0 = *reinterpret_cast<const float4*>(x + k), x1 = *reinterpret_cast<const float4*>(x + k + 4);
-      v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+      v[gi][0] = x0.x; v[gi][1] = x0.y; v[gi][2] = x0.z; v[gi][3] = x0.w;
+      v[gi][4] = x1.x; v[gi][5] = x1.y; v[gi][6] = x1.z; v[gi][7] = x1.w;
     }
     if (a.part)
       for (int s = 0; s < a.S; ++s) {
         const float* p = a.part + ((size_t)s * a.Mpad + r) * a.Npad + k;
         const float4 p0 = *reinterpret_cast<const float4*>(p), p1 = *reinterpret_cast<const float4*>(p + 4);
-        v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
-        v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+        v[gi][0] += p0.x; v[gi][1] += p0.y; v[gi][2] += p0.z; v[gi][3] += p0.w;
+        v[gi][4] += p1.x; v[gi][5] += p1.y; v[gi][6] += p1.z; v[gi][7] += p1.w;
       }
-    *reinterpret_cast<float4*>(x + k) = make_float4(v[0], v[1], v[2], v[3]);
-    *reinterpret_cast<float4*>(x + k + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    *reinterpret_cast<float4*>(x + k) = make_float4(v[gi][0], v[gi][1], v[gi][2], v[gi][3]);
+    *reinterpret_cast<float4*>(x + k + 4) = make_float4(v[gi][4], v[gi][5], v[gi][6], v[gi][7]);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+    for (int j = 0; j < 8; ++j) ss = fmaf(v[gi][j], v[gi][j], ss);
   }
   if (!a.gain) return;
   const float tot = block_sum(ss, red);
   const float rs = 1.0f / sqrtf(tot / (float)a.H + a.eps);
-  for (int k = threadIdx.x * 8; k < a.KC * kBK; k += kRowThreads * 8) {
-    float v[8];
-    if (k < a.H) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = x[k + j] * rs * bf2f(a.gain[k + j]);
-    } else {
+  for (int gi = 0; gi < kNormGroups; ++gi) {
+    const int k = (threadIdx.x + gi * kRowThreads) * 8;
+    if (k >= a.H) break;
+    const uint4 gw = *reinterpret_cast<const uint4*>(a.gain + k);
+    const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
+    float o[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.f;  // K padding
+    for (int j = 0; j < 4; ++j) {
+      o[2 * j] = v[gi][2 * j] * rs * bf2f(gg[j] & 0xFFFFu);
+      o[2 * j + 1] = v[gi][2 * j + 1] * rs * bf2f(gg[j] >> 16);
     }
-    put8(a.A, r, k, a.KC, v);
+    put8(a.A, r, k, a.KC, o);
+  }
+  for (int k = a.H + threadIdx.x * 8; k < a.KC * kBK; k += kRowThreads * 8) {  // K padding
+    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    put8(a.A, r, k, a.KC, z);
   }
 }
 
@@ -425,51 +442,64 @@ struct QkvArgs {
 };
 
 // QKV epilogue of row r: fused rows come as rotate-half pairs (dims i and
-// i + d/2 of one q or k head), then v in pairs of adjacent dims
+// i + d/2 of one q or k head), then v in pairs of adjacent dims. A thread
+// takes 8 columns (4 pairs) at a time: all in one head.
 __global__ void __launch_bounds__(kRowThreads) qkv_kernel(QkvArgs a) {
   if (err_now(a.err)) return;  // the chunk's sessions failed validation
   const int r = blockIdx.x, b = r % a.B, p = r / a.B;
   const int pos = a.sess[b].kv_len + p;
   const int half = a.d / 2;
   const int nqk = (a.nq + a.nkv) * a.d;
-  const int npair = (a.nq + 2 * a.nkv) * a.d / 2;
+  const int ncol = (a.nq + 2 * a.nkv) * a.d;
   int page = a.bt[(size_t)b * a.bt_stride + pos / kPage];
   if (page < 0 || page >= a.pool_pages) {  // checked before the chunk; stay in bounds regardless
     err_set(a.err, QTTS_DEV_BAD_PAGE);
     return;
   }
-  for (int u = threadIdx.x; u < npair; u += kRowThreads) {
-    const int n0 = 2 * u;
-    float y0 = 0.f, y1 = 0.f;
+  const size_t kvrow = (size_t)(pos % kPage) * a.d;
+  for (int n0 = threadIdx.x * 8; n0 < ncol; n0 += kRowThreads * 8) {
+    float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < a.S; ++s) {
-      const float2 t = *reinterpret_cast<const float2*>(a.part + ((size_t)s * a.Mpad + r) * a.Npad + n0);
-      y0 += t.x;
-      y1 += t.y;
+      const float* src = a.part + ((size_t)s * a.Mpad + r) * a.Npad + n0;
+      const float4 t0 = *reinterpret_cast<const float4*>(src), t1 = *reinterpret_cast<const float4*>(src + 4);
+      y[0] += t0.x; y[1] += t0.y; y[2] += t0.z; y[3] += t0.w;
+      y[4] += t1.x; y[5] += t1.y; y[6] += t1.z; y[7] += t1.w;
     }
     if (n0 < nqk) {
       const bool is_q = n0 < a.nq * a.d;
       const int rel = is_q ? n0 : n0 - a.nq * a.d;
-      const int head = rel / a.d, i = (rel % a.d) / 2;
-      const float c = a.rope_cos[(size_t)pos * half + i], sn = a.rope_sin[(size_t)pos * half + i];
-      const float o0 = y0 * c - y1 * sn;
-      const float o1 = y1 * c + y0 * sn;
+      const int head = rel / a.d, i0 = (rel % a.d) / 2;  // pairs i0 .. i0 + 3
+      const float4 c4 = *reinterpret_cast<const float4*>(a.rope_cos + (size_t)pos * half + i0);
+      const float4 s4 = *reinterpret_cast<const float4*>(a.rope_sin + (size_t)pos * half + i0);
+      const float cs[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+      float o0[4], o1[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        o0[j] = y[2 * j] * cs[j] - y[2 * j + 1] * sn[j];
+        o1[j] = y[2 * j + 1] * cs[j] + y[2 * j] * sn[j];
+      }
       if (is_q) {
         float* qr = a.q + (size_t)r * a.nq * a.d + head * a.d;
-        qr[i] = o0;
-        qr[i + half] = o1;
+        *reinterpret_cast<float4*>(qr + i0) = make_float4(o0[0], o0[1], o0[2], o0[3]);
+        *reinterpret_cast<float4*>(qr + i0 + half) = make_float4(o1[0], o1[1], o1[2], o1[3]);
       } else {
         uint16_t* kp = a.kv_pool +
-                       ((((size_t)a.layer * a.pool_pages + page) * 2 + 0) * a.nkv + head) * kPage * a.d +
-                       (size_t)(pos % kPage) * a.d;
-        kp[i] = f2bf(o0);
-        kp[i + half] = f2bf(o1);
+                       ((((size_t)a.layer * a.pool_pages + page) * 2 + 0) * a.nkv + head) * kPage * a.d + kvrow;
+        *reinterpret_cast<uint2*>(kp + i0) = make_uint2((uint32_t)f2bf(o0[0]) | ((uint32_t)f2bf(o0[1]) << 16),
+                                                        (uint32_t)f2bf(o0[2]) | ((uint32_t)f2bf(o0[3]) << 16));
+        *reinterpret_cast<uint2*>(kp + i0 + half) =
+            make_uint2((uint32_t)f2bf(o1[0]) | ((uint32_t)f2bf(o1[1]) << 16),
+                       (uint32_t)f2bf(o1[2]) | ((uint32_t)f2bf(o1[3]) << 16));
       }
     } else {
       const int rel = n0 - nqk;
       const int head = rel / a.d, e = rel % a.d;
       uint16_t* vp = a.kv_pool + ((((size_t)a.layer * a.pool_pages + page) * 2 + 1) * a.nkv + head) * kPage * a.d +
-                     (size_t)(pos % kPage) * a.d;
-      *reinterpret_cast<uint32_t*>(vp + e) = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
+                     kvrow + e;
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = (uint32_t)f2bf(y[2 * j]) | ((uint32_t)f2bf(y[2 * j + 1]) << 16);
+      *reinterpret_cast<uint4*>(vp) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
