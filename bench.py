@@ -242,7 +242,7 @@ def prefill_kv_bytes(d, kv_len0, n_tok, per_chunk):
     return n
 
 
-def run_prefill(wl, n_tok, reps, local, weights):
+def run_prefill(wl, n_tok, reps, local, weights, warmup=1):
     """Talker prefill throughput: every session of the workload takes an
     n_tok-token prompt after its prefix (kv_len rewound between repetitions,
     median of reps timed with CUDA events on the launching stream)."""
@@ -260,7 +260,9 @@ def run_prefill(wl, n_tok, reps, local, weights):
     sess0 = eng.sess.clone()
     e = to_dev_u16(sess.prompt_embeds(n_tok), eng.dev)
     stream = torch.cuda.current_stream()
-    eng.prefill(e, stream)  # warm-up
+    for _ in range(warmup):
+        eng.sess.copy_(sess0)
+        eng.prefill(e, stream)
     times = []
     for _ in range(reps):
         eng.sess.copy_(sess0)
@@ -457,9 +459,32 @@ def main():
                     help="fewest activation rows a GEMV takes on the tensor cores (library default 8; 65: off)")
     ap.add_argument("--ksplit-min-rows", type=int, default=None,
                     help="fewest activation rows for the K-split tensor-core GEMV (library default 8; below it only the deepest GEMVs split)")
+    ap.add_argument("--prefill-only", type=int, default=0, metavar="TOKENS",
+                    help="time only the Talker prefill of TOKENS prompt tokens per session of --workload "
+                         "(--warmup untimed passes, then --steps timed ones; prints one JSON line)")
     args = ap.parse_args()
     wl = configs.WORKLOADS[args.workload]
     cores = os.cpu_count()
+
+    if args.prefill_only > 0 and args.impl == "ours":
+        w = synth.make_weights(wl.dims, 1000 + wl.seed)
+        rp = run_prefill(wl, args.prefill_only, args.steps, 0, w, warmup=args.warmup)
+        peak, _ = measured_peak_gbs()
+        tc_peak, tc_kind = measured_peak_tflops()
+        t_hbm, t_tc = rp["bytes"] / (peak * 1e9), rp["flops"] / (tc_peak * 1e12)
+        tensor = t_tc > t_hbm
+        line = {"metric": "Talker prefill prompt tokens/s", "value": rp["tokens_per_s"], "unit": "tokens/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": rp["ms"],
+                "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": workload_desc(wl), "prompt_tokens": args.prefill_only,
+                           "chunks": rp["chunks"]},
+                "roofline": {"bound": "tensor" if tensor else "hbm",
+                             "achieved": rp["achieved_tflops"] if tensor else rp["achieved_gbs"],
+                             "peak": tc_peak if tensor else peak, "unit": "TFLOP/s" if tensor else "GB/s",
+                             "frac": rp["achieved_tflops"] / tc_peak if tensor else rp["achieved_gbs"] / peak,
+                             "flops": rp["flops"], "bytes": rp["bytes"], "peak_kind": tc_kind if tensor else "measured"}}
+        print(json.dumps(line))
+        return
 
     if args.impl == "reference":
         # the oracle on the host cores: rank 0 alone runs it (no process group
