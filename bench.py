@@ -300,8 +300,12 @@ def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, tra
     cap = min(2048, int(sess.kv_len0.max()) + steps + warmup + 4)
     limit = cap - int(sess.kv_len0.max()) - 2  # frames before the contexts are rewound
     pool = wl.batch * ((cap + 15) // 16) + 8
+    torch.cuda.synchronize(local)
+    free0 = torch.cuda.mem_get_info(local)[0]
     eng = Engine(d, weights, max_batch=max(wl.batch, 1), max_context=cap, pool_pages=pool, device=local, int8=wl.int8)
     eng.setup_sessions(sess, cap, shuffle=wl.shuffle_pages)
+    torch.cuda.synchronize(local)
+    model_bytes = free0 - torch.cuda.mem_get_info(local)[0]  # the library's allocations: weights, copies, pool, scratch
     if ring_slots is not None:
         qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_RING_SLOTS, ring_slots)
     if tc_min_rows is not None:
@@ -399,6 +403,7 @@ def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, tra
     h2d = sess_h.nbytes + B * eng.bt_stride * 4 + emb_h.nbytes + rng_h.nbytes + seen_h.nbytes
     d2h = codes_h.nbytes + eos_h.nbytes + sess_h.nbytes + rng_h.nbytes + seen_h.nbytes
     res["e2e"] = dict(value=B * e2e_steps / e2e_s, s=e2e_s, frames=B * e2e_steps, h2d=h2d, d2h=d2h)
+    res["model_device_bytes"] = model_bytes
     if trace:
         qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_TRACE, 1)
         eng.sess.copy_(sess0)
@@ -535,7 +540,8 @@ def main():
                     "h2d_bytes_per_step": r["e2e"]["h2d"],
                     "d2h_bytes_per_step": r["e2e"]["d2h"]},
             "gpu_launches": 2 * args.steps,
-            "clocks": r["clocks"]}
+            "clocks": r["clocks"],
+            "model_device_bytes": r["model_device_bytes"]}
     if rank == 0:
         fps, nfr, bs = oracle_sample(wl, w, args.oracle_frames)
         line["cpu_baseline"] = {"value": fps, "unit": UNIT, "cores": cores, "kind": "oracle",

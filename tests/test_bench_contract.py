@@ -67,7 +67,8 @@ def test_device_arm_line_keys_with_the_gpu_run_stubbed(orc_lib, monkeypatch, cap
 
     fake = {"total_ms": 500.0, "frame_ms": 4.9, "weight_bytes": 1, "bytes_per_frame": 2.0e9, "achieved_gbs": 400.0,
             "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 9},
-            "e2e": {"value": 190.0, "s": 0.52, "frames": 100, "h2d": 4096, "d2h": 512}}
+            "e2e": {"value": 190.0, "s": 0.52, "frames": 100, "h2d": 4096, "d2h": 512},
+            "model_device_bytes": 11 << 30}
     monkeypatch.setattr(bench, "run_gpu", lambda *a, **k: fake)
     monkeypatch.setattr(bench, "dist_setup", lambda: (1, 0, 0))
     monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "tiny", "--steps", "100", "--warmup", "3",
@@ -87,5 +88,6 @@ def test_device_arm_line_keys_with_the_gpu_run_stubbed(orc_lib, monkeypatch, cap
     assert d["e2e"]["value"] == pytest.approx(100 / 0.52)
     assert (d["e2e"]["h2d_bytes_per_step"], d["e2e"]["d2h_bytes_per_step"]) == (4096, 512)
     assert d["gpu_launches"] == 200 and d["clocks"]["sm_mhz"] == 2070.0
+    assert d["model_device_bytes"] == 11 << 30
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert d["config"]["workload"].startswith("tiny") and d["config"]["global_batch"] == 1
