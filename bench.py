@@ -289,7 +289,7 @@ def run_prefill(wl, n_tok, reps, local, weights, warmup=1):
 
 
 def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, trace_file=None, tc_min_rows=None,
-            ksplit_min_rows=None):
+            ksplit_min_rows=None, chunk_talker_min_b=None):
     import torch
 
     from codebook_decode_gb300 import qtts
@@ -312,6 +312,8 @@ def run_gpu(wl, steps, warmup, local, weights, trace=False, ring_slots=None, tra
         qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_TC_MIN_ROWS, tc_min_rows)
     if ksplit_min_rows is not None:
         qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_KSPLIT_MIN_ROWS, ksplit_min_rows)
+    if chunk_talker_min_b is not None:
+        qtts.qtts_set_option(eng.m, qtts.QTTS_OPT_CHUNK_TALKER_MIN_B, chunk_talker_min_b)
     dev = eng.dev
     stream = torch.cuda.current_stream()
     sess0 = eng.sess.clone()
@@ -464,6 +466,8 @@ def main():
                     help="fewest activation rows a GEMV takes on the tensor cores (library default 8; 65: off)")
     ap.add_argument("--ksplit-min-rows", type=int, default=None,
                     help="fewest activation rows for the K-split tensor-core GEMV (library default 8; below it only the deepest GEMVs split)")
+    ap.add_argument("--chunk-talker-min-b", type=int, default=None,
+                    help="fewest sessions whose BF16 frames run the Talker on the chunk kernels (library default 33: off)")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="TOKENS",
                     help="time only the Talker prefill of TOKENS prompt tokens per session of --workload "
                          "(--warmup untimed passes, then --steps timed ones; prints one JSON line)")
@@ -518,7 +522,7 @@ def main():
     w = synth.make_weights(wl.dims, 1000 + wl.seed)
     barrier(ws)
     r = run_gpu(wl, args.steps, args.warmup, local, w, trace=args.trace, ring_slots=args.ring_slots, tc_min_rows=args.tc_min_rows,
-                ksplit_min_rows=args.ksplit_min_rows,
+                ksplit_min_rows=args.ksplit_min_rows, chunk_talker_min_b=args.chunk_talker_min_b,
                 trace_file=args.trace_file)
     if args.trace:
         print(json.dumps(r["trace"]), file=sys.stderr)
@@ -551,7 +555,8 @@ def main():
             for name in ("full_b8", "full_b32", "int8_b1", "int8_b32"):
                 o = configs.WORKLOADS[name]
                 rr = run_gpu(o, min(args.steps, 50), 3, local, w, ring_slots=args.ring_slots,
-                             tc_min_rows=args.tc_min_rows, ksplit_min_rows=args.ksplit_min_rows)  # same weights
+                             tc_min_rows=args.tc_min_rows, ksplit_min_rows=args.ksplit_min_rows,
+                             chunk_talker_min_b=args.chunk_talker_min_b)  # same weights
                 sweep[name] = {"frames_per_s": o.batch * min(args.steps, 50) / (rr["total_ms"] / 1e3),
                                "frame_ms": rr["frame_ms"], "achieved_gbs": rr["achieved_gbs"],
                                "frac": rr["achieved_gbs"] / peak, "bytes_per_frame": rr["bytes_per_frame"]}

@@ -172,6 +172,7 @@ struct GemmArgs {
   const uint16_t* W;
   float* out;  // [S][Mpad][Npad]
   int KC, S, Mpad, Npad;
+  int M;       // rows with data: the epilogue stores no partial sums of rows past it
   int Nt, Mt;  // tiles: units = Nt Mt S, unit u = (u % Nt, u / Nt % Mt, u / (Nt Mt))
   int* err;
   unsigned long long wait_ns;
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
       tc_after();
       const int nt = u % a.Nt, mt = (u / a.Nt) % a.Mt, s = u / (a.Nt * a.Mt);
       const int row = mt * kBM + q * 32 + lane;
+      const bool store = row < a.M;
       float* o = a.out + ((size_t)s * a.Mpad + row) * a.Npad + (size_t)nt * kBN;
       const uint32_t acc = tmem + (uint32_t)(buf * kTmemCols) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
@@ -303,10 +305,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
               "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
             : "r"(acc + (uint32_t)(c * 16)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (store)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          *reinterpret_cast<uint4*>(o + c * 16 + 4 * jj) =
-              make_uint4(r[4 * jj], r[4 * jj + 1], r[4 * jj + 2], r[4 * jj + 3]);
+          for (int jj = 0; jj < 4; ++jj)
+            *reinterpret_cast<uint4*>(o + c * 16 + 4 * jj) =
+                make_uint4(r[4 * jj], r[4 * jj + 1], r[4 * jj + 2], r[4 * jj + 3]);
       }
       tc_before();
       __syncwarp();
@@ -804,6 +807,168 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// attention for one query token per session (a decode step): bound by
+// reading the cache, so on CUDA cores. One CTA per (session, kv head,
+// kAttnChunk-position chunk), 8 warps of 32 positions: a warp stages its K
+// rows in shared memory (coalesced 16-byte loads), a lane scores its
+// position for the group's q heads in fp32, the warp's base-2 softmax state
+// per head, then O += P V with V rows read coalesced and a lane owning HD/32
+// dims; the warps' states merge in shared memory in warp order into the
+// chunk's partial, the format attn_kernel writes and attn_combine_kernel
+// merges.
+// ---------------------------------------------------------------------------
+constexpr int kDecWarps = kAttnChunk / 32;
+__host__ __device__ constexpr int dec_ldk(int HD) { return HD + 8; }  // bf16 per staged K row (16-byte pad)
+__host__ __device__ constexpr int dec_smem(int HD) {
+  return kDecWarps * 32 * dec_ldk(HD) * 2 + 2 * HD * 4 + kDecWarps * 2 * (HD + 4) * 4;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kDecWarps * 32) attn_decode_kernel(AttnArgs a) {
+  constexpr int E = HD / 32;
+  constexpr int LDK = dec_ldk(HD);
+  extern __shared__ __align__(16) unsigned char dsm[];
+  uint16_t* ks = reinterpret_cast<uint16_t*>(dsm);                                       // [warps][32][LDK]
+  float* qs = reinterpret_cast<float*>(dsm + kDecWarps * 32 * LDK * 2);                 // [2][HD]
+  float* st = qs + 2 * HD;                                                              // [warps][2][HD + 4]
+  if (err_now(a.err)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
+  const int grp = a.nq / a.nkv;  // 1 or 2
+  const int chunk = blockIdx.y;
+  const int kv0 = a.sess[b].kv_len;
+  const int npos = kv0 + 1;  // positions 0 .. kv_len: the cache and the new token
+  if (chunk * kAttnChunk >= npos) return;
+  const float scale = 1.4426950408889634f / sqrtf((float)HD);
+  for (int i = threadIdx.x; i < grp * HD; i += kDecWarps * 32)
+    qs[i] = a.q[(size_t)b * a.nq * HD + (size_t)kvh * grp * HD + i];
+  // lane j resolves position p0 + j's K and V rows once (0: past the last
+  // position); the warp shares them by shuffle, so no load waits on a page id
+  const int p0 = chunk * kAttnChunk + warp * 32;
+  const int pos = p0 + lane;
+  const bool valid = pos < npos;
+  unsigned long long krow = 0, vrow = 0;
+  if (valid) {
+    const int page = a.bt[(size_t)b * a.bt_stride + pos / kPage];
+    if (page >= 0 && page < a.pool_pages) {  // checked before the step
+      const size_t base = (((size_t)a.layer * a.pool_pages + page) * 2 * a.nkv + kvh) * kPage * HD + (size_t)(pos % kPage) * HD;
+      krow = (unsigned long long)(a.kv_pool + base);
+      vrow = (unsigned long long)(a.kv_pool + base + (size_t)a.nkv * kPage * HD);
+    }
+  }
+  // this warp's K rows in shared memory: 32 positions x HD bf16, 16 bytes per lane step
+  uint16_t* kw = ks + warp * 32 * LDK;
+#pragma unroll 4
+  for (int i = lane; i < 32 * (HD / 8); i += 32) {
+    const int j = i / (HD / 8), e = (i % (HD / 8)) * 8;
+    const unsigned long long kr = __shfl_sync(0xffffffffu, krow, j);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (kr) v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(kr) + e);
+    *reinterpret_cast<uint4*>(kw + j * LDK + e) = v;
+  }
+  __syncthreads();
+  float sc[2] = {0.f, 0.f};
+#pragma unroll 4
+  for (int e = 0; e < HD; e += 8) {
+    const uint4 kv = *reinterpret_cast<const uint4*>(kw + lane * LDK + e);
+    const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+    float kf[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      kf[2 * u] = bf2f(kk[u] & 0xFFFFu);
+      kf[2 * u + 1] = bf2f(kk[u] >> 16);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (h < grp) {
+        const float4 q0 = *reinterpret_cast<const float4*>(qs + h * HD + e);
+        const float4 q1 = *reinterpret_cast<const float4*>(qs + h * HD + e + 4);
+        sc[h] = fmaf(q0.x, kf[0], sc[h]);
+        sc[h] = fmaf(q0.y, kf[1], sc[h]);
+        sc[h] = fmaf(q0.z, kf[2], sc[h]);
+        sc[h] = fmaf(q0.w, kf[3], sc[h]);
+        sc[h] = fmaf(q1.x, kf[4], sc[h]);
+        sc[h] = fmaf(q1.y, kf[5], sc[h]);
+        sc[h] = fmaf(q1.z, kf[6], sc[h]);
+        sc[h] = fmaf(q1.w, kf[7], sc[h]);
+      }
+  }
+  float m[2], l[2], p[2], o[2][E];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float v = valid && h < grp ? sc[h] * scale : -INFINITY;
+    float mx = v;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    m[h] = mx;
+    p[h] = v == -INFINITY ? 0.f : exp2f(v - mx);
+    float sum = p[h];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    l[h] = sum;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[h][e] = 0.f;
+  }
+  // O += P V: V row j read by the whole warp (lane: dims lane E .. lane E + E - 1)
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) {
+    const unsigned long long vr = __shfl_sync(0xffffffffu, vrow, j);
+    float vf[E];
+    if (vr) {
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(vr) + lane * E;
+      if constexpr (E == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(src);
+        vf[0] = bf2f(w.x & 0xFFFFu); vf[1] = bf2f(w.x >> 16); vf[2] = bf2f(w.y & 0xFFFFu); vf[3] = bf2f(w.y >> 16);
+      } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+        vf[0] = bf2f(w & 0xFFFFu); vf[1] = bf2f(w >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) vf[e] = 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float pb = __shfl_sync(0xffffffffu, p[h], j);
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[h][e] = fmaf(pb, vf[e], o[h][e]);
+    }
+  }
+  // the warps' states, then the chunk's partial per q head (warp order)
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (h >= grp) break;
+    float* sw = st + (warp * 2 + h) * (HD + 4);
+#pragma unroll
+    for (int e = 0; e < E; ++e) sw[lane * E + e] = o[h][e];
+    if (lane == 0) {
+      sw[HD] = m[h];
+      sw[HD + 1] = l[h];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < grp * HD; i += kDecWarps * 32) {
+    const int h = i / HD, e = i % HD;
+    float mm = -INFINITY;
+    for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, st[(w * 2 + h) * (HD + 4) + HD]);
+    float acc = 0.f, ll = 0.f;
+    for (int w = 0; w < kDecWarps; ++w) {
+      const float* sw = st + (w * 2 + h) * (HD + 4);
+      if (sw[HD] == -INFINITY) continue;  // no position of this warp
+      const float wt = exp2f(sw[HD] - mm);
+      acc = fmaf(wt, sw[e], acc);
+      ll = fmaf(wt, sw[HD + 1], ll);
+    }
+    float* dst = a.po + ((size_t)(b * a.nq + kvh * grp + h) * a.maxc + chunk) * (HD + 4);
+    dst[e] = acc;
+    if (e == 0) {
+      dst[HD] = mm;
+      dst[HD + 1] = ll;
+    }
+  }
+}
+
 struct CombineArgs {
   const float* po;
   int maxc, B, nq, d, KC;
@@ -839,6 +1004,15 @@ __global__ void __launch_bounds__(kRowThreads) attn_combine_kernel(CombineArgs a
     for (int j = 0; j < 8; ++j) v[j] *= inv;
     put8(a.A, r, head * a.d + e, a.KC, v);
   }
+}
+
+// ---------------------------------------------------------------------------
+// decode: the Talker's last residual rows as the frame kernel's tagged words
+// (fp32 value in the low half, `tag` in the high half)
+// ---------------------------------------------------------------------------
+__global__ void publish_kernel(const float* __restrict__ x, int n, uint64_t* __restrict__ dst, uint32_t tag) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    dst[i] = ((uint64_t)tag << 32) | __float_as_uint(x[i]);
 }
 
 // ---------------------------------------------------------------------------
@@ -892,6 +1066,10 @@ cudaError_t pf_setup() {
     e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem(128));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem(64));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, dec_smem(128));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, dec_smem(64));
   return e;
 }
 
@@ -910,7 +1088,7 @@ static int pf_splits(int tiles, int KC, int G, size_t cap) {
   const size_t tile_floats = (size_t)kBM * kBN;
   int best = 1;
   long long best_cost = (long long)((tiles + G - 1) / G) * KC;
-  for (int S = 2; S <= 8 && S <= KC; ++S) {
+  for (int S = 2; S <= 16 && S <= KC; ++S) {
     if ((size_t)S * tiles * tile_floats > cap) break;
     const long long cost = (long long)((tiles * S + G - 1) / G) * ((KC + S - 1) / S);
     if (cost < best_cost) {
@@ -921,8 +1099,11 @@ static int pf_splits(int tiles, int KC, int G, size_t cap) {
   return best;
 }
 
-cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, const int32_t* bt, int bt_stride,
-                     const uint16_t* embeds, cudaStream_t s) {
+// The Talker layers over B x P rows. decode: the whole last layer too, its
+// output rows (the residual stream) left in c.x; else the last layer stops
+// after its K/V.
+static cudaError_t pf_layers(const PfCtx& c, int B, int P, const qtts_session* sess, const int32_t* bt,
+                             int bt_stride, const uint16_t* embeds, bool decode, cudaStream_t s) {
   const int M = B * P;
   if (M < 1 || M > c.max_rows) return cudaErrorInvalidValue;
   const int Mt = (M + kBM - 1) / kBM, Mpad = Mt * kBM;
@@ -933,7 +1114,7 @@ cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, con
     const int Nt = (N + kBN - 1) / kBN, KC = (K + kBK - 1) / kBK;
     S = pf_splits(Nt * Mt, KC, c.G, c.part_floats);
     Npad = Nt * kBN;
-    GemmArgs ga{c.A, W, c.part, KC, S, Mpad, Npad, Nt, Mt, c.err, c.wait_ns};
+    GemmArgs ga{c.A, W, c.part, KC, S, Mpad, Npad, M, Nt, Mt, c.err, c.wait_ns};
     gemm_kernel<<<std::min(Nt * Mt * S, c.G), kGemmThreads, kGemmSmem, s>>>(ga);
   };
   auto norm = [&](const uint16_t* emb, bool add, const uint16_t* gain) {
@@ -950,13 +1131,21 @@ cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, con
     QkvArgs qa{c.part, S, Mpad, Npad, B, sess, bt, bt_stride, l, c.nq, c.nkv, c.d, c.kv_pool, c.pool_pages,
                c.rope_cos, c.rope_sin, c.q, c.err};
     qkv_kernel<<<M, kRowThreads, 0, s>>>(qa);
-    if (l == c.n_layers - 1) break;  // the last layer's K/V are all a prompt pass leaves
+    const bool last = l == c.n_layers - 1;
+    if (last && !decode) break;  // the last layer's K/V are all a prompt pass leaves
     AttnArgs aa{c.q, B, P, sess, bt, bt_stride, l, c.nq, c.nkv, c.kv_pool, c.pool_pages, c.po, maxc, c.err};
     const dim3 ag(B * c.nkv, (P + tpc - 1) / tpc, maxc);
-    if (c.d == 128)
+    if (P == 1) {  // one query token per session: the cache-read-bound kernel
+      const dim3 dg(B * c.nkv, maxc);
+      if (c.d == 128)
+        attn_decode_kernel<128><<<dg, kDecWarps * 32, dec_smem(128), s>>>(aa);
+      else
+        attn_decode_kernel<64><<<dg, kDecWarps * 32, dec_smem(64), s>>>(aa);
+    } else if (c.d == 128) {
       attn_kernel<128><<<ag, kAttnThreads, attn_smem(128), s>>>(aa);
-    else
+    } else {
       attn_kernel<64><<<ag, kAttnThreads, attn_smem(64), s>>>(aa);
+    }
     CombineArgs ca{c.po, maxc, B, c.nq, c.d, KA, sess, c.A, c.err};
     attn_combine_kernel<<<M, kRowThreads, 0, s>>>(ca);
     gemm(L.o, c.H, c.nq * c.d);
@@ -965,8 +1154,22 @@ cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, con
     SwigluArgs sa{c.part, S, Mpad, Npad, c.F, KF, c.A};
     swiglu_kernel<<<M, kRowThreads, 0, s>>>(sa);
     gemm(L.down, c.H, c.F);
-    norm(nullptr, true, c.layers[l + 1].in_norm);
+    norm(nullptr, true, last ? nullptr : c.layers[l + 1].in_norm);  // last: the residual add alone
   }
+  return cudaGetLastError();
+}
+
+cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, const int32_t* bt, int bt_stride,
+                     const uint16_t* embeds, cudaStream_t s) {
+  return pf_layers(c, B, P, sess, bt, bt_stride, embeds, false, s);
+}
+
+cudaError_t pf_talker_step(const PfCtx& c, int B, const qtts_session* sess, const int32_t* bt, int bt_stride,
+                           const uint16_t* in_embeds, uint64_t* x_words, uint32_t tag, cudaStream_t s) {
+  cudaError_t e = pf_layers(c, B, 1, sess, bt, bt_stride, in_embeds, true, s);
+  if (e != cudaSuccess) return e;
+  const int n = B * c.H;
+  publish_kernel<<<(n + 255) / 256, 256, 0, s>>>(c.x, n, x_words, tag);
   return cudaGetLastError();
 }
 

@@ -84,6 +84,7 @@ struct qtts_model {
   float* T_bf[kCodebooks] = {};
   float* T_i8[kCodebooks] = {};
   bool loaded = false, quantized = false, use_int8 = false, stepwise = false;
+  int chunk_talker_min_b = kMaxBatch + 1;  // BF16 frames of this many sessions or more run the Talker on the chunk kernels (off)
 
   uint16_t* kv_pool = nullptr;
   std::vector<int32_t> free_ids;
@@ -600,7 +601,25 @@ int frame_part(qtts_model* m, int part, int B, qtts_session* sess, const int32_t
   }
   const int s0 = part == PART_CP ? m->s_cp : 0;
   const int s1 = part == PART_TALKER ? m->s_cp : m->n_stages;
-  const cudaError_t e = launch_frame(m->prog_dev[i8 ? 1 : 0], s0, s1, m->g, fa, m->stepwise, s);
+  const StageDesc* prog = m->prog_dev[i8 ? 1 : 0];
+  cudaError_t e;
+  if (part != PART_CP && !i8 && B >= m->chunk_talker_min_b) {
+    // the Talker on the tensor-core chunk kernels: the begin stage validates
+    // the sessions, the chunk kernels run the layers and publish the last
+    // layer's rows as the words the codebook-0 head stage reads (tag of the
+    // last Talker stage), then the frame kernel runs from that head stage on
+    const int L = m->cfg.n_layers, s_head = 1 + 5 * L;
+    e = launch_frame(prog, 0, 1, m->g, fa, m->stepwise, s);
+    if (e == cudaSuccess) {
+      PfCtx ctx = m->pf;
+      ctx.wait_ns = m->g.wait_ns;
+      e = pf_talker_step(ctx, B, sess, bt, bt_stride, in_embeds, m->acts.xout[(L - 1) & 1], fa.tag0 + (uint32_t)(s_head - 1),
+                         s);
+    }
+    if (e == cudaSuccess) e = launch_frame(prog, s_head, s1, m->g, fa, m->stepwise, s);
+  } else {
+    e = launch_frame(prog, s0, s1, m->g, fa, m->stepwise, s);
+  }
   m->last_stream = s;
   if (e != cudaSuccess) return cuda_fail(m, e, "frame launch");
   m->cp_pending = part == PART_TALKER;
@@ -1280,6 +1299,12 @@ int qtts_set_option(qtts_model* m, int option, int value) {
   if (option == QTTS_OPT_KSPLIT_MIN_ROWS) {
     if (value < 1 || value > 65) return fail(m, QTTS_E_INVALID, "K-split row threshold must be 1..65");
     m->g.ksplit_min_rows = value;
+    return QTTS_OK;
+  }
+  if (option == QTTS_OPT_CHUNK_TALKER_MIN_B) {
+    if (value < 1 || value > kMaxBatch + 1)
+      return fail(m, QTTS_E_INVALID, "chunk-kernel Talker threshold must be 1..%d", kMaxBatch + 1);
+    m->chunk_talker_min_b = value;
     return QTTS_OK;
   }
   if (option == QTTS_OPT_WAIT_LIMIT_US) {

@@ -255,6 +255,12 @@ cudaError_t pf_pack_weights(const uint16_t* w, int N, int K, uint16_t* dst, cuda
 // one chunk: validate, run the layers, append K/V (kv_len is not advanced here)
 cudaError_t pf_chunk(const PfCtx& c, int B, int P, const qtts_session* sess, const int32_t* bt, int bt_stride,
                      const uint16_t* embeds, cudaStream_t s);
+// a decode frame's Talker half on the same kernels (one row per session, the
+// new token at kv_len, the whole last layer): its K/V appended, its output
+// rows written as tagged words with `tag` to x_words [B][H] (the frame
+// kernel's codebook-0 head stage reads them); kv_len is not advanced here
+cudaError_t pf_talker_step(const PfCtx& c, int B, const qtts_session* sess, const int32_t* bt, int bt_stride,
+                           const uint16_t* in_embeds, uint64_t* x_words, uint32_t tag, cudaStream_t s);
 
 // qtts_api.cu: model internals for other translation units
 struct KvLayout {

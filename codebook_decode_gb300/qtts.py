@@ -31,6 +31,7 @@ QTTS_OPT_RING_SLOTS = 4
 QTTS_OPT_TC_MIN_ROWS = 5
 QTTS_OPT_KSPLIT_MIN_ROWS = 6
 QTTS_OPT_WAIT_LIMIT_US = 7
+QTTS_OPT_CHUNK_TALKER_MIN_B = 8
 
 
 class QttsError(RuntimeError):

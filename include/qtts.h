@@ -319,7 +319,8 @@ int qtts_feedback_embed(qtts_model* m, int B, const int32_t* codes, const uint16
 int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, const qtts_session* sessions,
                 const qtts_rng* rng, const uint32_t* seen, int32_t* codes_out, void* stream);
 
-/* Execution options (same results whatever their values):
+/* Execution options (the same frame within the parity tolerance whatever their
+ * values; STEPWISE and TRACE bit for bit):
  *   QTTS_OPT_STEPWISE  1: one launch per stage instead of one persistent
  *                      launch per frame (debugging aid). Default 0.
  *   QTTS_OPT_TRACE     1: record %globaltimer stamps inside every stage on
@@ -346,13 +347,25 @@ int qtts_sample(qtts_model* m, int B, int codebook, const float* logits, int V, 
  *                      work partly done: re-run it from the caller's copy of
  *                      the state). Default 2000000 (2 s). A short limit is a
  *                      test of the time-out path, which otherwise a working
- *                      GPU never takes. */
+ *                      GPU never takes.
+ *   QTTS_OPT_CHUNK_TALKER_MIN_B 1..33: a BF16 frame (or Talker half) of at
+ *                      least this many sessions runs the Talker layers on
+ *                      the prefill's tensor-core chunk kernels, one row per
+ *                      session (whole-matrix GEMMs over all sessions, then
+ *                      RoPE/KV append and attention kernels), and the frame
+ *                      kernel from the codebook-0 head on; INT8 frames and
+ *                      smaller batches keep the Talker in the frame kernel.
+ *                      The prompt pass and such frames share the chunk
+ *                      kernels' scratch: run them on one stream. 33 turns
+ *                      it off. Default 33 (off: at B = 8 and 32 it runs no
+ *                      faster than the frame kernel's Talker). */
 #define QTTS_OPT_STEPWISE 1
 #define QTTS_OPT_TRACE 3
 #define QTTS_OPT_RING_SLOTS 4
 #define QTTS_OPT_TC_MIN_ROWS 5
 #define QTTS_OPT_KSPLIT_MIN_ROWS 6
 #define QTTS_OPT_WAIT_LIMIT_US 7
+#define QTTS_OPT_CHUNK_TALKER_MIN_B 8
 int qtts_set_option(qtts_model* m, int option, int value);
 
 /* Stage timestamps of the last frame run with QTTS_OPT_TRACE on: 8 values

@@ -21,7 +21,7 @@ def rel_diff(a, b):
 
 class ParityRun:
     def __init__(self, dims, weights, sess, frames, shuffle=True, int8=False, max_batch=None, stepwise=False,
-                 oracle=None, engine=None, tc_min_rows=None, ksplit_min_rows=None):
+                 oracle=None, engine=None, tc_min_rows=None, ksplit_min_rows=None, chunk_talker_min_b=None):
         self.d = dims
         self.sess = sess
         self.frames = frames
@@ -38,6 +38,8 @@ class ParityRun:
             assert qtts.qtts_set_option(self.eng.m, qtts.QTTS_OPT_TC_MIN_ROWS, tc_min_rows) == 0
         if ksplit_min_rows is not None:
             assert qtts.qtts_set_option(self.eng.m, qtts.QTTS_OPT_KSPLIT_MIN_ROWS, ksplit_min_rows) == 0
+        if chunk_talker_min_b is not None:
+            assert qtts.qtts_set_option(self.eng.m, qtts.QTTS_OPT_CHUNK_TALKER_MIN_B, chunk_talker_min_b) == 0
         self.eng.setup_sessions(sess, self.cap, shuffle=shuffle)
         self.O = oracle or orc.Oracle(dims, weights, use_int8=int8)
         self.rows = sess.session_array().copy()

@@ -61,11 +61,13 @@ def test_full_b8_bf16(full_w, oracle_bf16):
         free(run)
 
 
-def test_full_b32_bf16_ragged_staggered(full_w, oracle_bf16):
+@pytest.mark.parametrize("chunk_talker", [8, 33])
+def test_full_b32_bf16_ragged_staggered(full_w, oracle_bf16, chunk_talker):
     """B=32, prefixes uniform in [100, 1000] plus staggered offsets 0..200
-    (history pre-filled, frame counters at the offset)."""
+    (history pre-filled, frame counters at the offset); the Talker on the
+    chunk kernels (option at 8) and in the frame kernel (33, the default)."""
     s = synth.make_sessions(configs.WORKLOADS["full_b32"], frames=1)
-    run = ParityRun(FULL, full_w, s, 1, oracle=oracle_bf16).run()
+    run = ParityRun(FULL, full_w, s, 1, oracle=oracle_bf16, chunk_talker_min_b=chunk_talker).run()
     try:
         check(run, TOL_BF16)
     finally:

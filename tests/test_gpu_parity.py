@@ -82,16 +82,39 @@ def test_tiny_max_batch_long_context(tiny_w):
                                                   (9, 8, 65, False), (9, 8, 8, False), (9, 8, 65, True),
                                                   (9, 8, 8, True), (2, 1, 1, True)])
 def test_gemv_path_choice(tiny_w, B, tc_min, ks_min, int8):
-    """Every GEMV path matches the oracle, BF16 and INT8 weights: tensor
-    cores from one activation row up (tc_min 1) with one K-slice (ks_min 65)
-    or K split across CTAs (ks_min <= rows), and the CUDA-core paths alone
-    (tc_min 65)."""
+    """Every GEMV path of the frame kernel matches the oracle, BF16 and INT8
+    weights: tensor cores from one activation row up (tc_min 1) with one
+    K-slice (ks_min 65) or K split across CTAs (ks_min <= rows), and the
+    CUDA-core paths alone (tc_min 65); the Talker stays in the frame kernel
+    at every batch size here."""
     s = tiny_sessions(B, [7, 33, 16, 2, 40, 1, 15, 64, 30][:B], [0, 2, 5, 1, 3, 0, 4, 6, 2][:B], T=0.9, k=50, r=1.05)
-    run = ParityRun(TINY, tiny_w, s, 3, shuffle=True, int8=int8, tc_min_rows=tc_min, ksplit_min_rows=ks_min).run()
+    run = ParityRun(TINY, tiny_w, s, 3, shuffle=True, int8=int8, tc_min_rows=tc_min, ksplit_min_rows=ks_min,
+                    chunk_talker_min_b=33).run()
     try:
         assert run.max_rel() < (TOL_INT8 if int8 else TOL_BF16), run.max_rel()
         assert run.confident_agree == run.confident
         run.check_state()
+    finally:
+        free(run)
+
+
+@pytest.mark.parametrize("B,free_run,split", [(8, False, False), (9, True, False), (12, False, True), (3, False, False)])
+def test_chunk_kernel_talker_matches_oracle(tiny_w, B, free_run, split):
+    """Frames whose Talker runs on the tensor-core chunk kernels (the option
+    at 1 for B = 3, at 8 otherwise) and the rest in the frame kernel: logits,
+    codes and EOS flags, K/V and state against the oracle, teacher-forced,
+    free-running, and as split Talker/CP halves."""
+    pre = [7, 33, 16, 2, 40, 1, 15, 64, 30, 5, 21, 48]
+    off = [0, 2, 5, 1, 3, 0, 4, 6, 2, 1, 0, 3]
+    s = tiny_sessions(B, pre[:B], off[:B], T=0.9, k=50, r=1.05)
+    run = ParityRun(TINY, tiny_w, s, 3, shuffle=True, chunk_talker_min_b=1 if B < 8 else 8)
+    try:
+        run.run(free=free_run, split=split)
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+        assert run.confident_agree == run.confident
+        assert run.codes_checked == 3 * B * 16
+        run.check_state()
+        run.check_kv()
     finally:
         free(run)
 
