@@ -480,14 +480,16 @@ __device__ float log_series_f32(float x) {
 
 // Gumbel noise -ln(-ln u) for vocabulary id v of codebook j, u from word v&3
 // of Philox(key, (v>>2, j, frame_ctr, 0)): u = (top 23 bits + 1/2) 2^-23.
-__device__ __forceinline__ float gumbel(uint32_t key0, uint32_t key1, int j, uint32_t fctr, int v) {
-  uint32_t c[4] = {(uint32_t)v >> 2, (uint32_t)j, fctr, 0u};
-  philox4x32_10(c, key0, key1);
-  const uint32_t w = c[v & 3];
+__device__ __forceinline__ float gumbel_of_word(uint32_t w) {
   const float u = __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
   const float l1 = log_series_f32(u);
   const float l2 = log_series_f32(-l1);
   return -l2;
+}
+__device__ __forceinline__ float gumbel(uint32_t key0, uint32_t key1, int j, uint32_t fctr, int v) {
+  uint32_t c[4] = {(uint32_t)v >> 2, (uint32_t)j, fctr, 0u};
+  philox4x32_10(c, key0, key1);
+  return gumbel_of_word(c[v & 3]);
 }
 
 // order-preserving map of a binary32 value to uint32 (-0 and +0 map together)
@@ -571,6 +573,7 @@ __device__ int block_excl_scan(int v, int* wsum) {
 struct SampleSmem {
   float lp[kMaxVocab];
   uint32_t key[kMaxVocab];
+  float gn[kMaxVocab];  // Gumbel noise of this thread's ids, when computed ahead (gumbel_ahead)
   int hist[256];
   int wsum[kWarps];
   float redv[kWarps + 1];
@@ -578,12 +581,33 @@ struct SampleSmem {
   int redh[kWarps + 1];
   uint32_t sel_prefix;
   int sel_rem;
+  int sel_whole;
 };
 
-// `row`: the raw logits, or nullptr when they are already in S.lp
+static_assert(sizeof(SampleSmem) <= kWorkBytes, "the sampler's shared memory fits the work region");
+
+// The noise of this thread's contiguous block of ids (the block sample_row
+// gives it) into S.gn, one Philox call per 4 ids; it needs no logits, so the
+// sampler stage runs it while the head stage's logits are still arriving.
+__device__ void gumbel_ahead(SampleSmem& S, int V, int j, uint32_t key0, uint32_t key1, uint32_t fctr) {
+  const int per = (V + kCThreads - 1) / kCThreads;
+  const int v0 = min(V, (int)threadIdx.x * per), v1 = min(V, v0 + per);
+  for (int q = v0 >> 2; q <= (v1 - 1) >> 2 && v0 < v1; ++q) {
+    uint32_t c[4] = {(uint32_t)q, (uint32_t)j, fctr, 0u};
+    philox4x32_10(c, key0, key1);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int v = q * 4 + w;
+      if (v >= v0 && v < v1) S.gn[v] = gumbel_of_word(c[w]);
+    }
+  }
+}
+
+// `row`: the raw logits, or nullptr when they are already in S.lp.
+// noise_ahead: S.gn holds this thread's noise (gumbel_ahead ran).
 __device__ int sample_row(SampleSmem& S, const float* row, int V, int j, const qtts_session& ss,
                           uint32_t key0, uint32_t key1, uint32_t fctr, const uint32_t* seen, int eos_id,
-                          int n_codes) {
+                          int n_codes, bool noise_ahead = false) {
   const int tid = threadIdx.x, lane = tid & 31;
   float T;
   int k;
@@ -635,10 +659,15 @@ __device__ int sample_row(SampleSmem& S, const float* row, int V, int j, const q
   const bool take_all = (k == V);
   uint32_t thr = 0u;
   int rem = 0;
+  // whole_bin: the selection ended on a digit bin holding exactly the keys
+  // still needed, so every key with the prefix thr in the bits of pmask is
+  // kept (no ties to rank)
+  bool whole_bin = false;
+  uint32_t pmask = 0u;
   if (!take_all) {
     // MSB-first radix select of the k-th largest key, 8 bits per pass; a warp
     // adds equal digits together so hot bins see one atomic per warp
-    uint32_t prefix = 0u, pmask = 0u;
+    uint32_t prefix = 0u;
     rem = k;
     for (int shift = 24; shift >= 0; shift -= 8) {
       if (tid < 256) S.hist[tid] = 0;
@@ -681,28 +710,37 @@ __device__ int sample_row(SampleSmem& S, const float* row, int V, int j, const q
           }
           S.sel_prefix = prefix | ((uint32_t)dsel << shift);
           S.sel_rem = rem - cum;
+          S.sel_whole = S.hist[dsel] == rem - cum;
         }
       }
       cbar();
       prefix = S.sel_prefix;
       rem = S.sel_rem;
       pmask |= 255u << shift;
+      if (S.sel_whole) {
+        whole_bin = true;
+        break;
+      }
     }
-    thr = prefix;  // k-th largest key; `rem` ties with it are kept, lowest ids first
+    thr = prefix;  // k-th largest key (or, whole_bin, its prefix); `rem` ties with it are kept, lowest ids first
   }
 
   // exclusive scan of per-thread tie counts gives each tie its rank by id
-  int ties = 0;
-  if (!take_all)
+  int rank = 0;
+  if (!take_all && !whole_bin) {
+    int ties = 0;
     for (int v = v0; v < v1; ++v) ties += (S.key[v] == thr);
-  int rank = block_excl_scan(ties, S.wsum);
+    rank = block_excl_scan(ties, S.wsum);
+  }
 
   bool have = false;
   float bv = 0.f;
   int bi = 0;
   for (int v = v0; v < v1; ++v) {
     bool cand = take_all;
-    if (!take_all) {
+    if (whole_bin) {
+      cand = (S.key[v] & pmask) >= thr;
+    } else if (!take_all) {
       const uint32_t kk = S.key[v];
       if (kk > thr) {
         cand = true;
@@ -712,7 +750,7 @@ __device__ int sample_row(SampleSmem& S, const float* row, int V, int j, const q
       }
     }
     if (cand) {
-      const float val = __fadd_rn(S.lp[v], gumbel(key0, key1, j, fctr, v));
+      const float val = __fadd_rn(S.lp[v], noise_ahead ? S.gn[v] : gumbel(key0, key1, j, fctr, v));
       if (better(true, val, v, have, bv, bi)) {
         have = true;
         bv = val;
@@ -2551,6 +2589,11 @@ __device__ __noinline__ bool stage_sample(const StageDesc& d, uint32_t tag, cons
   SampleSmem& S = *reinterpret_cast<SampleSmem*>(smem);
   const int j = d.codebook;
   const int V = d.V;
+  const qtts_session ss = fa.sess[b];
+  const qtts_rng rs = fa.rng[b];
+  // the noise does not depend on the logits: compute it while they arrive
+  const bool greedy = (j == 0 ? ss.temperature : ss.cp_temperature) == 0.0f || (j == 0 ? ss.top_k : ss.cp_top_k) == 1;
+  if (!greedy) gumbel_ahead(S, V, j, rs.key0, rs.key1, rs.frame_ctr);
   // the session's logits, tagged by the head stage
   {
     constexpr int NB = (kMaxVocab / 2 + kCThreads - 1) / kCThreads;
@@ -2580,10 +2623,9 @@ __device__ __noinline__ bool stage_sample(const StageDesc& d, uint32_t tag, cons
     }
     if (cbar_or(!ok)) return false;
   }
-  const qtts_session ss = fa.sess[b];
-  const qtts_rng rs = fa.rng[b];
   const uint32_t* seen = (j == 0 && fa.seen) ? fa.seen + (size_t)b * g.seen_words : nullptr;
-  const int code = sample_row(S, nullptr, V, j, ss, rs.key0, rs.key1, rs.frame_ctr, seen, g.eos_id, g.n_codes);
+  const int code = sample_row(S, nullptr, V, j, ss, rs.key0, rs.key1, rs.frame_ctr, seen, g.eos_id, g.n_codes,
+                              !greedy);
   const int committed = fa.forced ? fa.forced[(size_t)b * kCodebooks + j] : code;
   if (tid == 0) {
     fa.codes_out[(size_t)b * kCodebooks + j] = code;
