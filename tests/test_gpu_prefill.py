@@ -135,3 +135,64 @@ def test_full_width_prefill_several_tiles():
         assert run.max_rel() < TOL_BF16, run.max_rel()
     finally:
         free(run)
+
+
+@pytest.mark.parametrize("B,n_tok", [(3, 1), (32, 32), (32, 33), (2, 0)])
+def test_prefill_edge_sizes(tiny_w, B, n_tok):
+    """One prompt token (the one-row attention kernel), the largest chunk
+    (32 sessions x 32 tokens = 1024 rows), one row past it (a second chunk of
+    32 rows), and an empty prompt (nothing changes)."""
+    prefixes = [(7 * b + 3) % 50 for b in range(B)]
+    s = sessions(TINY, B, prefixes * 1, max(n_tok, 1) + 3)
+    run = ParityRun(TINY, tiny_w, s, max(n_tok, 1) + 2, shuffle=True, max_batch=B)
+    try:
+        e = s.prompt_embeds(n_tok) if n_tok else np.zeros((0, B, TINY.hidden), dtype=np.uint16)
+        sess0 = run.eng.sess.clone()
+        run.eng.prefill(to_dev_u16(e, run.eng.dev))
+        assert run.eng.status() == (0, 0)
+        if n_tok == 0:
+            assert torch.equal(run.eng.sess, sess0)
+        run.O.talker_prefill(run.rows, run.kv, run.cap, e)
+        run.check_state()
+        if n_tok:
+            run.check_kv()
+        run.run(frames=1)
+        assert run.max_rel() < TOL_BF16, run.max_rel()
+        run.check_kv()
+    finally:
+        free(run)
+
+
+def test_prefill_device_errors_leave_state(tiny_w):
+    """A block-table entry outside the pool, or a prompt past max_context:
+    the device error word says which, kv_len and every cached K/V stay as
+    they were, and a valid prompt after it matches the oracle."""
+    s = sessions(TINY, 2, [20, 9], 12)
+    run = ParityRun(TINY, tiny_w, s, 10, shuffle=True)
+    try:
+        eng = run.eng
+        e = s.prompt_embeds(6)
+        e_d = to_dev_u16(e, eng.dev)
+        sess0 = eng.sess.clone()
+        kv0 = [[eng.read_kv(b, l, run.cap) for l in range(TINY.n_layers)] for b in range(2)]
+        bt_bad = eng.bt.clone()
+        bt_bad[0, 1] = 10 ** 6  # positions 16-31: session 0's prompt (20..25) writes there
+        qtts.qtts_talker_prefill(eng.m, 2, eng.sess, bt_bad, eng.bt_stride, e_d, 6, None)
+        assert eng.status() == (qtts.QTTS_E_DEVICE, qtts.QTTS_DEV_BAD_PAGE)
+        assert torch.equal(eng.sess, sess0)
+        too_long = eng.sess.clone()
+        too_long[0, 0] = run.cap - 3  # kv_len + 6 > max_context
+        qtts.qtts_talker_prefill(eng.m, 2, too_long, eng.bt, eng.bt_stride, e_d, 6, None)
+        assert eng.status() == (qtts.QTTS_E_DEVICE, qtts.QTTS_DEV_BAD_SESSION)
+        assert int(too_long[0, 0]) == run.cap - 3
+        for b in range(2):
+            for l in range(TINY.n_layers):
+                k, v = eng.read_kv(b, l, run.cap)
+                assert np.array_equal(k, kv0[b][l][0]) and np.array_equal(v, kv0[b][l][1]), (b, l)
+        eng.prefill(e_d)
+        assert eng.status() == (0, 0)
+        run.O.talker_prefill(run.rows, run.kv, run.cap, e)
+        run.check_state()
+        run.check_kv()
+    finally:
+        free(run)
