@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_kernel(SwigluArgs a) {
 // scratch area that a second kernel combines in chunk order. Q and P enter
 // as bf16 hi + lo pairs (two MMAs each), K and V are the cache's bf16 values.
 // ---------------------------------------------------------------------------
-constexpr int kAttnWarps = 2;
+constexpr int kAttnWarps = 4;
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kAttnKT = 64;      // positions per K/V tile
 constexpr int kAttnChunk = 256;  // positions per CTA (4 tiles)
