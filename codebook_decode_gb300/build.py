@@ -26,7 +26,8 @@ def _flags():
 def _stale(obj, src):
     if not os.path.exists(obj):
         return True
-    deps = [src, os.path.join(CSRC, "qtts_internal.h"), os.path.join(ROOT, "include", "qtts.h")]
+    deps = [src, os.path.join(CSRC, "qtts_internal.h"), os.path.join(CSRC, "device_util.cuh"),
+            os.path.join(ROOT, "include", "qtts.h")]
     return any(os.path.getmtime(d) > os.path.getmtime(obj) for d in deps)
 
 

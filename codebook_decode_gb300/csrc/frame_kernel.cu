@@ -22,6 +22,7 @@
 #include <math.h>
 
 #include "qtts_internal.h"
+#include "device_util.cuh"
 
 namespace qtts {
 
@@ -33,10 +34,8 @@ constexpr int kProducerWarp = kCWarps;
 // helpers
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ float bf2f(uint32_t h16) { return __uint_as_float(h16 << 16); }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
 // streaming read-only load of weights: never written while a frame runs
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
@@ -52,17 +51,6 @@ __device__ __forceinline__ uint2 ld_stream8(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
 // barrier of the compute warps only (the producer warp never joins it)
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory"); }
 __device__ __forceinline__ int cbar_or(int pred) {
@@ -75,13 +63,6 @@ __device__ __forceinline__ int cbar_or(int pred) {
   return r;
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ int read_err(const int* e) { return *(const volatile int*)e; }
-__device__ __forceinline__ void set_err(int* e, int code) { atomicCAS(e, 0, code); }
 
 // Time limit of every wait for another CTA's data or for weights (default
 // 2 s: a frame takes milliseconds; qtts_set_option can shorten it), copied
@@ -290,19 +271,11 @@ __device__ __forceinline__ void trace_mark(const Globals& g, int which) {
 
 // ---- mbarriers and TMA bulk copies into shared memory ----
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 __device__ __forceinline__ void mbar_inval(uint64_t* bar) {
   asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 // L2 policy for data read once per frame (weights, KV): evict it first, so
 // it streams through L2 without displacing the small data every stage reuses
@@ -324,27 +297,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // generic-proxy global writes (KV appends) become visible to later bulk copies
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// The same test, but a thread that finds the phase incomplete is suspended
-// until it completes or about `ns` nanoseconds pass: no issue slots are spent
-// spinning (the producer warp shares its SM sub-partition with compute warps).
-__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
 constexpr uint32_t kSuspendNs = 20000;  // recheck the error word and the time limit this often
 
 // Wait for a copy or MMA this CTA issued itself to complete before leaving
@@ -372,33 +324,9 @@ __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   return true;
 }
 
-// ---- 5th-generation tensor cores: tcgen05 MMA with TMEM accumulators ----
-// Operands sit in shared memory in the canonical K-major layout without
-// swizzle: 8 rows x 16 bytes per core matrix, `lbo` bytes between core
-// matrices along K, `sbo` bytes between them along M (or N).
+// ---- 5th-generation tensor cores: the TMEM accumulator (operand
+// descriptors and MMA issue: device_util.cuh) ----
 
-__device__ __forceinline__ uint64_t tc_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);  // descriptor version 1, no swizzle
-}
-// kind::f16 instruction: fp32 accumulator, bf16 A and B, both K-major, M x N
-__host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
-          d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc)
-      : "memory");
-}
-// arrive once on `bar` when every MMA this thread issued so far has completed
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 constexpr uint32_t kTmemCols = 128;  // the accumulator: 128 lanes (weight rows) x up to 128 columns
 // one warp
 __device__ __forceinline__ void tc_alloc(uint32_t* dst) {
@@ -1778,7 +1706,6 @@ __device__ __noinline__ bool stage_gemv(const StageDesc& d, uint32_t tag, const 
     RT = RT >= 8 ? 8 : RT >= 4 ? 4 : RT >= 2 ? 2 : 1;
     while (RT > 1 && RT / 2 >= rows) RT /= 2;
   }
-  const RowMap rm{d.rps, d.in_rps, d.in_off};
   const Seg& s0 = d.seg[0];
   const bool has_resid = s0.epi == E_RESID;  // single-segment stage
   const SegShare sh0(s0, K);

@@ -29,79 +29,29 @@
 #include <algorithm>
 
 #include "qtts_internal.h"
+#include "device_util.cuh"
 
 namespace qtts {
 
 namespace {
 
-// ---- small device helpers (this translation unit's own) ----
+// ---- device helpers of this translation unit (the shared ones: device_util.cuh) ----
 
-__device__ __forceinline__ float bf2f(uint32_t h16) { return __uint_as_float(h16 << 16); }
-__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
-__device__ __forceinline__ uint64_t gtimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ int err_now(const int* e) { return *(const volatile int*)e; }
-__device__ __forceinline__ void err_set(int* e, int code) { atomicCAS(e, 0, code); }
-__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(n) : "memory");
-}
-__device__ __forceinline__ void bar_expect(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(saddr(b)), "r"(parity), "r"(20000u)
-      : "memory");
-  return ok != 0;
-}
 // Wait for phase `parity` of `b`, at most `ns` nanoseconds.
 __device__ bool bar_wait(uint64_t* b, uint32_t parity, uint64_t ns) {
-  if (bar_try(b, parity)) return true;
-  const uint64_t t0 = gtimer_ns();
-  while (!bar_try(b, parity))
-    if (gtimer_ns() - t0 > ns) return false;
+  if (mbar_test_sleep(b, parity, 20000u)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test_sleep(b, parity, 20000u))
+    if (global_timer_ns() - t0 > ns) return false;
   return true;
 }
 // global -> shared bulk copy, completing `bytes` of the barrier's transaction
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   saddr(dst)),
-               "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(saddr(b))
+                   smem_addr(dst)),
+               "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(b))
                : "memory");
 }
-
-// tcgen05: K-major canonical operand layout without swizzle (core matrices of
-// 8 rows x 16 bytes; lbo = bytes between core matrices along K, sbo along the
-// rows), descriptor version 1
-__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
-}
-// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, both K-major
-constexpr uint32_t umma_idesc(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
-          d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* b) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(b))
-               : "memory");
-}
-__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
 // ---- GEMM operand tiles ----
 // Activations: [m tile of 128 rows][32-wide K chunk][hi | lo] images; weights
@@ -187,25 +137,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
   const int units = a.Nt * a.Mt * a.S;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      bar_init(&full[i], 1);
-      bar_init(&empty[i], 1);
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      bar_init(&acc_full[i], 1);
-      bar_init(&acc_empty[i], 4);  // one lane of each epilogue warp
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);  // one lane of each epilogue warp
     }
     failed = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
                  "n"(2 * kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  tc_before();
+  tc_fence_before();
   __syncthreads();
-  tc_after();
+  tc_fence_after();
   const uint32_t tmem = tmem_base;
   int consumed = 0;   // MMA thread: ring uses whose copies it waited for
   int issued_mma = 0; // MMA thread: units whose MMAs it issued
@@ -224,55 +174,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
       for (int i = 0; i < nk; ++i, ++it) {
         const int st = it % kStages, use = it / kStages;
         if (use > 0 && !bar_wait(&empty[st], (use - 1) & 1, a.wait_ns)) {
-          err_set(a.err, QTTS_DEV_TIMEOUT);
+          set_err(a.err, QTTS_DEV_TIMEOUT);
           failed = 1;
           break;
         }
         unsigned char* base = smem + st * kStageBytes;
         const int kc = kc0 + i;
-        bar_expect(&full[st], kStageBytes);
+        mbar_arrive_expect_tx(&full[st], kStageBytes);
         bulk_g2s(base, a.A + (size_t)(mt * a.KC + kc) * 2 * kAImg, 2 * kAImg * 2, &full[st]);
         bulk_g2s(base + 2 * kAImg * 2, a.W + (size_t)(nt * a.KC + kc) * kWImg, kWImg * 2, &full[st]);
       }
     }
   } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = umma_idesc(kBM, kBN);
+    constexpr uint32_t idesc = tc_idesc_bf16(kBM, kBN);
     int it = 0, j = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
       const int buf = j & 1;
       const uint32_t acc = tmem + (uint32_t)(buf * kTmemCols);
       // the epilogue has drained this accumulator (unit j - 2)
       if (j >= 2 && !bar_wait(&acc_empty[buf], ((j >> 1) - 1) & 1, a.wait_ns)) {
-        err_set(a.err, QTTS_DEV_TIMEOUT);
+        set_err(a.err, QTTS_DEV_TIMEOUT);
         failed = 1;
         break;
       }
-      tc_after();
+      tc_fence_after();
       int kc0, nk;
       unit_k(u, kc0, nk);
       bool ok = true;
       for (int i = 0; i < nk; ++i, ++it) {
         const int st = it % kStages, use = it / kStages;
         if (!bar_wait(&full[st], use & 1, a.wait_ns)) {
-          err_set(a.err, QTTS_DEV_TIMEOUT);
+          set_err(a.err, QTTS_DEV_TIMEOUT);
           failed = 1;
           ok = false;
           break;
         }
-        tc_after();
-        const uint32_t base = saddr(smem + st * kStageBytes);
+        tc_fence_after();
+        const uint32_t base = smem_addr(smem + st * kStageBytes);
 #pragma unroll
         for (int ks = 0; ks < kBK / 16; ++ks) {
-          const uint64_t dhi = umma_desc(base + ks * 2 * (kBM * 16), kBM * 16, 128);
-          const uint64_t dlo = umma_desc(base + kAImg * 2 + ks * 2 * (kBM * 16), kBM * 16, 128);
-          const uint64_t dw = umma_desc(base + 2 * kAImg * 2 + ks * 2 * (kBN * 16), kBN * 16, 128);
-          umma(acc, dhi, dw, idesc, (i > 0 || ks > 0) ? 1u : 0u);
-          umma(acc, dlo, dw, idesc, 1u);
+          const uint64_t dhi = tc_smem_desc(base + ks * 2 * (kBM * 16), kBM * 16, 128);
+          const uint64_t dlo = tc_smem_desc(base + kAImg * 2 + ks * 2 * (kBM * 16), kBM * 16, 128);
+          const uint64_t dw = tc_smem_desc(base + 2 * kAImg * 2 + ks * 2 * (kBN * 16), kBN * 16, 128);
+          tc_mma(acc, dhi, dw, idesc, i > 0 || ks > 0);
+          tc_mma(acc, dlo, dw, idesc, true);
         }
         consumed = it + 1;
-        umma_commit(&empty[st]);
+        tc_commit(&empty[st]);
       }
-      umma_commit(&acc_full[buf]);  // also after a failure: completes once the issued MMAs have
+      tc_commit(&acc_full[buf]);  // also after a failure: completes once the issued MMAs have
       issued_mma = j + 1;
       if (!ok) break;
     }
@@ -286,11 +236,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
       const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // one verdict per warp: the loads are warp-wide
       __syncwarp();
       if (!ok) {
-        err_set(a.err, QTTS_DEV_TIMEOUT);
+        set_err(a.err, QTTS_DEV_TIMEOUT);
         failed = 1;
         break;
       }
-      tc_after();
+      tc_fence_after();
       const int nt = u % a.Nt, mt = (u / a.Nt) % a.Mt, s = u / (a.Nt * a.Mt);
       const int row = mt * kBM + q * 32 + lane;
       const bool store = row < a.M;
@@ -311,12 +261,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
             *reinterpret_cast<uint4*>(o + c * 16 + 4 * jj) =
                 make_uint4(r[4 * jj], r[4 * jj + 1], r[4 * jj + 2], r[4 * jj + 3]);
       }
-      tc_before();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&acc_empty[buf])) : "memory");
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acc_empty[buf])) : "memory");
     }
   }
-  tc_before();
+  tc_fence_before();
   __syncthreads();
   if (failed) {
     // nothing may land in shared memory or TMEM after the CTA is gone: wait
@@ -331,7 +281,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
   }
   if (warp == 0) {
     __syncwarp();
-    tc_after();
+    tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(2 * kTmemCols) : "memory");
   }
 }
@@ -448,7 +398,7 @@ struct QkvArgs {
 // i + d/2 of one q or k head), then v in pairs of adjacent dims. A thread
 // takes 8 columns (4 pairs) at a time: all in one head.
 __global__ void __launch_bounds__(kRowThreads) qkv_kernel(QkvArgs a) {
-  if (err_now(a.err)) return;  // the chunk's sessions failed validation
+  if (read_err(a.err)) return;  // the chunk's sessions failed validation
   const int r = blockIdx.x, b = r % a.B, p = r / a.B;
   const int pos = a.sess[b].kv_len + p;
   const int half = a.d / 2;
@@ -456,7 +406,7 @@ __global__ void __launch_bounds__(kRowThreads) qkv_kernel(QkvArgs a) {
   const int ncol = (a.nq + 2 * a.nkv) * a.d;
   int page = a.bt[(size_t)b * a.bt_stride + pos / kPage];
   if (page < 0 || page >= a.pool_pages) {  // checked before the chunk; stay in bounds regardless
-    err_set(a.err, QTTS_DEV_BAD_PAGE);
+    set_err(a.err, QTTS_DEV_BAD_PAGE);
     return;
   }
   const size_t kvrow = (size_t)(pos % kPage) * a.d;
@@ -617,7 +567,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   constexpr int NKS = HD / 16;  // k steps of Q K^T; pairs of 8-wide dim tiles of P V
   constexpr int NDT = HD / 8;   // 8-wide output dim tiles
   extern __shared__ __align__(16) uint16_t kvs[];  // [2 buffers][K | V][kAttnKT][LD]
-  if (err_now(a.err)) return;
+  if (read_err(a.err)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int b = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
@@ -660,7 +610,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   for (int j = 0; j < NDT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
-  const uint32_t sbase = saddr(kvs);
+  const uint32_t sbase = smem_addr(kvs);
   const int t_begin = chunk * (kAttnChunk / kAttnKT);
   const int t_end = min((npos + kAttnKT - 1) / kAttnKT, t_begin + kAttnChunk / kAttnKT);
   auto load_tile = [&](int t, int buf) {
@@ -832,7 +782,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_kernel(AttnArgs a)
   uint16_t* ks = reinterpret_cast<uint16_t*>(dsm);                                       // [warps][32][LDK]
   float* qs = reinterpret_cast<float*>(dsm + kDecWarps * 32 * LDK * 2);                 // [2][HD]
   float* st = qs + 2 * HD;                                                              // [warps][2][HD + 4]
-  if (err_now(a.err)) return;
+  if (read_err(a.err)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
   const int grp = a.nq / a.nkv;  // 1 or 2
@@ -980,7 +930,7 @@ struct CombineArgs {
 // O of row r and every q head: the chunks' partial states merged in chunk
 // order (max of the maxima, weights 2^(m_c - m)), packed as hi + lo
 __global__ void __launch_bounds__(kRowThreads) attn_combine_kernel(CombineArgs a) {
-  if (err_now(a.err)) return;
+  if (read_err(a.err)) return;
   const int r = blockIdx.x, b = r % a.B, p = r / a.B;
   const int nc = (a.sess[b].kv_len + p + 1 + kAttnChunk - 1) / kAttnChunk;  // chunks holding this row's positions
   for (int u = threadIdx.x; u < a.nq * a.d / 8; u += kRowThreads) {
@@ -1025,13 +975,13 @@ __global__ void check_kernel(const qtts_session* sess, const int32_t* bt, int bt
   for (int b = blockIdx.x; b < B; b += gridDim.x) {
     const int kv = sess[b].kv_len;
     if (kv < 0 || kv + P > max_context || kv + P > bt_stride * kPage) {
-      if (threadIdx.x == 0) err_set(err, QTTS_DEV_BAD_SESSION);
+      if (threadIdx.x == 0) set_err(err, QTTS_DEV_BAD_SESSION);
       continue;
     }
     const int np = (kv + P + kPage - 1) / kPage;
     for (int i = threadIdx.x; i < np; i += blockDim.x) {
       const int page = bt[(size_t)b * bt_stride + i];
-      if (page < 0 || page >= pool_pages) err_set(err, QTTS_DEV_BAD_PAGE);
+      if (page < 0 || page >= pool_pages) set_err(err, QTTS_DEV_BAD_PAGE);
     }
   }
 }
