@@ -1038,7 +1038,7 @@ static int pf_splits(int tiles, int KC, int G, size_t cap) {
   const size_t tile_floats = (size_t)kBM * kBN;
   int best = 1;
   long long best_cost = (long long)((tiles + G - 1) / G) * KC;
-  for (int S = 2; S <= 16 && S <= KC; ++S) {
+  for (int S = 2; S <= 8 && S <= KC; ++S) {  // more slices measured slower (partial sums to write and re-read)
     if ((size_t)S * tiles * tile_floats > cap) break;
     const long long cost = (long long)((tiles * S + G - 1) / G) * ((KC + S - 1) / S);
     if (cost < best_cost) {
