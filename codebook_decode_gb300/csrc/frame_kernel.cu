@@ -13,7 +13,7 @@
 // The pages' engines replay ~1,600 kernels per frame as a CUDA graph; here the
 // whole frame is one launch.
 //
-// Inside a CTA, warps 0..14 compute and warp 15 is a producer: it walks the
+// Inside a CTA, warps 0..10 compute and warp 11 is a producer: it walks the
 // same stage program and streams this CTA's share of every upcoming weight
 // matrix into a ring of shared-memory slots with TMA bulk copies, running
 // ahead across stage boundaries (weights do not depend on activations), so
