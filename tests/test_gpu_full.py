@@ -61,13 +61,14 @@ def test_full_b8_bf16(full_w, oracle_bf16):
         free(run)
 
 
-@pytest.mark.parametrize("chunk_talker", [8, 33])
-def test_full_b32_bf16_ragged_staggered(full_w, oracle_bf16, chunk_talker):
-    """B=32, prefixes uniform in [100, 1000] plus staggered offsets 0..200
-    (history pre-filled, frame counters at the offset); the Talker on the
-    chunk kernels (option at 8) and in the frame kernel (33, the default)."""
-    s = synth.make_sessions(configs.WORKLOADS["full_b32"], frames=1)
-    run = ParityRun(FULL, full_w, s, 1, oracle=oracle_bf16, chunk_talker_min_b=chunk_talker).run()
+@pytest.mark.parametrize("chunk_talker,frames", [(33, 8), (8, 1)])
+def test_full_b32_bf16_ragged_staggered(full_w, oracle_bf16, chunk_talker, frames):
+    """Config 3's first window: B=32, prefixes uniform in [100, 1000] plus
+    staggered offsets 0..200 (history pre-filled, frame counters at the
+    offset), frames 0..7 with the Talker in the frame kernel (the default),
+    frame 0 with it on the chunk kernels (option at 8)."""
+    s = synth.make_sessions(configs.WORKLOADS["full_b32"], frames=frames)
+    run = ParityRun(FULL, full_w, s, frames, oracle=oracle_bf16, chunk_talker_min_b=chunk_talker).run()
     try:
         check(run, TOL_BF16)
     finally:
@@ -93,8 +94,9 @@ def test_full_int8_b1_and_export(full_w, oracle_int8):
 
 
 def test_full_int8_b32(full_w, oracle_int8):
-    s = synth.make_sessions(configs.WORKLOADS["int8_b32"], frames=1)
-    run = ParityRun(FULL, full_w, s, 1, int8=True, oracle=oracle_int8).run()
+    """Config 4's first window at B=32: frames 0..7, INT8 weights."""
+    s = synth.make_sessions(configs.WORKLOADS["int8_b32"], frames=8)
+    run = ParityRun(FULL, full_w, s, 8, int8=True, oracle=oracle_int8).run()
     try:
         check(run, TOL_INT8)
     finally:
