@@ -59,8 +59,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // element (r, k) at ((k / 8) * R / 8 + r / 8) * 64 + (r % 8) * 8 + k % 8.
 constexpr int kBM = 128, kBN = 256, kBK = 32, kStages = 6;
 // 32-wide K chunks in 6 stages keep 5 x 32 KB of copies in flight per SM
-// while one stage feeds the MMAs (64-wide chunks in 3 stages: 2 x 64 KB,
-// which measured ~1.6x slower per chunk)
+// while one stage feeds the MMAs (64-wide chunks in 3 stages, 2 x 64 KB in
+// flight, measured as fast)
 constexpr int kAImg = kBM * kBK;                    // elements of one hi or lo image (8 KB)
 constexpr int kWImg = kBN * kBK;                    // 16 KB
 constexpr int kStageBytes = (2 * kAImg + kWImg) * 2;  // 32 KB
@@ -312,7 +312,7 @@ struct NormArgs {
   int S, Mpad, Npad;
   const uint16_t* gain;  // RMSNorm gain [H] (nullptr: no norm, no packing)
   float eps;
-  int H, KC;             // K chunks of the packed rows (H rounded up to 64)
+  int H, KC;             // K chunks of the packed rows (H rounded up to whole chunks)
   uint16_t* A;
 };
 
