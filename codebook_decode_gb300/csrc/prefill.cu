@@ -128,8 +128,11 @@ struct GemmArgs {
   unsigned long long wait_ns;
 };
 
+constexpr int kEpiLd = 33;  // floats per row of an epilogue transpose tile (conflict-free both ways)
+
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ float epi[4][32 * kEpiLd];  // one 32 x 32 transpose tile per epilogue warp
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
   __shared__ int failed;
@@ -242,24 +245,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
       }
       tc_fence_after();
       const int nt = u % a.Nt, mt = (u / a.Nt) % a.Mt, s = u / (a.Nt * a.Mt);
-      const int row = mt * kBM + q * 32 + lane;
-      const bool store = row < a.M;
-      float* o = a.out + ((size_t)s * a.Mpad + row) * a.Npad + (size_t)nt * kBN;
+      const int row0 = mt * kBM + q * 32;  // this warp's 32 rows
       const uint32_t acc = tmem + (uint32_t)(buf * kTmemCols) + ((uint32_t)(q * 32) << 16);
+      float* tile = epi[q];
+      // 32 columns at a time: lane = row out of TMEM, through shared memory,
+      // then four rows of 128 bytes per store instruction
 #pragma unroll 1
-      for (int c = 0; c < kBN / 16; ++c) {
-        uint32_t r[16];
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
               "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(acc + (uint32_t)(c * 16)));
+            : "r"(acc + (uint32_t)(c * 32)));
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+              "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+              "=r"(r[30]), "=r"(r[31])
+            : "r"(acc + (uint32_t)(c * 32 + 16)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (store)
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            *reinterpret_cast<uint4*>(o + c * 16 + 4 * jj) =
-                make_uint4(r[4 * jj], r[4 * jj + 1], r[4 * jj + 2], r[4 * jj + 3]);
+        for (int j = 0; j < 32; ++j) tile[lane * kEpiLd + j] = __uint_as_float(r[j]);
+        __syncwarp();
+#pragma unroll
+        for (int pass = 0; pass < 8; ++pass) {
+          const int rr = pass * 4 + (lane >> 3), cc = (lane & 7) * 4;
+          if (row0 + rr < a.M) {
+            const float* t = tile + rr * kEpiLd + cc;
+            *reinterpret_cast<float4*>(a.out + ((size_t)s * a.Mpad + row0 + rr) * a.Npad + (size_t)nt * kBN + c * 32 +
+                                       cc) = make_float4(t[0], t[1], t[2], t[3]);
+          }
+        }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
