@@ -14,7 +14,8 @@
 //   qkv      RoPE; K and V rounded to bf16 into the sessions' pages; q kept
 //   attn     causal attention over each session's pages, packed hi + lo
 //   gemm     O, then norm adds it to the residual and normalises
-//   gemm     gate/up, then swiglu packs silu(gate) x up
+//   gemm     gate/up, then swiglu packs silu(gate) x up (or, with one
+//            K-slice, the GEMM's epilogue does, into a second input buffer)
 //   gemm     down, then norm adds it and applies the next layer's input norm
 // The last layer stops after its K/V: nothing after them is observable.
 //
@@ -123,6 +124,11 @@ struct GemmArgs {
   float* out;  // [S][Mpad][Npad]
   int KC, S, Mpad, Npad;
   int M;       // rows with data: the epilogue stores no partial sums of rows past it
+  // act != nullptr (one K-slice; columns 2j, 2j + 1 = gate j, up j): the
+  // epilogue writes silu(gate) x up as the next GEMM's packed hi + lo input
+  // (KCa 32-wide chunks) instead of partial sums
+  uint16_t* act;
+  int KCa;
   int Nt, Mt;  // tiles: units = Nt Mt S, unit u = (u % Nt, u / Nt % Mt, u / (Nt Mt))
   int* err;
   unsigned long long wait_ns;
@@ -265,6 +271,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(GemmArgs a) {
               "=r"(r[30]), "=r"(r[31])
             : "r"(acc + (uint32_t)(c * 32 + 16)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (a.act) {
+          // this row's 16 SwiGLU outputs, k = (n tile columns) / 2: a lane per
+          // row writes 16 bytes of its core-matrix row, the warp 512 bytes
+          const int k0 = (nt * kBN + c * 32) / 2;
+          if (row0 + lane < a.M && k0 < a.KCa * kBK) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float g = __uint_as_float(r[16 * h + 2 * e]);
+                v[e] = g / (1.0f + expf(-g)) * __uint_as_float(r[16 * h + 2 * e + 1]);
+              }
+              put8(a.act, row0 + lane, k0 + 8 * h, a.KCa, v);
+            }
+          }
+          __syncwarp();  // converged for the next warp-wide TMEM load
+          continue;
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) tile[lane * kEpiLd + j] = __uint_as_float(r[j]);
         __syncwarp();
@@ -1067,6 +1092,16 @@ static int pf_splits(int tiles, int KC, int G, size_t cap) {
   return best;
 }
 
+// SwiGLU in the gate/up GEMM's epilogue (one K-slice) or a pass over the S
+// slices' partial sums: the pass re-reads S x tiles of partial sums, charged
+// here in chunk-times at ~3 MB of HBM traffic each (one 32-wide step of a
+// 128 x 256 tile took ~0.46 us in the 512-row GEMMs, HBM moves ~6.7 TB/s)
+static bool pf_fuse_swiglu(int tiles, int KC, int G, int S) {
+  const double one = (double)((tiles + G - 1) / G) * KC;
+  const double split = (double)((tiles * S + G - 1) / G) * ((KC + S - 1) / S);
+  return one <= split + (double)S * tiles * kBM * kBN * 4 / 3.0e6;
+}
+
 // The Talker layers over B x P rows. decode: the whole last layer too, its
 // output rows (the residual stream) left in c.x; else the last layer stops
 // after its K/V.
@@ -1078,11 +1113,12 @@ static cudaError_t pf_layers(const PfCtx& c, int B, int P, const qtts_session* s
   const int KH = (c.H + kBK - 1) / kBK, KA = (c.nq * c.d + kBK - 1) / kBK, KF = (c.F + kBK - 1) / kBK;
   check_kernel<<<std::min(B, 32), 128, 0, s>>>(sess, bt, bt_stride, B, P, c.max_context, c.pool_pages, c.err);
   int S = 1, Npad = 0;
-  auto gemm = [&](const uint16_t* W, int N, int K) {
+  auto gemm = [&](const uint16_t* W, int N, int K, const uint16_t* Ain = nullptr, uint16_t* act = nullptr,
+                  int KCa = 0) {
     const int Nt = (N + kBN - 1) / kBN, KC = (K + kBK - 1) / kBK;
-    S = pf_splits(Nt * Mt, KC, c.G, c.part_floats);
+    S = act ? 1 : pf_splits(Nt * Mt, KC, c.G, c.part_floats);
     Npad = Nt * kBN;
-    GemmArgs ga{c.A, W, c.part, KC, S, Mpad, Npad, M, Nt, Mt, c.err, c.wait_ns};
+    GemmArgs ga{Ain ? Ain : c.A, W, c.part, KC, S, Mpad, Npad, M, act, KCa, Nt, Mt, c.err, c.wait_ns};
     gemm_kernel<<<std::min(Nt * Mt * S, c.G), kGemmThreads, kGemmSmem, s>>>(ga);
   };
   auto norm = [&](const uint16_t* emb, bool add, const uint16_t* gain) {
@@ -1093,6 +1129,8 @@ static cudaError_t pf_layers(const PfCtx& c, int B, int P, const qtts_session* s
   const int grp = c.nq / c.nkv;
   const int tpc = kAttnWarps * (16 / grp);  // prompt tokens per attention CTA
   const int maxc = pf_attn_chunks(c.max_context);
+  const int gu_tiles = (2 * c.F + kBN - 1) / kBN * Mt;
+  const bool fuse = pf_fuse_swiglu(gu_tiles, KH, c.G, pf_splits(gu_tiles, KH, c.G, c.part_floats));
   for (int l = 0; l < c.n_layers; ++l) {
     const PfLayer& L = c.layers[l];
     gemm(L.qkv, (c.nq + 2 * c.nkv) * c.d, c.H);
@@ -1118,10 +1156,15 @@ static cudaError_t pf_layers(const PfCtx& c, int B, int P, const qtts_session* s
     attn_combine_kernel<<<M, kRowThreads, 0, s>>>(ca);
     gemm(L.o, c.H, c.nq * c.d);
     norm(nullptr, true, L.post_norm);
-    gemm(L.gu, 2 * c.F, c.H);
-    SwigluArgs sa{c.part, S, Mpad, Npad, c.F, KF, c.A};
-    swiglu_kernel<<<M, kRowThreads, 0, s>>>(sa);
-    gemm(L.down, c.H, c.F);
+    if (fuse) {  // silu(gate) x up straight into the second input buffer
+      gemm(L.gu, 2 * c.F, c.H, nullptr, c.A2, KF);
+      gemm(L.down, c.H, c.F, c.A2);
+    } else {
+      gemm(L.gu, 2 * c.F, c.H);
+      SwigluArgs sa{c.part, S, Mpad, Npad, c.F, KF, c.A};
+      swiglu_kernel<<<M, kRowThreads, 0, s>>>(sa);
+      gemm(L.down, c.H, c.F);
+    }
     norm(nullptr, true, last ? nullptr : c.layers[l + 1].in_norm);  // last: the residual add alone
   }
   return cudaGetLastError();

@@ -685,6 +685,7 @@ int build_prefill(qtts_model* m) {
   AL(m, p.x, (size_t)kPfMaxRows * c.hidden);
   AL(m, p.q, (size_t)kPfMaxRows * c.n_q_heads * c.head_dim);
   AL(m, p.A, pf_act_elems(kPfMaxRows, maxK));
+  AL(m, p.A2, pf_act_elems(kPfMaxRows, c.ffn));
   AL(m, p.part, p.part_floats);
   AL(m, p.po, pf_attn_floats(kPfMaxRows, c.n_q_heads, c.head_dim, c.max_context));
   CK(m, cudaDeviceSynchronize());

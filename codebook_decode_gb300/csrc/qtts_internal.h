@@ -240,6 +240,7 @@ struct PfCtx {
   float* x;                 // [kPfMaxRows][H]
   float* q;                 // [kPfMaxRows][nq d]
   uint16_t* A;              // pf_act_elems(kPfMaxRows, max(H, nq d, F))
+  uint16_t* A2;             // pf_act_elems(kPfMaxRows, F): the down GEMM's input when gate/up applies SwiGLU
   float* part;              // part_floats
   size_t part_floats;
   float* po;                // attention partials: pf_attn_floats(kPfMaxRows, nq, d, max_context)

@@ -38,12 +38,14 @@ def test_frames_match_oracle(dims, B):
 
 
 @pytest.mark.parametrize("dims", [ODD, GQA1], ids=["odd_widths", "gqa_group_1"])
-def test_prefill_matches_oracle(dims):
+@pytest.mark.parametrize("n_tok", [37, 320])
+def test_prefill_matches_oracle(dims, n_tok):
+    """2 x 320 rows: one K-slice per gate/up tile, SwiGLU in its epilogue."""
     w = synth.make_weights(dims, 1101)
-    s = sessions(dims, 2, [9, 30], 40)
-    run = ParityRun(dims, w, s, 39, shuffle=True)
+    s = sessions(dims, 2, [9, 30], n_tok + 3)
+    run = ParityRun(dims, w, s, n_tok + 2, shuffle=True)
     try:
-        e = s.prompt_embeds(37)
+        e = s.prompt_embeds(n_tok)
         run.eng.prefill(to_dev_u16(e, run.eng.dev))
         assert run.eng.status() == (0, 0)
         run.O.talker_prefill(run.rows, run.kv, run.cap, e)
