@@ -1093,13 +1093,15 @@ static int pf_splits(int tiles, int KC, int G, size_t cap) {
 }
 
 // SwiGLU in the gate/up GEMM's epilogue (one K-slice) or a pass over the S
-// slices' partial sums: the pass re-reads S x tiles of partial sums, charged
-// here in chunk-times at ~3 MB of HBM traffic each (one 32-wide step of a
-// 128 x 256 tile took ~0.46 us in the 512-row GEMMs, HBM moves ~6.7 TB/s)
+// slices' partial sums: the split writes S x tiles of partial sums and the
+// pass re-reads them, charged here in chunk-times at ~3 MB of HBM traffic
+// each (one 32-wide step of a 128 x 256 tile took ~0.46 us in the 512-row
+// GEMMs, HBM moves ~6.7 TB/s). At 512 full-width rows (128 against 96 + 34)
+// the single slice measured 2-3 % faster.
 static bool pf_fuse_swiglu(int tiles, int KC, int G, int S) {
   const double one = (double)((tiles + G - 1) / G) * KC;
   const double split = (double)((tiles * S + G - 1) / G) * ((KC + S - 1) / S);
-  return one <= split + (double)S * tiles * kBM * kBN * 4 / 3.0e6;
+  return one <= split + 2.0 * S * tiles * kBM * kBN * 4 / 3.0e6;
 }
 
 // The Talker layers over B x P rows. decode: the whole last layer too, its
