@@ -197,8 +197,8 @@ int qtts_kv_read(qtts_model* m, int layer, int n_tok, const int32_t* pages_host,
  * later, in stream order, so they must stay valid and unmodified until the
  * stream has run the copies. The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress, in the device's primary context, which
- * is the context every later call uses); make that first call before any
- * stream capture. The caller's current device is left as it was. All calls
+ * is the context every later call uses). The caller's current device is left
+ * as it was. All calls
  * share the one array, so calls whose work overlaps on the GPU (different
  * streams, no ordering between them) race. */
 int qtts_kv_write_noalloc(qtts_model* m, int layer, int n_tok, const int32_t* pages_host, const uint16_t* k,
